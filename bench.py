@@ -1,0 +1,513 @@
+#!/usr/bin/env python
+"""Benchmark of the INT8 KV cache decode step on GB300.
+
+One step = the whole hot path over one batch of synthetic input: append one
+new token (fp16 -> int8 codes + fp16 scales, written through the page table)
+and split-K GQA decode attention over the dequantized cache with the per-head
+combine.  Workload: batch 1, 16 query heads, 2 kv heads, head_dim 256, one
+fp16 scale per 64 values, context 8192 (8191 cached + the appended token),
+k8v8 store, K with 4 outlier channels per kv head (x20).
+
+Inputs are resident in HBM when the timed region starts.  The pool is
+replicated into enough copies (each step uses the next copy) that the bytes a
+step reads were not left in L2 by the previous steps.  Steps are replayed
+from a CUDA graph and timed with CUDA events on the launching stream.
+
+Lines printed (rank 0, one JSON object):
+  default            this library; ``value`` = algorithmic bytes per step /
+                     device time per step (GB/s), plus ``e2e`` (the same metric
+                     through the public API with pinned host buffers copied in
+                     and the result copied out every step), ``roofline`` of the
+                     decode kernel, ``cpu_baseline`` (the oracle on this host),
+                     and ``extra`` (128K-context decode, k8v8 and k8v16).
+  --impl reference   the oracle timed on the host cores on a bounded sample
+                     of the same workload.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("INT8-KV decode attn: achieved HBM GB/s (% of ~8 TB/s), μs/step at "
+          "8K–128K ctx")
+WORKLOAD = ("decode step (append 1 token + split-K GQA decode + combine): batch 1, 16 q heads, "
+            "2 kv heads, head_dim 256, fp16 scale per 64 values, ctx 8192, k8v8, outlier K "
+            "channels")
+
+B, H, HKV, D, GS, PS, CTX = 1, 16, 2, 256, 64, 64, 8192
+
+
+def step_bytes(ctx=CTX, hkv=HKV, h=H, d=D, gs=GS, k_int8=True, v_int8=True, append=True):
+    """Algorithmic bytes of one step: int8 KV + scales (fp16 for an fp16 store)
+    read once, q (fp16) read, O (fp32) written, and the appended token
+    (fp16 in, codes + scales out)."""
+    per_pos = 0
+    for is8 in (k_int8, v_int8):
+        per_pos += hkv * d + hkv * (d // gs) * 2 if is8 else hkv * d * 2
+    n = ctx * per_pos + h * d * 2 + h * d * 4
+    if append:
+        n += 2 * hkv * d * 2 + per_pos
+    return n
+
+
+def decode_bytes(**kw):
+    return step_bytes(append=False, **kw)
+
+
+# --------------------------------------------------------------------------- helpers
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) >= 9 and f[1].replace(".", "").isdigit():
+                    rows.append(f)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(float(r[2]) for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- device state
+class DecodeState:
+    """R copies of the workload's pool (one physical page range per copy)."""
+
+    def __init__(self, w, ctx, variant, copies, append_token=True):
+        import torch
+
+        from int8_kv_cache_02_gb300 import binding, inputs
+        self.torch, self.binding = torch, binding
+        self.ctx, self.copies = ctx, copies
+        n_pages_copy = -(-ctx // PS)
+        hkv, d, gs = w["Hkv"], w["D"], w["gs"]
+        self.h = w["H"]
+        self.pool = binding.KVPool(1, hkv, d, gs, PS, n_pages_copy * copies, variant)
+        pts = []
+        for c in range(copies):
+            pt, _ = inputs.page_table([ctx], PS, n_pages_total=n_pages_copy * copies, seed=100 + c)
+            pts.append(pt)
+        self.pt = torch.cat(pts).cuda()                      # [copies][pages]
+        n_cached = ctx - 1 if append_token else ctx
+        kd = w["k"][:n_cached].reshape(1, n_cached, hkv, d).cuda()
+        vd = w["v"][:n_cached].reshape(1, n_cached, hkv, d).cuda()
+        zero = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for c in range(copies):
+            binding.kv_quant_append(self.pool, 0, kd, vd, zero, self.pt[c:c + 1])
+        del kd, vd
+        self.k_new = w["k"][ctx - 1:ctx].reshape(1, 1, hkv, d).cuda()
+        self.v_new = w["v"][ctx - 1:ctx].reshape(1, 1, hkv, d).cuda()
+        self.pos = torch.tensor([ctx - 1], dtype=torch.int32, device="cuda")
+        self.lens = torch.tensor([ctx], dtype=torch.int32, device="cuda")
+        self.q = w["q"].cuda()
+        self.out = torch.zeros((1, self.h, d), dtype=torch.float32, device="cuda")
+        self.n_splits = binding.attn_decode_n_splits(1, hkv, ctx, PS)
+        self.ws = self.pool.decode_workspace(1, self.h, self.n_splits)
+        self.append_token = append_token
+        torch.cuda.synchronize()
+
+    def step(self, c, append=True, decode=True):
+        b = self.binding
+        pt = self.pt[c:c + 1]
+        if append and self.append_token:
+            b.kv_quant_append(self.pool, 0, self.k_new, self.v_new, self.pos, pt)
+        if decode:
+            b.attn_decode_int8(self.pool, 0, self.q, self.lens, pt, self.out, self.ws,
+                               n_splits=self.n_splits)
+
+    def graph(self, n_steps, start=0, append=True, decode=True):
+        torch = self.torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for i in range(3):                               # eager warm-up on the capture stream
+                self.step((start + i) % self.copies, append, decode)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n_steps):
+                self.step((start + i) % self.copies, append, decode)
+        torch.cuda.synchronize()
+        return g
+
+
+def time_graph(g):
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def l2_bytes():
+    import torch
+    try:
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        return 129 * 2 ** 20
+
+
+def copies_for(bytes_per_copy):
+    return max(2, math.ceil(2 * l2_bytes() / bytes_per_copy) + 1)
+
+
+def traffic_from_profiles(kernel_src_sha):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_grouped8k.md")
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    sha = val = None
+    for line in txt.splitlines():
+        if line.startswith("kernel source sha256:"):
+            sha = line.split(":", 1)[1].strip()
+        if line.startswith("dram bytes per launch:"):
+            val = float(line.split(":", 1)[1].strip())
+    return val if sha == kernel_src_sha and val is not None else None
+
+
+def decode_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "int8_kv_cache_02_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        if n.startswith("decode") or n in ("common.cuh", "internal.h"):
+            h.update(open(os.path.join(csrc, n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# --------------------------------------------------------------------------- oracle timing
+ORACLE_SNIPPET = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+from int8_kv_cache_02_gb300 import inputs
+from oracle import pool as opool, attention as oatt
+budget, max_steps, n_pos = {budget}, {max_steps}, {n_pos}
+w = inputs.grouped8k()
+pt, n = inputs.page_table([8192], 64)
+P = opool.Pool(1, 2, 256, 64, 64, n, 0)
+P.append_contiguous(0, w["k"][:8191].numpy(), w["v"][:8191].numpy(), 0, pt[0].numpy())
+kn, vn, q = w["k"][8191:].numpy()[None], w["v"][8191:].numpy()[None], w["q"][0].numpy()
+ptn = pt.numpy()
+def step():
+    P.append(0, kn, vn, [8191], ptn)
+    kh, vh = P.gather_range(0, ptn[0], 8192 - n_pos, 8192)
+    return oatt.decode(q, kh, vh, n_pos)
+for _ in range({warmup}):
+    step()
+t0 = time.perf_counter(); k = 0
+while k < max_steps and (k == 0 or time.perf_counter() - t0 < budget):
+    step(); k += 1
+print(json.dumps({{"steps": k, "seconds": time.perf_counter() - t0}}))
+"""
+
+
+def run_oracle(budget_s, max_steps, n_pos, warmup):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ORACLE_SNIPPET.format(root=ROOT, budget=budget_s, max_steps=max_steps, n_pos=n_pos,
+                                 warmup=warmup)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("oracle run failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def oracle_sample_bytes(n_pos):
+    """Bytes of the sampled step: append + decode of all heads over the last n_pos positions."""
+    return step_bytes(ctx=n_pos)
+
+
+# --------------------------------------------------------------------------- arms
+def run_ours(args, rank, world, local):
+    import torch
+
+    from int8_kv_cache_02_gb300 import binding, build, inputs
+    build.build()
+    torch.cuda.set_device(local)
+    binding.lib()
+    w = inputs.grouped8k()
+    per_copy = decode_bytes()
+    copies = args.copies or copies_for(per_copy)
+    st = DecodeState(w, CTX, binding.K8V8, copies)
+    K, W = args.steps, args.warmup
+
+    g_warm = st.graph(W)
+    g_step = st.graph(K, start=W)
+    g_dec = st.graph(K, start=W, append=False)             # decode kernel alone
+    g_warm.replay()
+    torch.cuda.synchronize()
+
+    barrier(world)
+    with ClockSampler(local) as clk:
+        ms = time_graph(g_step)
+        ms_dec = time_graph(g_dec)
+    ms = max_over_ranks(ms, world)
+    ms_dec = max_over_ranks(ms_dec, world)
+    barrier(world)
+    clocks = clk.summary()
+
+    ms_step = ms / K
+    value = step_bytes() * K * world / (ms * 1e-3) / 1e9
+    dec_s = ms_dec / K * 1e-3
+    peak, peak_kind = measured_peaks()
+    achieved = decode_bytes() / dec_s / 1e9
+    src_sha = decode_source_sha()
+    traffic = traffic_from_profiles(src_sha)
+
+    # end to end through the public API: pinned host inputs in, result out, every step
+    hq = w["q"].pin_memory()
+    hk = st.k_new.cpu().pin_memory()
+    hv = st.v_new.cpu().pin_memory()
+    hout = torch.empty((1, H, D), dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(st.q), torch.empty_like(st.k_new), torch.empty_like(st.v_new)
+    n_e2e = max(50, min(K, 500))
+
+    def e2e_step(c):
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        pt = st.pt[c:c + 1]
+        binding.kv_quant_append(st.pool, 0, dk, dv, st.pos, pt)
+        binding.attn_decode_int8(st.pool, 0, dq, st.lens, pt, st.out, st.ws, n_splits=st.n_splits)
+        hout.copy_(st.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for i in range(5):
+        e2e_step(i % copies)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        e2e_step(i % copies)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
+    d2h = hout.numel() * 4
+
+    # correctness of what was timed: the last output against the first eager run
+    ref = st.out.clone()
+    st.step(0)
+    torch.cuda.synchronize()
+    assert torch.equal(ref, st.out), "decode output changed between runs"
+    assert binding.kv_pool_read_device_error(st.pool) == 0
+
+    extra = {}
+    if not args.no_extra:
+        extra = run_extra(args)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        r = run_oracle(budget_s=10.0, max_steps=1000, n_pos=CTX, warmup=1)
+        cpu = {"value": step_bytes() * r["steps"] / r["seconds"] / 1e9, "unit": "GB/s",
+               "cores": 1, "kind": "oracle",
+               "sample": f"{r['steps']} full decode steps of the same workload (append + fp64 "
+                         f"decode over 8192 positions, all 16 heads), single thread, "
+                         f"{r['seconds']:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "s8 codes + f16 scales in, f32 compute", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": B, "n_heads": H, "n_kv_heads": HKV,
+                   "head_dim": D, "group_size": GS, "ctx": CTX, "page_size": PS,
+                   "n_splits": st.n_splits, "pool_copies": copies,
+                   "l2": f"inputs larger than L2: {copies} rotating pool copies "
+                         f"({copies * per_copy / 2**20:.0f} MiB, L2 {l2_bytes() / 2**20:.0f} MiB)",
+                   "timing": "CUDA graph of K steps, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{world}"},
+        "attn_tokens_per_s": B * 1e3 / ms_step * world,
+        "kv_positions_per_s": B * CTX * 1e3 / ms_step * world,
+        "pct_of_8tbs": round(100 * value / world / 8000, 1),
+        "e2e": {"value": round(step_bytes() * n_e2e * world / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_step": e2e_s / n_e2e * 1e6, "steps": n_e2e},
+        "roofline": {"bound": "hbm", "kernel": "attn_decode_int8 (split-K partial + combine)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "traffic": traffic, "algorithmic_bytes": decode_bytes(),
+                     "us_per_launch": dec_s * 1e6, "kernel_src_sha": src_sha},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "extra": extra,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_extra(args):
+    """128K-context decode (k8v8 and k8v16), decode kernel alone, L2 defeated by copies."""
+    import torch
+
+    from int8_kv_cache_02_gb300 import binding, inputs
+    out = {}
+    w = inputs.long128k()
+    for name, variant, vi8 in (("long128k_k8v8", binding.K8V8, True),
+                               ("long128k_k8v16", binding.K8V16, False)):
+        per = decode_bytes(ctx=131072, v_int8=vi8)
+        copies = max(2, math.ceil(2 * l2_bytes() / per) + 1)
+        st = DecodeState(w, 131072, variant, copies, append_token=False)
+        n = 60
+        g = st.graph(n, append=False)
+        time_graph(g)
+        ms = time_graph(g)
+        us = ms / n * 1e3
+        out[name] = {"us_per_step": us, "GBps": per / (us * 1e-6) / 1e9,
+                     "algorithmic_bytes": per, "n_splits": st.n_splits, "copies": copies}
+        del st, g
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_reference(args, rank, world, local):
+    if rank != 0:
+        return
+    K, W = args.steps, args.warmup
+    probe = run_oracle(budget_s=1e9, max_steps=2, n_pos=CTX, warmup=1)
+    t_full = probe["seconds"] / max(1, probe["steps"])
+    frac = min(1.0, 60.0 / max(1e-9, K * t_full))
+    n_pos = max(PS, int(CTX * frac) // PS * PS)
+    r = run_oracle(budget_s=1e9, max_steps=K, n_pos=n_pos, warmup=W)
+    byt = oracle_sample_bytes(n_pos)
+    value = byt * r["steps"] / r["seconds"] / 1e9
+    ms = r["seconds"] / r["steps"] * 1e3
+    sample = (f"each step: append 1 token + fp64 decode of all 16 heads over the last {n_pos} "
+              f"of the 8192 positions (single thread)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": r["steps"], "warmup": W, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": B, "n_heads": H, "n_kv_heads": HKV,
+                   "head_dim": D, "group_size": GS, "ctx": CTX, "sampled_positions": n_pos},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--copies", type=int, default=0, help="pool copies (0: enough to defeat L2)")
+    ap.add_argument("--no-extra", action="store_true", help="skip the 128K measurements")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        if args.impl == "ours":
+            import torch
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world, local)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * int8kv.h -- C ABI of the INT8 KV cache and split-K decode attention library
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes
+ * -------------------------
+ *  1. kv_quant_append: fp16 K/V rows of new tokens become int8 codes with an
+ *     fp16 absmax/127 scale, one per (position, kv head) as in the genie-ai-
+ *     runtime INT8 KV cache (release v0.1.0-alpha.12, "Path I series", rows
+ *     I1-I2; release v0.1.0-alpha.11, "--int8-kv triage": scales are captured
+ *     for all n_kv_heads rows, never dropped), or one per 64 values as in
+ *     Strata pull request #2698 ("What it does", kKVG = 64).  Rounding:
+ *         s = fp16_round_nearest_even(fp32(absmax) / 127.0f)
+ *         c = clamp(round_half_even(fp32(x) / fp32(s)), -127, 127), c = 0 if s == 0
+ *     Codes go into a paged pool; scales go into a separate region.
+ *  2. attn_decode_int8: GQA decode attention over that pool, dequantizing on
+ *     load (alpha.12 row I3: the scale of cached row (pos, kv_head) is read
+ *     per position), split-K across the key range with an online-softmax
+ *     partial per split and a per-head combine (genie-ai-runtime v1.3.0,
+ *     "split-K decode attention"), with an optional sliding window (v1.3.0
+ *     "Details").  Query head h uses kv head h / (n_heads / n_kv_heads).
+ *  3. attn_prefill_chunk_int8: causal attention of a chunk of new queries over
+ *     the same int8 cache (Strata #2698: the prompt chunk dequantizes on the
+ *     fly; genie-ai-runtime v1.3.1: a fused query-tiled kernel for chunks).
+ *
+ * Store variants (Strata #2698 "What it does": k8v8, and one-store variants):
+ *     INT8KV_K8V8  K and V int8 with scales
+ *     INT8KV_K8V16 K int8 with scales, V fp16
+ *     INT8KV_K16V8 K fp16, V int8 with scales
+ *
+ * Pool layout in device memory (caller-allocated; the library never
+ * allocates device memory):
+ *     int8 store   int8    [n_layers][n_pages][n_kv_heads][page_size][head_dim]
+ *     fp16 store   fp16    [n_layers][n_pages][n_kv_heads][page_size][head_dim]
+ *     scales       fp16    [n_layers][n_pages][n_kv_heads][page_size][head_dim/group_size]
+ * Position p of sequence b lives on physical page page_table[b*max_pages + p/page_size],
+ * slot p % page_size.
+ *
+ * Conventions
+ * -----------
+ *  - fp16 arrays are passed as uint16_t* holding IEEE binary16 bit patterns.
+ *  - "device" pointers are CUDA device (or managed) memory of the current
+ *    device; "host" pointers are ordinary host memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call only enqueues work on it: no call synchronises, no
+ *    call allocates, so every call can be captured in a CUDA graph.
+ *  - Every function returns an int status: INT8KV_OK (0) or a negative
+ *    INT8KV_ERR_* code; int8kv_status_string() names it.  Arguments are
+ *    validated on the host before anything is launched; nothing falls back
+ *    silently to another path.
+ *  - Device-side checks (a page id outside the pool, a sequence length beyond
+ *    its page-table row, a wait on an asynchronous copy that does not finish)
+ *    never fault: the kernel skips the access, ORs a bit into the pool's device
+ *    error word and carries on.  kv_pool_read_device_error() returns the word.
+ */
+#ifndef INT8KV_H
+#define INT8KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define INT8KV_OK                 0
+#define INT8KV_ERR_INVALID_ARG   -1  /* a size or index out of range */
+#define INT8KV_ERR_NULL_PTR      -2  /* a required pointer is NULL (e.g. scales of an int8 store) */
+#define INT8KV_ERR_ALIGNMENT     -3  /* a region or row is not 16-byte aligned */
+#define INT8KV_ERR_GROUP         -4  /* head_dim is not a multiple of group_size, or group_size unsupported */
+#define INT8KV_ERR_CAPACITY      -5  /* pages, positions or splits exceed what the pool / workspace holds */
+#define INT8KV_ERR_UNSUPPORTED   -6  /* a shape the kernels are not built for (see each call) */
+#define INT8KV_ERR_CUDA          -7  /* a CUDA runtime call or launch failed */
+#define INT8KV_ERR_WORKSPACE     -8  /* workspace NULL or smaller than the *_workspace_bytes query */
+
+/* Bits of the device error word. */
+#define INT8KV_DEVERR_PAGE_ID     1  /* page-table entry outside [0, n_pages) */
+#define INT8KV_DEVERR_LENGTH      2  /* position beyond max_pages_per_seq * page_size */
+#define INT8KV_DEVERR_TIMEOUT     4  /* an mbarrier wait on an async copy hit its iteration cap */
+
+typedef enum {
+  INT8KV_K8V8 = 0,
+  INT8KV_K8V16 = 1,
+  INT8KV_K16V8 = 2
+} int8kv_variant;
+
+/* Regions of a pool, for int8kv_pool_region_bytes. */
+#define INT8KV_REGION_K_STORE  0
+#define INT8KV_REGION_V_STORE  1
+#define INT8KV_REGION_K_SCALES 2
+#define INT8KV_REGION_V_SCALES 3
+
+/* Opaque host-side pool descriptor.  It holds the shapes and the caller's
+ * device pointers; it owns no device memory. */
+typedef struct int8kv_pool int8kv_pool;
+
+/* Bytes of one region of a pool of this shape (0 for the scales of an fp16
+ * store).  Writes *out_bytes.  Errors: INVALID_ARG, GROUP, NULL_PTR. */
+int int8kv_pool_region_bytes(int n_layers, int n_kv_heads, int head_dim, int group_size,
+                             int page_size, int n_pages, int variant, int region,
+                             size_t* out_bytes);
+
+/* Create a pool descriptor over caller-allocated device regions.
+ *   head_dim    64, 128 or 256
+ *   group_size  values per scale: head_dim (one scale per (position, kv head))
+ *               or 16/32/64/128 dividing head_dim (64 = Strata's grouping)
+ *   page_size   positions per page: 16, 32, 64 or 128
+ *   k_store, v_store   device, 16-byte aligned, region bytes as queried
+ *   k_scales, v_scales device, 16-byte aligned; required for an int8 store,
+ *                      must be NULL for an fp16 store
+ *   dev_error   device int32 word (4-byte aligned) for device-side checks, or
+ *               NULL to disable reporting (the checks still skip bad accesses)
+ * On success *out receives a descriptor to free with kv_pool_destroy.
+ * Errors: NULL_PTR, INVALID_ARG, GROUP, ALIGNMENT, UNSUPPORTED. */
+int kv_pool_create(int8kv_pool** out, int n_layers, int n_kv_heads, int head_dim,
+                   int group_size, int page_size, int n_pages, int variant,
+                   void* k_store, void* v_store, void* k_scales, void* v_scales,
+                   int32_t* dev_error);
+
+/* Free a descriptor (device regions stay the caller's).  NULL is ignored. */
+void kv_pool_destroy(int8kv_pool* pool);
+
+/* Quantize and append n_new tokens for each of n_seqs sequences of one layer
+ * (alpha.12 "Path I series" I2; Strata #2698 "What it does").
+ *   k_new, v_new  device fp16 [n_seqs][n_new][n_kv_heads][head_dim]
+ *   seq_pos       device int32 [n_seqs]: position of each sequence's first new token
+ *   page_table    device int32 [n_seqs][max_pages_per_seq]
+ * A store that is fp16 receives the values unchanged.  Positions whose page
+ * is outside the table row or the pool are skipped and flagged in the device
+ * error word.  Errors: NULL_PTR, INVALID_ARG, CUDA. */
+int kv_quant_append(const int8kv_pool* pool, int layer, const uint16_t* k_new,
+                    const uint16_t* v_new, int n_seqs, int n_new, const int32_t* seq_pos,
+                    const int32_t* page_table, int max_pages_per_seq, void* stream);
+
+/* Splits the library picks for a decode of this shape on `device` when
+ * attn_decode_int8 gets n_splits = 0: enough (sequence, kv head, split) blocks
+ * to fill the device's SMs, each split at least one page.  Returns >= 1, or a
+ * negative status. */
+int attn_decode_n_splits(int batch, int n_kv_heads, int max_ctx, int page_size, int device);
+
+/* Workspace bytes attn_decode_int8 needs for this shape (0 when n_splits == 1).
+ * Errors: INVALID_ARG. */
+int attn_decode_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_dim,
+                                int n_splits, size_t* out_bytes);
+
+/* Split-K GQA decode attention over the int8 cache of one layer.
+ *   q            device fp16 [batch][n_heads][head_dim]
+ *   seq_lens     device int32 [batch]: keys 0..L-1 of sequence b are attended
+ *                (read on the device, so a captured graph can be replayed as
+ *                lengths grow); L = 0 gives a zero output row
+ *   page_table   device int32 [batch][max_pages_per_seq]
+ *   window       0 = full context; W > 0 = only the last W positions L-W..L-1
+ *   softmax_scale 0 -> 1/sqrt(head_dim)
+ *   n_splits     0 -> attn_decode_n_splits(); 1 -> single pass, no workspace;
+ *                otherwise the key range [lo, L) is cut page-aligned into
+ *                n_splits pieces of ceil(pages/n_splits) pages
+ *   out          device fp32 [batch][n_heads][head_dim]
+ *   workspace    device, >= attn_decode_workspace_bytes, 16-byte aligned, and
+ *                ZERO-FILLED before its first use; every completed call leaves
+ *                it ready for the next one.  Calls sharing one workspace must
+ *                not overlap on the device.
+ * n_heads must be a multiple of n_kv_heads with n_heads / n_kv_heads <= 8.
+ * Errors: NULL_PTR, INVALID_ARG, UNSUPPORTED, WORKSPACE, CAPACITY, CUDA. */
+int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int batch,
+                     int n_heads, const int32_t* seq_lens, const int32_t* page_table,
+                     int max_pages_per_seq, int window, float softmax_scale, int n_splits,
+                     float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Copy the pool's device error word into *out (host) and clear it.  Blocks
+ * until `stream` has finished.  Errors: NULL_PTR (no word given), CUDA. */
+int kv_pool_read_device_error(const int8kv_pool* pool, int32_t* out, void* stream);
+
+/* Static name of a status code. */
+const char* int8kv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* INT8KV_H */

@@ -1,0 +1,273 @@
+// Host side of the C ABI declared in include/int8kv.h: argument validation,
+// pool descriptors, workspace layout, split heuristic and kernel dispatch.
+// Nothing here allocates device memory or synchronises (except
+// kv_pool_read_device_error, which is documented to).
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <new>
+
+#include <cuda_runtime.h>
+
+#include "decode_common.cuh"
+#include "internal.h"
+
+using namespace int8kv;
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool valid_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
+
+bool valid_page_size(int ps) { return ps == 16 || ps == 32 || ps == 64 || ps == 128; }
+
+// group_size: a power of two in [16, head_dim] dividing head_dim, and at least
+// head_dim / 32 (a lane of the quantizer never straddles two groups).
+bool valid_group(int d, int gs) {
+  if (gs < 16 || gs > d || (gs & (gs - 1)) != 0 || d % gs != 0) return false;
+  return gs >= d / 32;
+}
+
+bool variant_int8(int variant, bool* k8, bool* v8) {
+  switch (variant) {
+    case INT8KV_K8V8: *k8 = true; *v8 = true; return true;
+    case INT8KV_K8V16: *k8 = true; *v8 = false; return true;
+    case INT8KV_K16V8: *k8 = false; *v8 = true; return true;
+    default: return false;
+  }
+}
+
+int shape_status(int n_layers, int n_kv_heads, int head_dim, int group_size, int page_size,
+                 int n_pages, int variant) {
+  bool k8, v8;
+  if (!variant_int8(variant, &k8, &v8)) return INT8KV_ERR_INVALID_ARG;
+  if (n_layers <= 0 || n_kv_heads <= 0 || n_pages <= 0) return INT8KV_ERR_INVALID_ARG;
+  if (!valid_head_dim(head_dim)) return INT8KV_ERR_UNSUPPORTED;
+  if (!valid_page_size(page_size)) return INT8KV_ERR_UNSUPPORTED;
+  if (!valid_group(head_dim, group_size)) return INT8KV_ERR_GROUP;
+  return INT8KV_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+namespace int8kv {
+
+size_t decode_workspace_layout(int B, int H, int Hkv, int D, int n_splits, DecodeWorkspace* ws,
+                               void* base) {
+  if (n_splits <= 1) {
+    if (ws) *ws = DecodeWorkspace{nullptr, nullptr, nullptr};
+    return 0;
+  }
+  const size_t o_bytes = round_up((size_t)B * H * n_splits * D * sizeof(float), 256);
+  const size_t ml_bytes = round_up((size_t)B * H * n_splits * sizeof(float2), 256);
+  const size_t c_bytes = round_up((size_t)B * Hkv * sizeof(unsigned), 256);
+  if (ws) {
+    char* p = (char*)base;
+    ws->part_o = (float*)p;
+    ws->part_ml = (float2*)(p + o_bytes);
+    ws->counters = (unsigned*)(p + o_bytes + ml_bytes);
+  }
+  return o_bytes + ml_bytes + c_bytes;
+}
+
+}  // namespace int8kv
+
+extern "C" {
+
+const char* int8kv_status_string(int status) {
+  switch (status) {
+    case INT8KV_OK: return "ok";
+    case INT8KV_ERR_INVALID_ARG: return "invalid argument";
+    case INT8KV_ERR_NULL_PTR: return "required pointer is NULL";
+    case INT8KV_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case INT8KV_ERR_GROUP: return "group_size does not fit head_dim";
+    case INT8KV_ERR_CAPACITY: return "request exceeds pool or workspace capacity";
+    case INT8KV_ERR_UNSUPPORTED: return "shape not supported by the kernels";
+    case INT8KV_ERR_CUDA: return "CUDA runtime error";
+    case INT8KV_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int int8kv_pool_region_bytes(int n_layers, int n_kv_heads, int head_dim, int group_size,
+                             int page_size, int n_pages, int variant, int region,
+                             size_t* out_bytes) {
+  if (!out_bytes) return INT8KV_ERR_NULL_PTR;
+  const int st = shape_status(n_layers, n_kv_heads, head_dim, group_size, page_size, n_pages,
+                              variant);
+  if (st != INT8KV_OK) return st;
+  bool k8, v8;
+  variant_int8(variant, &k8, &v8);
+  const size_t rows = (size_t)n_layers * n_pages * n_kv_heads * page_size;
+  switch (region) {
+    case INT8KV_REGION_K_STORE: *out_bytes = rows * head_dim * (k8 ? 1 : 2); break;
+    case INT8KV_REGION_V_STORE: *out_bytes = rows * head_dim * (v8 ? 1 : 2); break;
+    case INT8KV_REGION_K_SCALES: *out_bytes = k8 ? rows * (head_dim / group_size) * 2 : 0; break;
+    case INT8KV_REGION_V_SCALES: *out_bytes = v8 ? rows * (head_dim / group_size) * 2 : 0; break;
+    default: return INT8KV_ERR_INVALID_ARG;
+  }
+  return INT8KV_OK;
+}
+
+int kv_pool_create(int8kv_pool** out, int n_layers, int n_kv_heads, int head_dim,
+                   int group_size, int page_size, int n_pages, int variant, void* k_store,
+                   void* v_store, void* k_scales, void* v_scales, int32_t* dev_error) {
+  if (!out) return INT8KV_ERR_NULL_PTR;
+  *out = nullptr;
+  const int st = shape_status(n_layers, n_kv_heads, head_dim, group_size, page_size, n_pages,
+                              variant);
+  if (st != INT8KV_OK) return st;
+  bool k8, v8;
+  variant_int8(variant, &k8, &v8);
+  if (!k_store || !v_store) return INT8KV_ERR_NULL_PTR;
+  if ((k8 && !k_scales) || (v8 && !v_scales)) return INT8KV_ERR_NULL_PTR;
+  if ((!k8 && k_scales) || (!v8 && v_scales)) return INT8KV_ERR_INVALID_ARG;
+  if (!aligned16(k_store) || !aligned16(v_store) || !aligned16(k_scales) ||
+      !aligned16(v_scales))
+    return INT8KV_ERR_ALIGNMENT;
+  if (((uintptr_t)dev_error & 3u) != 0) return INT8KV_ERR_ALIGNMENT;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return INT8KV_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return INT8KV_ERR_CUDA;
+  int8kv_pool* p = new (std::nothrow) int8kv_pool;
+  if (!p) return INT8KV_ERR_CAPACITY;
+  p->n_layers = n_layers;
+  p->n_kv_heads = n_kv_heads;
+  p->head_dim = head_dim;
+  p->group_size = group_size;
+  p->n_groups = head_dim / group_size;
+  p->page_size = page_size;
+  p->n_pages = n_pages;
+  p->variant = variant;
+  p->k_int8 = k8;
+  p->v_int8 = v8;
+  p->k_store = k_store;
+  p->v_store = v_store;
+  p->k_scales = (uint16_t*)k_scales;
+  p->v_scales = (uint16_t*)v_scales;
+  p->dev_error = dev_error;
+  p->device = dev;
+  p->num_sms = sms;
+  *out = p;
+  return INT8KV_OK;
+}
+
+void kv_pool_destroy(int8kv_pool* pool) { delete pool; }
+
+int kv_quant_append(const int8kv_pool* pool, int layer, const uint16_t* k_new,
+                    const uint16_t* v_new, int n_seqs, int n_new, const int32_t* seq_pos,
+                    const int32_t* page_table, int max_pages_per_seq, void* stream) {
+  if (!pool) return INT8KV_ERR_NULL_PTR;
+  if (layer < 0 || layer >= pool->n_layers || n_seqs < 0 || n_new < 0 || max_pages_per_seq <= 0)
+    return INT8KV_ERR_INVALID_ARG;
+  if ((long long)n_seqs * n_new == 0) return INT8KV_OK;
+  if (!k_new || !v_new || !seq_pos || !page_table) return INT8KV_ERR_NULL_PTR;
+  if (!aligned16(k_new) || !aligned16(v_new)) return INT8KV_ERR_ALIGNMENT;
+  const cudaError_t e = launch_quant_append(layer_view(pool, layer), k_new, v_new, n_seqs, n_new,
+                                            seq_pos, page_table, max_pages_per_seq, pool->k_int8,
+                                            pool->v_int8, (cudaStream_t)stream);
+  return e == cudaSuccess ? INT8KV_OK : INT8KV_ERR_CUDA;
+}
+
+int attn_decode_n_splits(int batch, int n_kv_heads, int max_ctx, int page_size, int device) {
+  if (batch <= 0 || n_kv_heads <= 0 || max_ctx < 0 || !valid_page_size(page_size))
+    return INT8KV_ERR_INVALID_ARG;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return INT8KV_ERR_CUDA;
+  const long long units = (long long)batch * n_kv_heads;
+  const int pages = max_ctx > 0 ? (max_ctx + page_size - 1) / page_size : 1;
+  // Two resident blocks per SM worth of (sequence, kv head, split) blocks.
+  const long long target = 2LL * sms;
+  long long n = (target + units - 1) / units;
+  if (n > pages) n = pages;
+  if (n > kMaxSplits) n = kMaxSplits;
+  if (n < 1) n = 1;
+  return (int)n;
+}
+
+int attn_decode_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_dim,
+                                int n_splits, size_t* out_bytes) {
+  if (!out_bytes) return INT8KV_ERR_NULL_PTR;
+  if (batch < 0 || n_heads <= 0 || n_kv_heads <= 0 || !valid_head_dim(head_dim) ||
+      n_splits < 1 || n_splits > kMaxSplits)
+    return INT8KV_ERR_INVALID_ARG;
+  *out_bytes = decode_workspace_layout(batch, n_heads, n_kv_heads, head_dim, n_splits, nullptr,
+                                       nullptr);
+  return INT8KV_OK;
+}
+
+int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int batch,
+                     int n_heads, const int32_t* seq_lens, const int32_t* page_table,
+                     int max_pages_per_seq, int window, float softmax_scale, int n_splits,
+                     float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!pool) return INT8KV_ERR_NULL_PTR;
+  if (layer < 0 || layer >= pool->n_layers || batch < 0 || n_heads <= 0 ||
+      max_pages_per_seq <= 0 || window < 0 || n_splits < 0 || n_splits > kMaxSplits ||
+      !std::isfinite(softmax_scale))
+    return INT8KV_ERR_INVALID_ARG;
+  if (n_heads % pool->n_kv_heads != 0) return INT8KV_ERR_INVALID_ARG;
+  const int G = n_heads / pool->n_kv_heads;
+  if (G > 8) return INT8KV_ERR_UNSUPPORTED;
+  if (batch == 0) return INT8KV_OK;
+  if (!q || !seq_lens || !page_table || !out) return INT8KV_ERR_NULL_PTR;
+  if (!aligned16(q) || !aligned16(out)) return INT8KV_ERR_ALIGNMENT;
+  if (n_splits == 0) {
+    n_splits = attn_decode_n_splits(batch, pool->n_kv_heads,
+                                    max_pages_per_seq * pool->page_size, pool->page_size,
+                                    pool->device);
+    if (n_splits < 0) return n_splits;
+  }
+  DecodeArgs a;
+  const size_t need = decode_workspace_layout(batch, n_heads, pool->n_kv_heads, pool->head_dim,
+                                              n_splits, &a.ws, workspace);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return INT8KV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return INT8KV_ERR_ALIGNMENT;
+  }
+  a.pool = layer_view(pool, layer);
+  a.q = q;
+  a.seq_lens = seq_lens;
+  a.page_table = page_table;
+  a.out = out;
+  a.B = batch;
+  a.H = n_heads;
+  a.G = G;
+  a.max_pages = max_pages_per_seq;
+  a.window = window;
+  a.n_splits = n_splits;
+  const float scale = softmax_scale != 0.f ? softmax_scale : 1.0f / std::sqrt((float)pool->head_dim);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const cudaError_t e = launch_decode(a, pool->variant, (cudaStream_t)stream);
+  if (e == cudaErrorNotSupported) return INT8KV_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? INT8KV_OK : INT8KV_ERR_CUDA;
+}
+
+int kv_pool_read_device_error(const int8kv_pool* pool, int32_t* out, void* stream) {
+  if (!pool || !out || !pool->dev_error) return INT8KV_ERR_NULL_PTR;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(out, pool->dev_error, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return INT8KV_ERR_CUDA;
+  if (cudaMemsetAsync(pool->dev_error, 0, sizeof(int32_t), s) != cudaSuccess)
+    return INT8KV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return INT8KV_ERR_CUDA;
+  return INT8KV_OK;
+}
+
+}  // extern "C"
+
+namespace int8kv {
+
+cudaError_t launch_decode(const DecodeArgs& a, int variant, cudaStream_t stream) {
+  bool k8, v8;
+  variant_int8(variant, &k8, &v8);
+  return launch_decode_simt(a, k8, v8, stream);
+}
+
+}  // namespace int8kv

@@ -1,0 +1,189 @@
+// Split-K GQA decode attention over the int8 cache, CUDA-core version.
+//
+// Method: genie-ai-runtime v1.3.0 "split-K decode attention": the key range of
+// each head is cut into n_splits pieces, each block computes an online-softmax
+// partial (m, l, o~) and a reduce combines the partials per head.  Keys are
+// dequantized on load with their own (position, kv head[, group]) scale
+// (genie-ai-runtime v0.1.0-alpha.12 "Path I series" row I3).
+//
+// Grid (n_splits, Hkv, B); one block serves all G query heads of its kv head so
+// every cached byte is read once.  Four warps take the block's keys round-robin;
+// lane l owns dims [l*VPL, (l+1)*VPL) of every row, so a row is one coalesced
+// warp access.  Scores are reduced with warp shuffles; softmax runs in base 2
+// (scale folded with log2 e).  The warps' partials are merged in shared memory;
+// with n_splits > 1 the block stores its partial, and the last block of a
+// (sequence, kv head) to arrive (atomic ticket, no waiting) combines all splits
+// and resets the ticket.
+//
+// This kernel is the general path (any G <= 8, head_dim 64/128/256, every
+// store variant); the tensor-core kernel in decode_mma.cu serves the shapes it
+// is specialised for.
+
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "decode_common.cuh"
+
+namespace int8kv {
+namespace {
+
+constexpr int kWarps = 4;
+
+template <int VPL>
+__device__ __forceinline__ void load_row(const void* store, bool is_int8, const uint16_t* scales,
+                                         size_t row, int D, int ng, int gs, int lane,
+                                         float (&x)[VPL]) {
+  if (is_int8) {
+    const int8_t* src = (const int8_t*)store + row * D + lane * VPL;
+    int8_t c[VPL];
+    if constexpr (VPL == 8) {
+      *reinterpret_cast<uint2*>(c) = __ldg(reinterpret_cast<const uint2*>(src));
+    } else if constexpr (VPL == 4) {
+      *reinterpret_cast<uint32_t*>(c) = __ldg(reinterpret_cast<const uint32_t*>(src));
+    } else {
+      *reinterpret_cast<uint16_t*>(c) = __ldg(reinterpret_cast<const uint16_t*>(src));
+    }
+    const float s = h2f(__ldg(scales + row * ng + (lane * VPL) / gs));
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) x[i] = (float)c[i] * s;
+  } else {
+    const uint16_t* src = (const uint16_t*)store + row * D + lane * VPL;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) x[i] = h2f(__ldg(src + i));
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeArgs a, bool k_int8,
+                                                                   bool v_int8) {
+  constexpr int VPL = D / 32;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int G = a.G;
+  const PoolView& p = a.pool;
+
+  __shared__ float s_m[kWarps][8], s_l[kWarps][8];
+  __shared__ float s_o[kWarps][8][D];
+  __shared__ int s_last;
+
+  float qr[8][VPL];
+#pragma unroll
+  for (int g = 0; g < 8; ++g)
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      qr[g][i] = g < G ? h2f(__ldg(a.q + ((size_t)b * a.H + kvh * G + g) * D + lane * VPL + i)) : 0.f;
+
+  const int L = clamp_length(__ldg(a.seq_lens + b), a.max_pages, p);
+  const int lo = a.window > 0 ? max(0, L - a.window) : 0;
+  int j0, j1;
+  split_range(lo, L, split, a.n_splits, p.ps, &j0, &j1);
+
+  float m[8], l[8], o[8][VPL];
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    m[g] = -INFINITY;
+    l[g] = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) o[g][i] = 0.f;
+  }
+
+  const int32_t* ptrow = a.page_table + (size_t)b * a.max_pages;
+  for (int j = j0 + warp; j < j1; j += kWarps) {
+    const int pg = lookup_page(ptrow, j / p.ps, a.max_pages, p);
+    if (pg < 0) continue;
+    const size_t row = row_index(p, pg, kvh, j % p.ps);
+    float kf[VPL], vf[VPL];
+    load_row<VPL>(p.k, k_int8, p.ks, row, D, p.ng, p.gs, lane, kf);
+    load_row<VPL>(p.v, v_int8, p.vs, row, D, p.ng, p.gs, lane, vf);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      if (g < G) {
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) s = fmaf(qr[g][i], kf[i], s);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        const float z = s * a.scale_log2;
+        const float mn = fmaxf(m[g], z);
+        const float alpha = exp2f(m[g] - mn);
+        const float pz = exp2f(z - mn);
+        l[g] = l[g] * alpha + pz;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) o[g][i] = fmaf(o[g][i], alpha, pz * vf[i]);
+        m[g] = mn;
+      }
+    }
+  }
+
+  // merge the warps' partials in shared memory
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    if (lane == 0) {
+      s_m[warp][g] = m[g];
+      s_l[warp][g] = l[g];
+    }
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) s_o[warp][g][lane * VPL + i] = o[g][i];
+  }
+  __syncthreads();
+
+  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+    const int g = e / D, d = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][g]);
+    float Ls = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = exp2f(s_m[w][g] - M);
+        Ls = fmaf(s_l[w][g], f, Ls);
+        O = fmaf(s_o[w][g][d], f, O);
+      }
+    }
+    const size_t h = (size_t)b * a.H + kvh * G + g;
+    if (a.n_splits == 1) {
+      a.out[h * D + d] = Ls > 0.f ? O / Ls : 0.f;
+    } else {
+      a.ws.part_o[(h * a.n_splits + split) * D + d] = O;
+      if (d == 0) a.ws.part_ml[h * a.n_splits + split] = make_float2(M, Ls);
+    }
+  }
+  if (a.n_splits == 1) return;
+
+  // last block of this (sequence, kv head) combines the splits
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned t = atomicAdd(a.ws.counters + (size_t)b * p.Hkv + kvh, 1u);
+    s_last = (t == (unsigned)a.n_splits - 1);
+    __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+  combine_splits_block(a, b, kvh, &s_o[0][0][0]);
+  if (threadIdx.x == 0) a.ws.counters[(size_t)b * p.Hkv + kvh] = 0u;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_simt(const DecodeArgs& a, bool k_int8, bool v_int8,
+                               cudaStream_t stream) {
+  const dim3 grid(a.n_splits, a.pool.Hkv, a.B);
+  switch (a.pool.D) {
+    case 64:
+      decode_simt_kernel<64><<<grid, kWarps * 32, 0, stream>>>(a, k_int8, v_int8);
+      break;
+    case 128:
+      decode_simt_kernel<128><<<grid, kWarps * 32, 0, stream>>>(a, k_int8, v_int8);
+      break;
+    case 256:
+      decode_simt_kernel<256><<<grid, kWarps * 32, 0, stream>>>(a, k_int8, v_int8);
+      break;
+    default:
+      return cudaErrorNotSupported;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace int8kv

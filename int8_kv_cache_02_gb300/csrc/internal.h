@@ -1,0 +1,84 @@
+// Internal definitions shared by the C-ABI host code and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "int8kv.h"
+
+// Host-side pool descriptor (opaque in the public header).
+struct int8kv_pool {
+  int n_layers, n_kv_heads, head_dim, group_size, n_groups, page_size, n_pages, variant;
+  bool k_int8, v_int8;
+  void* k_store;
+  void* v_store;
+  uint16_t* k_scales;
+  uint16_t* v_scales;
+  int32_t* dev_error;
+  int device;        // CUDA device the pool was created on
+  int num_sms;       // its SM count (split heuristic)
+};
+
+namespace int8kv {
+
+// The pool as the kernels see it, for one layer (pointers already offset).
+struct PoolView {
+  const void* k;            // K store of the layer: int8 or fp16 [n_pages][Hkv][ps][D]
+  const void* v;            // V store of the layer
+  const uint16_t* ks;       // K scales of the layer (fp16) [n_pages][Hkv][ps][ng], or null
+  const uint16_t* vs;       // V scales of the layer, or null
+  int32_t* err;             // device error word, or null
+  int n_pages, Hkv, D, gs, ng, ps;
+};
+
+inline PoolView layer_view(const int8kv_pool* p, int layer) {
+  PoolView v;
+  const size_t rows = (size_t)p->n_pages * p->n_kv_heads * p->page_size;
+  const size_t kb = p->k_int8 ? 1 : 2, vb = p->v_int8 ? 1 : 2;
+  v.k = (const char*)p->k_store + (size_t)layer * rows * p->head_dim * kb;
+  v.v = (const char*)p->v_store + (size_t)layer * rows * p->head_dim * vb;
+  v.ks = p->k_scales ? p->k_scales + (size_t)layer * rows * p->n_groups : nullptr;
+  v.vs = p->v_scales ? p->v_scales + (size_t)layer * rows * p->n_groups : nullptr;
+  v.err = p->dev_error;
+  v.n_pages = p->n_pages;
+  v.Hkv = p->n_kv_heads;
+  v.D = p->head_dim;
+  v.gs = p->group_size;
+  v.ng = p->n_groups;
+  v.ps = p->page_size;
+  return v;
+}
+
+// Workspace of the split-K decode: partial (m, l) and unnormalised o per
+// (sequence, query head, split), and one arrival counter per (sequence, kv head).
+struct DecodeWorkspace {
+  float* part_o;      // [B][H][n_splits][D]
+  float2* part_ml;    // [B][H][n_splits]
+  unsigned* counters; // [B][Hkv]
+};
+
+size_t decode_workspace_layout(int B, int H, int Hkv, int D, int n_splits,
+                               DecodeWorkspace* ws, void* base);
+
+struct DecodeArgs {
+  PoolView pool;
+  const uint16_t* q;        // [B][H][D] fp16
+  const int32_t* seq_lens;  // [B]
+  const int32_t* page_table;// [B][max_pages]
+  float* out;               // [B][H][D]
+  DecodeWorkspace ws;
+  int B, H, G, max_pages, window, n_splits;
+  float scale_log2;         // softmax_scale * log2(e)
+};
+
+cudaError_t launch_quant_append(const PoolView& pool, const uint16_t* k_new, const uint16_t* v_new,
+                                int n_seqs, int n_new, const int32_t* seq_pos,
+                                const int32_t* page_table, int max_pages, bool k_int8,
+                                bool v_int8, cudaStream_t stream);
+
+// Returns cudaErrorNotSupported when no kernel is built for the shape.
+cudaError_t launch_decode(const DecodeArgs& a, int variant, cudaStream_t stream);
+
+}  // namespace int8kv

@@ -1,0 +1,145 @@
+// kv_quant_append: fp16 K/V rows of new tokens -> int8 codes + fp16 absmax/127
+// scales, written through the page table into the paged pool.
+//
+// Method: genie-ai-runtime release v0.1.0-alpha.12, "Path I series" rows I1-I2
+// (per-head conversion with scale capture into a separate scales region) and
+// Strata pull request #2698, "What it does" (one FP16 scale per 64 values,
+// group absmax / 127).  Rounding: s = fp16_rn(fp32(absmax) / 127.0f) with an
+// IEEE division; code = round-half-even(fp32(x) / fp32(s)), clamped to ±127;
+// s == 0 gives code 0.
+//
+// One warp per (sequence, new token, kv head) row; lane l holds the head_dim/32
+// consecutive values [l*VPL, (l+1)*VPL), loaded and stored with one vector
+// access each, so a row is one coalesced read and one coalesced write.  The
+// absmax of a group of gs values is a butterfly max over the gs/VPL lanes that
+// hold it.  HBM-bound: per row 2*D bytes in, D + 2*D/gs bytes out per store.
+
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+
+namespace int8kv {
+namespace {
+
+template <int VPL>
+struct Vec;
+template <>
+struct Vec<2> { using H = uint32_t; using B = uint16_t; };
+template <>
+struct Vec<4> { using H = uint2; using B = uint32_t; };
+template <>
+struct Vec<8> { using H = uint4; using B = uint2; };
+
+template <int VPL>
+__device__ __forceinline__ void load_halves(const uint16_t* src, float (&x)[VPL]) {
+  typename Vec<VPL>::H raw = *reinterpret_cast<const typename Vec<VPL>::H*>(src);
+  const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+  for (int i = 0; i < VPL / 2; ++i) {
+    const float2 f = __half22float2(h2[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+template <int VPL>
+__device__ __forceinline__ void quantize_row(const uint16_t* src, int8_t* dst_codes,
+                                             uint16_t* dst_scales, int lane, int lanes_per_group) {
+  float x[VPL];
+  load_halves<VPL>(src + lane * VPL, x);
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  for (int off = 1; off < lanes_per_group; off <<= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
+  const float s = __half2float(s16);
+  union { typename Vec<VPL>::B v; int8_t c[VPL]; } out;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    int c = 0;
+    if (s != 0.f) {
+      c = __float2int_rn(__fdiv_rn(x[i], s));  // round half to even
+      c = max(-127, min(127, c));
+    }
+    out.c[i] = (int8_t)c;
+  }
+  *reinterpret_cast<typename Vec<VPL>::B*>(dst_codes + lane * VPL) = out.v;
+  if ((lane % lanes_per_group) == 0) dst_scales[(lane * VPL) / (lanes_per_group * VPL)] =
+      __half_as_ushort(s16);
+}
+
+template <int VPL>
+__device__ __forceinline__ void copy_row(const uint16_t* src, uint16_t* dst, int lane) {
+  *reinterpret_cast<typename Vec<VPL>::H*>(dst + lane * VPL) =
+      *reinterpret_cast<const typename Vec<VPL>::H*>(src + lane * VPL);
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(256) quant_append_kernel(
+    PoolView p, const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
+    int n_seqs, int n_new, const int32_t* __restrict__ seq_pos,
+    const int32_t* __restrict__ page_table, int max_pages, bool k_int8, bool v_int8) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long n_rows = (long long)n_seqs * n_new * p.Hkv;
+  if (row >= n_rows) return;
+  const int kvh = (int)(row % p.Hkv);
+  const long long bi = row / p.Hkv;      // b * n_new + i
+  const int i = (int)(bi % n_new);
+  const int b = (int)(bi / n_new);
+  const int pos = __ldg(seq_pos + b) + i;
+  if (pos < 0) {
+    if (lane == 0) flag_error(p.err, INT8KV_DEVERR_LENGTH);
+    return;
+  }
+  const int page = lookup_page(page_table + (size_t)b * max_pages, pos / p.ps, max_pages, p);
+  if (page < 0) return;
+  const size_t dst_row = row_index(p, page, kvh, pos % p.ps);
+  const size_t src_off = (size_t)row * p.D;
+  const int lpg = p.gs / VPL;  // lanes per scale group
+  if (k_int8)
+    quantize_row<VPL>(k_new + src_off, (int8_t*)p.k + dst_row * p.D,
+                      (uint16_t*)p.ks + dst_row * p.ng, lane, lpg);
+  else
+    copy_row<VPL>(k_new + src_off, (uint16_t*)p.k + dst_row * p.D, lane);
+  if (v_int8)
+    quantize_row<VPL>(v_new + src_off, (int8_t*)p.v + dst_row * p.D,
+                      (uint16_t*)p.vs + dst_row * p.ng, lane, lpg);
+  else
+    copy_row<VPL>(v_new + src_off, (uint16_t*)p.v + dst_row * p.D, lane);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_append(const PoolView& pool, const uint16_t* k_new, const uint16_t* v_new,
+                                int n_seqs, int n_new, const int32_t* seq_pos,
+                                const int32_t* page_table, int max_pages, bool k_int8,
+                                bool v_int8, cudaStream_t stream) {
+  const long long rows = (long long)n_seqs * n_new * pool.Hkv;
+  if (rows == 0) return cudaSuccess;
+  const int warps = 8;
+  const unsigned grid = (unsigned)((rows + warps - 1) / warps);
+  switch (pool.D) {
+    case 64:
+      quant_append_kernel<2><<<grid, warps * 32, 0, stream>>>(pool, k_new, v_new, n_seqs, n_new,
+                                                              seq_pos, page_table, max_pages,
+                                                              k_int8, v_int8);
+      break;
+    case 128:
+      quant_append_kernel<4><<<grid, warps * 32, 0, stream>>>(pool, k_new, v_new, n_seqs, n_new,
+                                                              seq_pos, page_table, max_pages,
+                                                              k_int8, v_int8);
+      break;
+    case 256:
+      quant_append_kernel<8><<<grid, warps * 32, 0, stream>>>(pool, k_new, v_new, n_seqs, n_new,
+                                                              seq_pos, page_table, max_pages,
+                                                              k_int8, v_int8);
+      break;
+    default:
+      return cudaErrorNotSupported;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace int8kv

@@ -112,8 +112,12 @@ class Pool:
 
     def gather(self, layer, page_table_row, length):
         """Exact fp64 K^, V^ [length][n_kv_heads][head_dim] of positions 0..length-1."""
-        pos = np.arange(length)
-        pages = np.asarray(page_table_row)[pos // self.page_size] if length else np.zeros(0, int)
+        return self.gather_range(layer, page_table_row, 0, length)
+
+    def gather_range(self, layer, page_table_row, start, stop):
+        """Exact fp64 K^, V^ [stop-start][n_kv_heads][head_dim] of positions start..stop-1."""
+        pos = np.arange(start, stop)
+        pages = np.asarray(page_table_row)[pos // self.page_size] if stop > start else np.zeros(0, int)
         slots = pos % self.page_size
         out = []
         for store, scales, is8 in (

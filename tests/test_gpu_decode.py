@@ -1,0 +1,205 @@
+"""attn_decode_int8 on the GPU against the fp64 oracle over the dequantized cache.
+
+Tolerance (fp32 kernel vs fp64 oracle): max abs error <= 2e-3 and max relative
+L2 error per (sequence, query head) output vector <= 1e-4.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from int8_kv_cache_02_gb300 import inputs
+from oracle import attention as oatt
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    gu.lib_ready()
+
+
+def _setup(seed, B, H, Hkv, D, gs, lens, variant, ps=64, n_layers=1, layer=0, outliers=False,
+           page_seed=1, spare_pages=3):
+    q, ks, vs = inputs.random_case(seed, B, H, Hkv, D, lens, outliers=outliers)
+    pt, n_pages = inputs.page_table([max(1, L) for L in lens], ps,
+                                    n_pages_total=sum(-(-max(1, L) // ps) for L in lens) + spare_pages,
+                                    seed=page_seed)
+    dev, orc = gu.make_pools(n_layers, Hkv, D, gs, ps, n_pages, variant)
+    for b, L in enumerate(lens):
+        if L:
+            gu.fill_sequence(dev, orc, layer, ks[b], vs[b], pt[b])
+    return q, pt, dev, orc
+
+
+def _decode(dev, layer, q, lens, pt, window=0, n_splits=0, scale=0.0, ws=None):
+    from int8_kv_cache_02_gb300 import binding
+    B, H, D = q.shape
+    if n_splits == 0:
+        n_splits = binding.attn_decode_n_splits(B, dev.n_kv_heads, pt.shape[1] * dev.page_size,
+                                                dev.page_size)
+    if ws is None:
+        ws = dev.decode_workspace(B, H, n_splits)
+    out = torch.full((B, H, D), float("nan"), dtype=torch.float32, device="cuda")
+    binding.attn_decode_int8(dev, layer, q.cuda(), torch.tensor(lens, dtype=torch.int32,
+                                                                  device="cuda"),
+                             pt.cuda(), out, ws, window=window, softmax_scale=scale,
+                             n_splits=n_splits)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def _oracle(orc, layer, q, lens, pt, window=0, scale=None):
+    outs = []
+    for b, L in enumerate(lens):
+        kh, vh = orc.gather(layer, pt[b].numpy(), L)
+        outs.append(oatt.decode(q[b].numpy(), kh, vh, L, window=window, scale=scale))
+    return np.stack(outs)
+
+
+CASES = [
+    # seed, B, H, Hkv, D, gs, lens, variant, ps
+    (1, 1, 8, 2, 128, 128, [512], 0, 64),
+    (2, 2, 16, 2, 256, 64, [700, 129], 0, 64),
+    (3, 3, 32, 8, 128, 128, [64, 1, 1000], 0, 64),
+    (4, 2, 8, 1, 64, 32, [300, 77], 0, 16),
+    (5, 1, 16, 2, 256, 64, [1500], 1, 64),
+    (6, 1, 16, 2, 256, 64, [1500], 2, 64),
+    (7, 2, 4, 4, 128, 64, [333, 65], 0, 32),
+    (8, 2, 12, 2, 128, 32, [257, 999], 1, 128),
+    (9, 1, 10, 2, 64, 64, [200], 2, 64),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"s{c[0]}")
+@pytest.mark.parametrize("n_splits", [1, 4, 0])
+def test_decode_matches_oracle(case, n_splits):
+    seed, B, H, Hkv, D, gs, lens, variant, ps = case
+    q, pt, dev, orc = _setup(seed, B, H, Hkv, D, gs, lens, variant, ps=ps, outliers=True)
+    out = _decode(dev, 0, q, lens, pt, n_splits=n_splits)
+    ref = _oracle(orc, 0, q, lens, pt)
+    gu.assert_attention_close(out, ref, f"case {seed} n_splits {n_splits}")
+
+
+@pytest.mark.parametrize("window,lens", [(512, [2000, 300, 513]), (100, [100, 101, 5000]),
+                                         (1, [7, 1])])
+def test_sliding_window(window, lens):
+    q, pt, dev, orc = _setup(21, len(lens), 32, 8, 128, 128, lens, 0)
+    for ns in (1, 3, 0):
+        out = _decode(dev, 0, q, lens, pt, window=window, n_splits=ns)
+        gu.assert_attention_close(out, _oracle(orc, 0, q, lens, pt, window=window),
+                                  f"window {window} n_splits {ns}")
+
+
+def test_split_equals_single_pass_tiny_workload():
+    """genie-ai-runtime v1.3.0: split-K is exact against the single-block kernel.
+    The tiny workload (512 positions, GQA 4): n_splits 4 against 1."""
+    w = inputs.tiny()
+    pt, n_pages = inputs.page_table([512], 64)
+    dev, orc = gu.make_pools(1, 2, 128, 128, 64, n_pages, 0)
+    gu.fill_sequence(dev, orc, 0, w["k"], w["v"], pt[0])
+    one = _decode(dev, 0, w["q"], [512], pt, n_splits=1)
+    four = _decode(dev, 0, w["q"], [512], pt, n_splits=4)
+    assert np.max(np.abs(one - four)) <= 1e-6
+    gu.assert_attention_close(four, _oracle(orc, 0, w["q"], [512], pt), "tiny")
+
+
+def test_context_one_returns_the_dequantized_v_row():
+    q, pt, dev, orc = _setup(31, 2, 16, 2, 256, 64, [1, 1], 0)
+    out = _decode(dev, 0, q, [1, 1], pt, n_splits=1)
+    for b in range(2):
+        _, vh = orc.gather(0, pt[b].numpy(), 1)
+        for h in range(16):
+            assert np.array_equal(out[b, h].astype(np.float64), vh[0, h // 8])
+
+
+def test_identical_keys_return_the_mean_of_v():
+    from int8_kv_cache_02_gb300 import binding
+    L, Hkv, D = 300, 2, 128
+    g = torch.Generator().manual_seed(41)
+    k = inputs.normal_f16((1, Hkv, D), g).expand(L, Hkv, D).contiguous()
+    v = inputs.normal_f16((L, Hkv, D), g)
+    q = inputs.normal_f16((1, 8, D), g)
+    pt, n_pages = inputs.page_table([L], 64, seed=2)
+    dev, orc = gu.make_pools(1, Hkv, D, 128, 64, n_pages, 0)
+    gu.fill_sequence(dev, orc, 0, k, v, pt[0])
+    out = _decode(dev, 0, q, [L], pt, n_splits=3)
+    _, vh = orc.gather(0, pt[0].numpy(), L)
+    for h in range(8):
+        assert np.allclose(out[0, h], vh[:, h // 4].mean(axis=0), rtol=0, atol=2e-6)
+    assert binding.kv_pool_read_device_error(dev) == 0
+
+
+def test_empty_sequences_give_zero_rows():
+    q, pt, dev, orc = _setup(51, 3, 8, 2, 128, 128, [0, 130, 0], 0)
+    out = _decode(dev, 0, q, [0, 130, 0], pt, n_splits=4)
+    assert (out[0] == 0).all() and (out[2] == 0).all()
+    gu.assert_attention_close(out[1:2], _oracle(orc, 0, q[1:2], [130], pt[1:2]), "mid")
+
+
+def test_paged_equals_contiguous_bitwise_and_workspace_reuse():
+    L = 1000
+    q, ks, vs = inputs.random_case(61, 1, 16, 2, 256, [L], outliers=True)
+    res = []
+    for seed in (None, 5):
+        pt, n_pages = inputs.page_table([L], 64, n_pages_total=40, seed=seed)
+        dev, orc = gu.make_pools(1, 2, 256, 64, 64, n_pages, 0)
+        gu.fill_sequence(dev, orc, 0, ks[0], vs[0], pt[0], oracle=False)
+        ws = dev.decode_workspace(1, 16, 6)
+        a = _decode(dev, 0, q, [L], pt, n_splits=6, ws=ws)
+        b = _decode(dev, 0, q, [L], pt, n_splits=6, ws=ws)        # same workspace again
+        assert np.array_equal(a, b)
+        res.append(a)
+    assert np.array_equal(res[0], res[1])
+
+
+def test_softmax_scale_override_and_second_layer():
+    q, pt, dev, orc = _setup(71, 1, 8, 2, 128, 64, [400], 0, n_layers=2, layer=1)
+    sc = 0.3
+    out = _decode(dev, 1, q, [400], pt, n_splits=2, scale=sc)
+    gu.assert_attention_close(out, _oracle(orc, 1, q, [400], pt, scale=sc), "scale")
+    out0 = _decode(dev, 0, q, [400], pt, n_splits=2)            # layer 0 is empty: all codes 0
+    assert np.isfinite(out0).all()
+
+
+def test_length_beyond_the_page_table_is_clamped_and_flagged():
+    from int8_kv_cache_02_gb300 import binding
+    q, pt, dev, orc = _setup(81, 1, 8, 2, 128, 128, [128], 0)      # page table holds 2 pages
+    out = _decode(dev, 0, q, [5000], pt, n_splits=2)
+    assert binding.kv_pool_read_device_error(dev) & binding.DEVERR_LENGTH
+    gu.assert_attention_close(out, _oracle(orc, 0, q, [128], pt), "clamped")
+
+
+@pytest.mark.slow
+def test_grouped8k_workload_with_append():
+    """8192-position context, 64-value groups with outlier K channels: 8191 cached
+    positions, the step appends the last token and decodes over all 8192."""
+    from int8_kv_cache_02_gb300 import binding
+    w = inputs.grouped8k()
+    pt, n_pages = inputs.page_table([8192], 64, seed=7)
+    dev, orc = gu.make_pools(1, 2, 256, 64, 64, n_pages, 0)
+    gu.fill_sequence(dev, orc, 0, w["k"][:8191], w["v"][:8191], pt[0])
+    binding.kv_quant_append(dev, 0, w["k"][8191:].reshape(1, 1, 2, 256).cuda(),
+                            w["v"][8191:].reshape(1, 1, 2, 256).cuda(),
+                            torch.tensor([8191], dtype=torch.int32, device="cuda"), pt.cuda())
+    orc.append(0, w["k"][8191:].numpy()[None], w["v"][8191:].numpy()[None], [8191], pt.numpy())
+    gu.regions_equal(dev, orc)
+    ref = _oracle(orc, 0, w["q"], [8192], pt)
+    for ns in (0, 1, 16):
+        gu.assert_attention_close(_decode(dev, 0, w["q"], [8192], pt, n_splits=ns), ref,
+                                  f"8k n_splits {ns}")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("variant", [0, 1])
+def test_long128k_workload(variant):
+    w = inputs.long128k()
+    L = 131072
+    pt, n_pages = inputs.page_table([L], 64, seed=8)
+    dev, orc = gu.make_pools(1, 2, 256, 64, 64, n_pages, variant)
+    gu.fill_sequence(dev, orc, 0, w["k"], w["v"], pt[0])
+    ref = _oracle(orc, 0, w["q"], [L], pt)
+    gu.assert_attention_close(_decode(dev, 0, w["q"], [L], pt), ref, f"128k v{variant}")
