@@ -169,9 +169,9 @@ class DecodeState:
         self.h = w["H"]
         self.pool = binding.KVPool(1, hkv, d, gs, PS, n_pages_copy * copies, variant)
         pts = []
-        for c in range(copies):
-            pt, _ = inputs.page_table([ctx], PS, n_pages_total=n_pages_copy * copies, seed=100 + c)
-            pts.append(pt)
+        for c in range(copies):                              # disjoint page range per copy
+            pt, _ = inputs.page_table([ctx], PS, seed=100 + c)
+            pts.append(pt + c * n_pages_copy)
         self.pt = torch.cat(pts).cuda()                      # [copies][pages]
         n_cached = ctx - 1 if append_token else ctx
         kd = w["k"][:n_cached].reshape(1, n_cached, hkv, d).cuda()

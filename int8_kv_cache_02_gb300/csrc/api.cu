@@ -52,26 +52,59 @@ int shape_status(int n_layers, int n_kv_heads, int head_dim, int group_size, int
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_tiled_fn() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiled)f;
+  }
+  return fn;
+}
+
+// 2-D view [rows][head_dim] of a whole store (all layers), 64-row x 128-byte
+// boxes with the 128-byte swizzle.
+bool make_store_map(CUtensorMap* map, void* base, bool is_int8, int head_dim, size_t rows) {
+  EncodeTiled enc = encode_tiled_fn();
+  if (!enc) return false;
+  const size_t esz = is_int8 ? 1 : 2;
+  cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(head_dim * esz)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / esz), 64};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, is_int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+             base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 namespace int8kv {
 
 size_t decode_workspace_layout(int B, int H, int Hkv, int D, int n_splits, DecodeWorkspace* ws,
                                void* base) {
+  (void)Hkv;
   if (n_splits <= 1) {
-    if (ws) *ws = DecodeWorkspace{nullptr, nullptr, nullptr};
+    if (ws) *ws = DecodeWorkspace{nullptr, nullptr};
     return 0;
   }
   const size_t o_bytes = round_up((size_t)B * H * n_splits * D * sizeof(float), 256);
   const size_t ml_bytes = round_up((size_t)B * H * n_splits * sizeof(float2), 256);
-  const size_t c_bytes = round_up((size_t)B * Hkv * sizeof(unsigned), 256);
   if (ws) {
     char* p = (char*)base;
     ws->part_o = (float*)p;
     ws->part_ml = (float2*)(p + o_bytes);
-    ws->counters = (unsigned*)(p + o_bytes + ml_bytes);
   }
-  return o_bytes + ml_bytes + c_bytes;
+  return o_bytes + ml_bytes;
 }
 
 }  // namespace int8kv
@@ -153,6 +186,16 @@ int kv_pool_create(int8kv_pool** out, int n_layers, int n_kv_heads, int head_dim
   p->dev_error = dev_error;
   p->device = dev;
   p->num_sms = sms;
+  p->has_tmaps = false;
+  if (page_size == 64 && (head_dim == 128 || head_dim == 256)) {
+    const size_t rows = (size_t)n_layers * n_pages * n_kv_heads * page_size;
+    if (rows >= (1ull << 31) || !make_store_map(&p->tmap_k, k_store, k8, head_dim, rows) ||
+        !make_store_map(&p->tmap_v, v_store, v8, head_dim, rows)) {
+      delete p;
+      return INT8KV_ERR_CUDA;
+    }
+    p->has_tmaps = true;
+  }
   *out = p;
   return INT8KV_OK;
 }
@@ -243,7 +286,7 @@ int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int 
   a.n_splits = n_splits;
   const float scale = softmax_scale != 0.f ? softmax_scale : 1.0f / std::sqrt((float)pool->head_dim);
   a.scale_log2 = scale * 1.4426950408889634f;
-  const cudaError_t e = launch_decode(a, pool->variant, (cudaStream_t)stream);
+  const cudaError_t e = launch_decode(pool, layer, a, (cudaStream_t)stream);
   if (e == cudaErrorNotSupported) return INT8KV_ERR_UNSUPPORTED;
   return e == cudaSuccess ? INT8KV_OK : INT8KV_ERR_CUDA;
 }
@@ -264,10 +307,17 @@ int kv_pool_read_device_error(const int8kv_pool* pool, int32_t* out, void* strea
 
 namespace int8kv {
 
-cudaError_t launch_decode(const DecodeArgs& a, int variant, cudaStream_t stream) {
+cudaError_t launch_decode(const int8kv_pool* pool, int layer, const DecodeArgs& a,
+                          cudaStream_t stream) {
   bool k8, v8;
-  variant_int8(variant, &k8, &v8);
-  return launch_decode_simt(a, k8, v8, stream);
+  variant_int8(pool->variant, &k8, &v8);
+  cudaError_t e;
+  if (pool->has_tmaps && decode_mma_supported(a.pool, a.G))
+    e = launch_decode_mma(a, k8, v8, pool->tmap_k, pool->tmap_v, layer * pool->n_pages, stream);
+  else
+    e = launch_decode_simt(a, k8, v8, stream);
+  if (e != cudaSuccess || a.n_splits == 1) return e;
+  return launch_decode_combine(a, stream);
 }
 
 }  // namespace int8kv

@@ -1,0 +1,554 @@
+// Split-K GQA decode attention over the int8 cache on the tensor cores
+// (mma.sync m16n8k16, f16 operands, f32 accumulation), pages staged by TMA.
+//
+// Method: genie-ai-runtime v1.3.0 "split-K decode attention" (the key range of
+// a head is cut into n_splits pieces; each block computes an online-softmax
+// partial, a reduce combines them per head) over a cache dequantized on load
+// (genie-ai-runtime v0.1.0-alpha.12 "Path I series" I3: every cached row has
+// its own scale; Strata pull request #2698 "What it does": one scale per 64
+// values, k8v8 / one-store variants).
+//
+// Why tensor cores in a bandwidth-bound kernel: one block serves the G <= 8
+// query heads of its kv head, so every cached byte feeds 2*G multiply-adds
+// (G for q.k, G for p.v).  At G = 8 and head_dim 256 that is ~7.8 FMA per byte,
+// more than the CUDA cores can retire at HBM speed (152 SMs x 128 FMA/clk is
+// ~5 TB/s worth at 1.9 GHz before any conversion work).  Both products are
+// genuine dense contractions over the G heads (q.K^T: [16 tok x D] x [D x 8
+// heads]; P.V: [D x 16 tok] x [16 tok x 8 heads]), so they go to mma.sync.
+//
+// Exactness.  int8 codes (|c| <= 127) and fp16 q are exact in fp16 and their
+// products are exact in the f32 accumulator; the K scales (and softmax scale)
+// are applied per (token, 64-value group) in f32 after each 64-wide partial
+// dot.  On the P.V side the weight of token j for output dims of V group g is
+// P'_jg = p_j * s_v(j, g) (exp-weights times the V scale); it is fed to the
+// tensor core as an fp16 hi + lo pair (two MMAs), which keeps ~22 bits.  To keep
+// P' away from fp16's subnormal range whatever the magnitude of V, each warp
+// tracks a power of two 2^e_g >= every V scale of group g it has seen and
+// feeds P' * 2^(14 - e_g) < 2^14; when e_g grows, the group's accumulators
+// are rescaled by the exact power-of-two ratio (the same move the online
+// softmax makes with its running max).
+//
+// Data movement.  A block owns a contiguous run of pages of one (sequence, kv
+// head).  One producer lane streams each page (K codes, V codes: 64 rows x
+// 128 B boxes with the 128-byte swizzle; scales: one bulk copy each) into a
+// ring of stages, completion counted on mbarriers; four consumer warps take
+// one 16-token tile of every page.  The swizzle plus the row/slot permutations
+// below make every shared-memory fragment load bank-conflict free.
+//
+// Layout of the work inside a 16-token tile (r = lane/4, t = lane%4):
+//  q.K^T : A = K rows.  MMA row r <-> token RHO(r), row r+8 <-> 8+RHO(r).
+//          K int8: thread loads 16 code bytes per 64-dim group; k-step i uses
+//          bytes 4i..4i+3, slots (2t, 2t+1, 2t+8, 2t+9) <-> bytes (0, 2, 1, 3),
+//          and q's B fragment follows the same permutation.  K fp16: ldmatrix.
+//  P.V   : A = V^T, B = P'^T.  Slots (2t, 2t+1) <-> tokens (RHO(2t), RHO(2t+1)),
+//          (2t+8, 2t+9) <-> 8 + the same; the q.K^T accumulator fragment, cast
+//          to f16x2, becomes this B fragment with one movmatrix transpose.
+//          V int8: M-tile m of group g holds dims 64g + 8r + 2m (row r) and
+//          +1 (row r+8).  V fp16: ldmatrix.trans, dims d0 + r and d0 + 8 + r.
+// RHO = (0,4,2,6,5,1,7,3) makes both the q.K^T and P.V loads conflict free and
+// lines the transposed fragment up with the P.V slots.
+
+#include <climits>
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "decode_common.cuh"
+#include "ptx.cuh"
+
+namespace int8kv {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kPage = 64;                  // page size served by this kernel
+constexpr int kBoxBytes = kPage * 128;     // one swizzled TMA box: 64 rows x 128 B
+constexpr uint32_t kMaxPolls = 1u << 26;   // bounded mbarrier waits (seconds)
+constexpr int kPShift = 14;                // P' is fed to the MMA as P' * 2^(14 - e) < 2^14
+
+__device__ __forceinline__ int rho(int r) { return (0x37156240u >> (4 * r)) & 0xF; }
+
+template <int D, bool KI8, bool VI8>
+struct Layout {
+  static constexpr int KBYTES = KI8 ? D * kPage : 2 * D * kPage;
+  static constexpr int VBYTES = VI8 ? D * kPage : 2 * D * kPage;
+  static constexpr int KBOXES = KBYTES / kBoxBytes;
+  static constexpr int VBOXES = VBYTES / kBoxBytes;
+  static constexpr int SCALE_BYTES = kPage * 4 * 2;   // up to 4 groups per row
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = KBYTES;
+  static constexpr int KS_OFF = KBYTES + VBYTES;
+  static constexpr int VS_OFF = KS_OFF + (KI8 ? SCALE_BYTES : 0);
+  static constexpr int RAW = VS_OFF + (VI8 ? SCALE_BYTES : 0);
+  static constexpr int STAGE = (RAW + 1023) / 1024 * 1024;
+  static constexpr int NS_FIT = (110 * 1024) / STAGE;
+  static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 4 ? 4 : NS_FIT);
+  static constexpr int MERGE = kConsumerWarps * 8 * D * 4;   // epilogue buffer (reuses stages)
+  static constexpr int BARS = NS * STAGE;
+  static constexpr int SMEM = 1024 + BARS + 2 * NS * 8 + NS * 4 + 64;
+  static_assert(MERGE <= NS * STAGE, "merge buffer must fit in the stages");
+};
+
+__device__ __forceinline__ uint32_t lop_i8pair(uint32_t x) {
+  // bytes 0 and 2 of x (int8 codes) -> fp16 pair (1152 + c): 0x6400 | (c ^ 0x80)
+  return (x & 0x00FF00FFu) ^ 0x64806480u;
+}
+
+__device__ __forceinline__ uint32_t sub1152(uint32_t h2) {
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h2), __half2half2(__ushort_as_half(0x6480)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Codes at byte k of W0 and W1 -> exact f16x2 (lo = W0's, hi = W1's).
+__device__ __forceinline__ uint32_t v_pair(uint32_t w0, uint32_t w1, int k) {
+  const uint32_t sel = (uint32_t)k | ((uint32_t)k << 4) | ((uint32_t)(4 + k) << 8) |
+                       ((uint32_t)(4 + k) << 12);
+  return sub1152(lop_i8pair(ptx::prmt(w0, w1, sel)));
+}
+
+__device__ __forceinline__ float pow2f(int e) {   // 2^e for e in [-126, 127]
+  return __uint_as_float((uint32_t)(127 + e) << 23);
+}
+
+__device__ __forceinline__ int exponent_of(float x) {   // floor(log2 x), x > 0 normal
+  return (int)((__float_as_uint(x) >> 23) & 0xFF) - 127;
+}
+
+template <int D, bool KI8, bool VI8>
+__global__ void __launch_bounds__(kThreads, 2)
+decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, int layer_page0) {
+  using LY = Layout<D, KI8, VI8>;
+  constexpr int KSTEPS = D / 16;     // 16-dim k-steps of q.K^T
+  constexpr int MACROS = D / 64;     // 64-dim groups
+  constexpr int MTILES = D / 16;     // 16-dim M-tiles of P.V
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = (uint64_t*)(smem + LY::BARS);
+  uint64_t* empty = full + LY::NS;
+  int* stage_page = (int*)(empty + LY::NS);
+  __shared__ float s_m[kConsumerWarps][8], s_l[kConsumerWarps][8];
+  __shared__ int s_abort;
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const PoolView& p = a.pool;
+  const int G = a.G, ng = p.ng, gs = p.gs;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < LY::NS; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], kConsumerWarps);
+    }
+    s_abort = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  // Launched as a programmatic dependent: no global memory is read before the
+  // preceding kernel of the stream has completed.
+  ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
+
+  const int L = clamp_length(__ldg(a.seq_lens + b), a.max_pages, p);
+  const int lo_pos = a.window > 0 ? max(0, L - a.window) : 0;
+  int j0, j1;
+  split_range(lo_pos, L, split, a.n_splits, kPage, &j0, &j1);
+  const int p_first = j0 / kPage;
+  const int n_pg = j1 > j0 ? (j1 - 1) / kPage - p_first + 1 : 0;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tmk);
+      ptx::prefetch_tensormap(&tmv);
+      const int32_t* ptrow = a.page_table + (size_t)b * a.max_pages;
+      const uint32_t tx = LY::KBYTES + LY::VBYTES + (KI8 ? kPage * ng * 2 : 0) +
+                          (VI8 ? kPage * ng * 2 : 0);
+      for (int i = 0; i < n_pg; ++i) {
+        const int st = i % LY::NS;
+        if (i >= LY::NS && !ptx::mbar_wait(&empty[st], ((i / LY::NS) - 1) & 1, kMaxPolls)) {
+          flag_error(p.err, INT8KV_DEVERR_TIMEOUT);
+          s_abort = 1;
+          break;
+        }
+        const int page = lookup_page(ptrow, p_first + i, a.max_pages, p);
+        stage_page[st] = page;
+        if (page < 0) {
+          ptx::mbar_arrive(&full[st]);
+          continue;
+        }
+        ptx::mbar_arrive_expect_tx(&full[st], tx);
+        unsigned char* sb = smem + st * LY::STAGE;
+        const int row = ((layer_page0 + page) * p.Hkv + kvh) * kPage;
+        constexpr int KX = KI8 ? 128 : 64;   // box width in elements
+        constexpr int VX = VI8 ? 128 : 64;
+#pragma unroll
+        for (int bx = 0; bx < LY::KBOXES; ++bx)
+          ptx::tma_load_2d(sb + LY::K_OFF + bx * kBoxBytes, &tmk, bx * KX, row, &full[st]);
+#pragma unroll
+        for (int bx = 0; bx < LY::VBOXES; ++bx)
+          ptx::tma_load_2d(sb + LY::V_OFF + bx * kBoxBytes, &tmv, bx * VX, row, &full[st]);
+        const size_t srow = ((size_t)page * p.Hkv + kvh) * kPage * ng;
+        if (KI8) ptx::bulk_load(sb + LY::KS_OFF, p.ks + srow, kPage * ng * 2, &full[st]);
+        if (VI8) ptx::bulk_load(sb + LY::VS_OFF, p.vs + srow, kPage * ng * 2, &full[st]);
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- consumers
+  const int r = lane >> 2, t = lane & 3;
+  float o[MTILES][4];
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  int vexp[4] = {INT_MIN, INT_MIN, INT_MIN, INT_MIN};   // per V group: 2^vexp > every scale seen
+#pragma unroll
+  for (int i = 0; i < MTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+  if (warp < kConsumerWarps) {
+    // q of head r (B operand columns = heads), in the slot order of the K loads
+    uint32_t qf[KSTEPS][2];
+    {
+      const bool live = r < G;
+      const __half* qh = reinterpret_cast<const __half*>(a.q) + ((size_t)b * a.H + (size_t)kvh * G +
+                                                                 (live ? r : 0)) * D;
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        int d0, d1, d2, d3;
+        if (KI8) {
+          d0 = (ks >> 2) * 64 + 16 * t + 4 * (ks & 3);
+          d1 = d0 + 2;
+          d2 = d0 + 1;
+          d3 = d0 + 3;
+        } else {
+          d0 = ks * 16 + 2 * t;
+          d1 = d0 + 1;
+          d2 = d0 + 8;
+          d3 = d0 + 9;
+        }
+        const __half z = __ushort_as_half(0);
+        const __half2 x = live ? __halves2half2(qh[d0], qh[d1]) : __halves2half2(z, z);
+        const __half2 y = live ? __halves2half2(qh[d2], qh[d3]) : __halves2half2(z, z);
+        qf[ks][0] = *reinterpret_cast<const uint32_t*>(&x);
+        qf[ks][1] = *reinterpret_cast<const uint32_t*>(&y);
+      }
+    }
+    const int rowA = rho(r), rowB = rho(r) + 8;          // q.K^T rows of this thread
+    const int tokS0 = rho(2 * t), tokS1 = rho(2 * t + 1);  // P.V slot tokens of this thread
+
+    for (int i = 0; i < n_pg; ++i) {
+      const int st = i % LY::NS;
+      if (!ptx::mbar_wait(&full[st], (i / LY::NS) & 1, kMaxPolls)) {
+        flag_error(p.err, INT8KV_DEVERR_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      const int page = stage_page[st];
+      const int tile0 = (p_first + i) * kPage + warp * 16;   // position of the tile's token 0
+      const bool any = page >= 0 && tile0 < j1 && tile0 + 16 > j0;
+      if (any) {
+        const unsigned char* sb = smem + st * LY::STAGE;
+        const uint32_t kbase = ptx::smem_u32(sb + LY::K_OFF);
+        const uint32_t vbase = ptx::smem_u32(sb + LY::V_OFF);
+        const __half* ks_s = reinterpret_cast<const __half*>(sb + LY::KS_OFF);
+        const __half* vs_s = reinterpret_cast<const __half*>(sb + LY::VS_OFF);
+        const int trA = warp * 16 + rowA, trB = warp * 16 + rowB;   // rows within the page
+        const bool vA = tile0 + rowA >= j0 && tile0 + rowA < j1;
+        const bool vB = tile0 + rowB >= j0 && tile0 + rowB < j1;
+        const bool full_tile = tile0 >= j0 && tile0 + 16 <= j1;
+
+        // ---- scores: s[0..1] token A heads (2t, 2t+1); s[2..3] token B
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int mc = 0; mc < MACROS; ++mc) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          if constexpr (KI8) {
+            const int box = mc >> 1, chunk = (mc & 1) * 4 + t;
+            const uint32_t bb = kbase + box * kBoxBytes;
+            const uint4 wa = ptx::lds128(bb + trA * 128 + ((chunk ^ (trA & 7)) << 4));
+            const uint4 wb = ptx::lds128(bb + trB * 128 + ((chunk ^ (trB & 7)) << 4));
+            const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
+            const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+              uint32_t af[4];
+              af[0] = sub1152(lop_i8pair(wA[ii]));
+              af[1] = sub1152(lop_i8pair(wB[ii]));
+              af[2] = sub1152(lop_i8pair(wA[ii] >> 8));
+              af[3] = sub1152(lop_i8pair(wB[ii] >> 8));
+              ptx::mma_f16(acc, af, qf[mc * 4 + ii][0], qf[mc * 4 + ii][1]);
+            }
+            const int grp = (mc * 64) / gs;
+            const float sa = __half2float(ks_s[trA * ng + grp]) * a.scale_log2;
+            const float sbb = __half2float(ks_s[trB * ng + grp]) * a.scale_log2;
+            s[0] = fmaf(acc[0], sa, s[0]);
+            s[1] = fmaf(acc[1], sa, s[1]);
+            s[2] = fmaf(acc[2], sbb, s[2]);
+            s[3] = fmaf(acc[3], sbb, s[3]);
+          } else {
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+              const int k0 = mc * 64 + ii * 16;          // 16 dims of this k-step
+              const int q4 = lane >> 3, rr = lane & 7;
+              const int tok = warp * 16 + rho(rr) + 8 * (q4 & 1);
+              const int c = ((k0 & 63) >> 3) + (q4 >> 1);
+              uint32_t af[4];
+              ptx::ldmatrix_x4(af, kbase + (k0 >> 6) * kBoxBytes + tok * 128 + ((c ^ (tok & 7)) << 4));
+              ptx::mma_f16(acc, af, qf[mc * 4 + ii][0], qf[mc * 4 + ii][1]);
+            }
+            s[0] += acc[0];
+            s[1] += acc[1];
+            s[2] += acc[2];
+            s[3] += acc[3];
+          }
+        }
+        if constexpr (!KI8) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) s[k] *= a.scale_log2;
+        }
+        if (!vA) s[0] = s[1] = -INFINITY;
+        if (!vB) s[2] = s[3] = -INFINITY;
+
+        // ---- online softmax (base 2) per head column
+        float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = exp2f(m0 - base0), al1 = exp2f(m1 - base1);
+        float pr[4];
+        pr[0] = exp2f(s[0] - base0);
+        pr[1] = exp2f(s[1] - base1);
+        pr[2] = exp2f(s[2] - base0);
+        pr[3] = exp2f(s[3] - base1);
+        l0 = fmaf(l0, al0, pr[0] + pr[2]);
+        l1 = fmaf(l1, al1, pr[1] + pr[3]);
+        m0 = mn0;
+        m1 = mn1;
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+          for (int j = 0; j < MTILES; ++j) {
+            o[j][0] *= al0;
+            o[j][1] *= al1;
+            o[j][2] *= al0;
+            o[j][3] *= al1;
+          }
+        }
+
+        // ---- P.V, one V scale group at a time
+        const int ngv = VI8 ? ng : 1;
+        const int macros_per_group = VI8 ? gs / 64 : MACROS;
+        for (int g = 0; g < ngv; ++g) {
+          float wA = 0.f, wB = 0.f;     // token weight: s_v * 2^(kPShift - e_g)
+          if constexpr (VI8) {
+            const float sva = vA ? __half2float(vs_s[trA * ng + g]) : 0.f;
+            const float svb = vB ? __half2float(vs_s[trB * ng + g]) : 0.f;
+            const float cap = vexp[g] == INT_MIN ? 0.f : pow2f(vexp[g]);
+            if (__any_sync(0xffffffffu, (sva >= cap && sva > 0.f) || (svb >= cap && svb > 0.f))) {
+              float mx = fmaxf(sva, svb);
+#pragma unroll
+              for (int off = 1; off < 32; off <<= 1)
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+              const int ne = exponent_of(mx) + 1;
+              if (vexp[g] != INT_MIN) {
+                const float f = pow2f(vexp[g] - ne);
+                const int j_lo = g * macros_per_group * 4, j_hi = j_lo + macros_per_group * 4;
+#pragma unroll
+                for (int j = 0; j < MTILES; ++j)
+                  if (j >= j_lo && j < j_hi) {
+                    o[j][0] *= f;
+                    o[j][1] *= f;
+                    o[j][2] *= f;
+                    o[j][3] *= f;
+                  }
+              }
+              vexp[g] = ne;
+            }
+            const float sh = vexp[g] == INT_MIN ? 0.f : pow2f(kPShift - vexp[g]);
+            wA = sva * sh;
+            wB = svb * sh;
+          } else {
+            wA = vA ? pow2f(kPShift) : 0.f;
+            wB = vB ? pow2f(kPShift) : 0.f;
+          }
+          const float p0 = pr[0] * wA, p1 = pr[1] * wA, p2 = pr[2] * wB, p3 = pr[3] * wB;
+          const uint32_t h01 = ptx::pack_f16x2(p0, p1), h23 = ptx::pack_f16x2(p2, p3);
+          const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+          const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+          const uint32_t e01 = ptx::pack_f16x2(p0 - f01.x, p1 - f01.y);
+          const uint32_t e23 = ptx::pack_f16x2(p2 - f23.x, p3 - f23.y);
+          const uint32_t bh0 = ptx::movmatrix_trans(h01), bh1 = ptx::movmatrix_trans(h23);
+          const uint32_t bl0 = ptx::movmatrix_trans(e01), bl1 = ptx::movmatrix_trans(e23);
+
+#pragma unroll
+          for (int mc = 0; mc < MACROS; ++mc) {
+            if (mc < g * macros_per_group || mc >= (g + 1) * macros_per_group) continue;
+            if constexpr (VI8) {
+              const int box = mc >> 1;
+              const uint32_t bb = vbase + box * kBoxBytes;
+              const int c16 = (mc & 1) * 4 + (r >> 1), h8 = (r & 1) << 3;
+              const int tk[4] = {warp * 16 + tokS0, warp * 16 + tokS1, warp * 16 + 8 + tokS0,
+                                 warp * 16 + 8 + tokS1};
+              uint2 w[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                w[j] = ptx::lds64(bb + tk[j] * 128 + (((c16 ^ (tk[j] & 7)) << 4) | h8));
+#pragma unroll
+              for (int mt = 0; mt < 4; ++mt) {
+                const int kb = 2 * (mt & 1);
+                const uint32_t x0 = (mt >> 1) ? w[0].y : w[0].x, x1 = (mt >> 1) ? w[1].y : w[1].x;
+                const uint32_t x2 = (mt >> 1) ? w[2].y : w[2].x, x3 = (mt >> 1) ? w[3].y : w[3].x;
+                uint32_t af[4];
+                af[0] = v_pair(x0, x1, kb);
+                af[1] = v_pair(x0, x1, kb + 1);
+                af[2] = v_pair(x2, x3, kb);
+                af[3] = v_pair(x2, x3, kb + 1);
+                ptx::mma_f16(o[mc * 4 + mt], af, bh0, bh1);
+                ptx::mma_f16(o[mc * 4 + mt], af, bl0, bl1);
+              }
+            } else {
+#pragma unroll
+              for (int mt = 0; mt < 4; ++mt) {
+                const int d0 = mc * 64 + mt * 16;
+                const int q4 = lane >> 3, rr = lane & 7;
+                const int tok = warp * 16 + rho(rr) + 8 * (q4 >> 1);
+                const int c = ((d0 & 63) >> 3) + (q4 & 1);
+                uint32_t af[4];
+                ptx::ldmatrix_x4_trans(af, vbase + (d0 >> 6) * kBoxBytes + tok * 128 +
+                                               ((c ^ (tok & 7)) << 4));
+                if (!full_tile) {
+                  // rows outside [j0, j1) may hold any bits: zero them (P' is 0 there)
+                  const bool ok0 = tile0 + tokS0 >= j0 && tile0 + tokS0 < j1;
+                  const bool ok1 = tile0 + tokS1 >= j0 && tile0 + tokS1 < j1;
+                  const bool ok2 = tile0 + 8 + tokS0 >= j0 && tile0 + 8 + tokS0 < j1;
+                  const bool ok3 = tile0 + 8 + tokS1 >= j0 && tile0 + 8 + tokS1 < j1;
+                  const uint32_t mlo = (ok0 ? 0x0000FFFFu : 0u) | (ok1 ? 0xFFFF0000u : 0u);
+                  const uint32_t mhi = (ok2 ? 0x0000FFFFu : 0u) | (ok3 ? 0xFFFF0000u : 0u);
+                  af[0] &= mlo;
+                  af[1] &= mlo;
+                  af[2] &= mhi;
+                  af[3] &= mhi;
+                }
+                ptx::mma_f16(o[mc * 4 + mt], af, bh0, bh1);
+                ptx::mma_f16(o[mc * 4 + mt], af, bl0, bl1);
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&empty[st]);
+    }
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 8);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
+  }
+  __syncthreads();   // every stage consumed: the stage memory becomes the merge buffer
+
+  float* s_o = reinterpret_cast<float*>(smem);   // [warp][head 8][D]
+  if (warp < kConsumerWarps) {
+    if (r == 0) {
+      s_m[warp][2 * t] = m0;
+      s_m[warp][2 * t + 1] = m1;
+      s_l[warp][2 * t] = l0;
+      s_l[warp][2 * t + 1] = l1;
+    }
+#pragma unroll
+    for (int j = 0; j < MTILES; ++j) {
+      const int mc = j >> 2, mt = j & 3;
+      int dx, dy;
+      float u;
+      if constexpr (VI8) {
+        dx = mc * 64 + 8 * r + 2 * mt;
+        dy = dx + 1;
+        const int g = (mc * 64) / gs;
+        u = vexp[g] == INT_MIN ? 0.f : pow2f(vexp[g] - kPShift);
+      } else {
+        dx = mc * 64 + mt * 16 + r;
+        dy = dx + 8;
+        u = pow2f(-kPShift);
+      }
+      float* h0 = s_o + ((size_t)warp * 8 + 2 * t) * D;
+      float* h1 = h0 + D;
+      h0[dx] = o[j][0] * u;
+      h1[dx] = o[j][1] * u;
+      h0[dy] = o[j][2] * u;
+      h1[dy] = o[j][3] * u;
+    }
+  }
+  __syncthreads();
+
+  for (int e = threadIdx.x; e < G * D; e += kThreads) {
+    const int g = e / D, d = e - g * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w][g]);
+    float Ls = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float f = exp2f(s_m[w][g] - M);
+        Ls = fmaf(s_l[w][g], f, Ls);
+        O = fmaf(s_o[((size_t)w * 8 + g) * D + d], f, O);
+      }
+    }
+    const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
+    if (a.n_splits == 1) {
+      a.out[h * D + d] = Ls > 0.f ? O / Ls : 0.f;
+    } else {
+      a.ws.part_o[(h * a.n_splits + split) * D + d] = O;
+      if (d == 0) a.ws.part_ml[h * a.n_splits + split] = make_float2(M, Ls);
+    }
+  }
+}
+
+template <int D, bool KI8, bool VI8>
+cudaError_t launch_typed(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                         int layer_page0, cudaStream_t stream) {
+  using LY = Layout<D, KI8, VI8>;
+  auto kern = decode_mma_kernel<D, KI8, VI8>;
+  static bool configured = false;   // per instantiation; attribute is per device function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         LY::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_splits, a.pool.Hkv, a.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = LY::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, tmk, tmv, layer_page0);
+}
+
+}  // namespace
+
+bool decode_mma_supported(const PoolView& p, int G) {
+  return G <= 8 && p.ps == kPage && (p.D == 128 || p.D == 256) && p.gs >= 64 && p.gs % 64 == 0;
+}
+
+cudaError_t launch_decode_mma(const DecodeArgs& a, bool k8, bool v8, const CUtensorMap& tmk,
+                              const CUtensorMap& tmv, int layer_page0, cudaStream_t stream) {
+  if (a.pool.D == 256) {
+    if (k8 && v8) return launch_typed<256, true, true>(a, tmk, tmv, layer_page0, stream);
+    if (k8) return launch_typed<256, true, false>(a, tmk, tmv, layer_page0, stream);
+    return launch_typed<256, false, true>(a, tmk, tmv, layer_page0, stream);
+  }
+  if (k8 && v8) return launch_typed<128, true, true>(a, tmk, tmv, layer_page0, stream);
+  if (k8) return launch_typed<128, true, false>(a, tmk, tmv, layer_page0, stream);
+  return launch_typed<128, false, true>(a, tmk, tmv, layer_page0, stream);
+}
+
+}  // namespace int8kv

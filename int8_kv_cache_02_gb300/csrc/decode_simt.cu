@@ -11,9 +11,8 @@
 // lane l owns dims [l*VPL, (l+1)*VPL) of every row, so a row is one coalesced
 // warp access.  Scores are reduced with warp shuffles; softmax runs in base 2
 // (scale folded with log2 e).  The warps' partials are merged in shared memory;
-// with n_splits > 1 the block stores its partial, and the last block of a
-// (sequence, kv head) to arrive (atomic ticket, no waiting) combines all splits
-// and resets the ticket.
+// with n_splits > 1 the block stores its partial and the combine kernel
+// (decode_combine.cu) reduces the splits.
 //
 // This kernel is the general path (any G <= 8, head_dim 64/128/256, every
 // store variant); the tensor-core kernel in decode_mma.cu serves the shapes it
@@ -64,7 +63,6 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeArgs a, 
 
   __shared__ float s_m[kWarps][8], s_l[kWarps][8];
   __shared__ float s_o[kWarps][8][D];
-  __shared__ int s_last;
 
   float qr[8][VPL];
 #pragma unroll
@@ -149,20 +147,6 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeArgs a, 
       if (d == 0) a.ws.part_ml[h * a.n_splits + split] = make_float2(M, Ls);
     }
   }
-  if (a.n_splits == 1) return;
-
-  // last block of this (sequence, kv head) combines the splits
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned t = atomicAdd(a.ws.counters + (size_t)b * p.Hkv + kvh, 1u);
-    s_last = (t == (unsigned)a.n_splits - 1);
-    __threadfence();
-  }
-  __syncthreads();
-  if (!s_last) return;
-  combine_splits_block(a, b, kvh, &s_o[0][0][0]);
-  if (threadIdx.x == 0) a.ws.counters[(size_t)b * p.Hkv + kvh] = 0u;
 }
 
 }  // namespace

@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "int8kv.h"
@@ -19,6 +20,9 @@ struct int8kv_pool {
   int32_t* dev_error;
   int device;        // CUDA device the pool was created on
   int num_sms;       // its SM count (split heuristic)
+  bool has_tmaps;    // TMA descriptors below are valid (shapes the tensor-core decode serves)
+  CUtensorMap tmap_k;              // K store as [rows][head_dim], 64-row x 128-byte swizzled boxes
+  CUtensorMap tmap_v;              // V store, same
 };
 
 namespace int8kv {
@@ -52,11 +56,10 @@ inline PoolView layer_view(const int8kv_pool* p, int layer) {
 }
 
 // Workspace of the split-K decode: partial (m, l) and unnormalised o per
-// (sequence, query head, split), and one arrival counter per (sequence, kv head).
+// (sequence, query head, split).
 struct DecodeWorkspace {
   float* part_o;      // [B][H][n_splits][D]
   float2* part_ml;    // [B][H][n_splits]
-  unsigned* counters; // [B][Hkv]
 };
 
 size_t decode_workspace_layout(int B, int H, int Hkv, int D, int n_splits,
@@ -78,7 +81,9 @@ cudaError_t launch_quant_append(const PoolView& pool, const uint16_t* k_new, con
                                 const int32_t* page_table, int max_pages, bool k_int8,
                                 bool v_int8, cudaStream_t stream);
 
-// Returns cudaErrorNotSupported when no kernel is built for the shape.
-cudaError_t launch_decode(const DecodeArgs& a, int variant, cudaStream_t stream);
+// Partial kernel (tensor-core when the shape allows, else CUDA-core) and, with
+// n_splits > 1, the combine.  cudaErrorNotSupported when no kernel fits.
+cudaError_t launch_decode(const int8kv_pool* pool, int layer, const DecodeArgs& a,
+                          cudaStream_t stream);
 
 }  // namespace int8kv

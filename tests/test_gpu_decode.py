@@ -203,3 +203,79 @@ def test_long128k_workload(variant):
     gu.fill_sequence(dev, orc, 0, w["k"], w["v"], pt[0])
     ref = _oracle(orc, 0, w["q"], [L], pt)
     gu.assert_attention_close(_decode(dev, 0, w["q"], [L], pt), ref, f"128k v{variant}")
+
+
+# --------------------------------------------------------------------------------------
+# Tensor-core path specifics (page size 64, head_dim 128/256, groups of >= 64 values)
+
+@pytest.mark.parametrize("G", [1, 3, 5, 8])
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_mma_path_head_counts(G, variant):
+    Hkv = 2
+    lens = [517, 64]
+    q, pt, dev, orc = _setup(300 + G + 10 * variant, 2, G * Hkv, Hkv, 256, 64, lens, variant,
+                             outliers=True)
+    for ns in (1, 5):
+        out = _decode(dev, 0, q, lens, pt, n_splits=ns)
+        gu.assert_attention_close(out, _oracle(orc, 0, q, lens, pt), f"G={G} v={variant} ns={ns}")
+
+
+@pytest.mark.parametrize("gs", [64, 128, 256])
+def test_mma_path_group_sizes(gs):
+    lens = [1000]
+    q, pt, dev, orc = _setup(400 + gs, 1, 16, 2, 256, gs, lens, 0, outliers=True)
+    out = _decode(dev, 0, q, lens, pt, n_splits=3)
+    gu.assert_attention_close(out, _oracle(orc, 0, q, lens, pt), f"gs={gs}")
+
+
+@pytest.mark.parametrize("vmag", [1e-6, 1e-3, 3e2, 6e4])
+@pytest.mark.parametrize("variant", [0, 2])
+def test_mma_path_value_magnitudes(vmag, variant):
+    """V from 1e-6 (fp16 subnormal range) to 6e4 (near fp16 max): the P' range shift
+    keeps the hi/lo weights normal whatever the V scale."""
+    L, Hkv, D = 700, 2, 128
+    g = torch.Generator().manual_seed(int(vmag * 1e6) % 1000 + variant)
+    q = inputs.normal_f16((1, 8, D), g)
+    k = inputs.normal_f16((L, Hkv, D), g)
+    v = (torch.randn((L, Hkv, D), generator=g) * vmag).clamp(-65000, 65000).to(torch.float16)
+    pt, n_pages = inputs.page_table([L], 64, seed=4)
+    dev, orc = gu.make_pools(1, Hkv, D, 64, 64, n_pages, variant)
+    gu.fill_sequence(dev, orc, 0, k, v, pt[0])
+    ref = _oracle(orc, 0, q, [L], pt)
+    for ns in (1, 4):
+        gu.assert_attention_close(_decode(dev, 0, q, [L], pt, n_splits=ns) / vmag, ref / vmag,
+                                  f"vmag {vmag}")
+
+
+def test_mma_path_v_scales_growing_along_the_sequence():
+    """V scales spanning 2^20 across positions, growing and shrinking, so the running
+    power-of-two range of every warp is raised many times."""
+    L, Hkv, D = 1024, 2, 256
+    g = torch.Generator().manual_seed(77)
+    q = inputs.normal_f16((1, 16, D), g)
+    k = inputs.normal_f16((L, Hkv, D), g)
+    ramp = torch.pow(2.0, torch.linspace(-12, 8, L)).roll(300)
+    v = (torch.randn((L, Hkv, D), generator=g) * ramp[:, None, None]).to(torch.float16)
+    pt, n_pages = inputs.page_table([L], 64, seed=5)
+    dev, orc = gu.make_pools(1, Hkv, D, 64, 64, n_pages, 0)
+    gu.fill_sequence(dev, orc, 0, k, v, pt[0])
+    ref = _oracle(orc, 0, q, [L], pt)
+    for ns in (1, 2, 7):
+        gu.assert_attention_close(_decode(dev, 0, q, [L], pt, n_splits=ns), ref, f"ns {ns}")
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_mma_path_ignores_garbage_beyond_the_context(variant):
+    """Slots past the sequence end of an fp16 store hold NaN / Inf bit patterns."""
+    from int8_kv_cache_02_gb300 import binding
+    L = 100
+    q, pt, dev, orc = _setup(501, 1, 16, 2, 256, 64, [L], variant)
+    store = dev.v_store if variant == 1 else dev.k_store
+    raw = store.view(torch.int16)
+    last = int(pt[0, 1])
+    raw[0, last, :, L - 64:, :] = 0x7E00            # NaN in fp16, in the unwritten slots
+    raw[0, last, :, 60 + L - 64:, :] = 0x7C00       # +Inf
+    out = _decode(dev, 0, q, [L], pt, n_splits=1)
+    assert np.isfinite(out).all()
+    gu.assert_attention_close(out, _oracle(orc, 0, q, [L], pt), "garbage")
+    assert binding.kv_pool_read_device_error(dev) == 0
