@@ -64,7 +64,7 @@ constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kPage = 64;                  // page size served by this kernel
 constexpr int kBoxBytes = kPage * 128;     // one swizzled TMA box: 64 rows x 128 B
-constexpr uint32_t kMaxPolls = 1u << 26;   // bounded mbarrier waits (seconds)
+constexpr uint32_t kMaxPolls = 1u << 22;   // bounded mbarrier waits (well over any copy time)
 constexpr int kPShift = 14;                // P' is fed to the MMA as P' * 2^(14 - e) < 2^14
 
 __device__ __forceinline__ int rho(int r) { return (0x37156240u >> (4 * r)) & 0xF; }
@@ -513,12 +513,14 @@ cudaError_t launch_typed(const DecodeArgs& a, const CUtensorMap& tmk, const CUte
                          int layer_page0, cudaStream_t stream) {
   using LY = Layout<D, KI8, VI8>;
   auto kern = decode_mma_kernel<D, KI8, VI8>;
-  static bool configured = false;   // per instantiation; attribute is per device function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         LY::SMEM);
+  static bool configured[64] = {};   // per device: the attribute belongs to the device's function
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM);
     if (e != cudaSuccess) return e;
-    configured = true;
+    if (dev < 64) configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_splits, a.pool.Hkv, a.B);
