@@ -485,6 +485,8 @@ def main():
     ap.add_argument("--copies", type=int, default=0, help="pool copies (0: enough to defeat L2)")
     ap.add_argument("--no-extra", action="store_true", help="skip the 128K measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--extra-only", action="store_true",
+                    help="run only the 128K measurements and print them (profiling aid)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -499,7 +501,14 @@ def main():
         else:
             dist.init_process_group("gloo")
     try:
-        if args.impl == "reference":
+        if args.extra_only:
+            import torch
+
+            from int8_kv_cache_02_gb300 import build
+            build.build()
+            torch.cuda.set_device(local)
+            print(json.dumps(run_extra(args)), flush=True)
+        elif args.impl == "reference":
             run_reference(args, rank, world, local)
         else:
             run_ours(args, rank, world, local)

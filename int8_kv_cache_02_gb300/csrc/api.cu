@@ -225,8 +225,9 @@ int attn_decode_n_splits(int batch, int n_kv_heads, int max_ctx, int page_size, 
     return INT8KV_ERR_CUDA;
   const long long units = (long long)batch * n_kv_heads;
   const int pages = max_ctx > 0 ? (max_ctx + page_size - 1) / page_size : 1;
-  // Two resident blocks per SM worth of (sequence, kv head, split) blocks.
-  const long long target = 2LL * sms;
+  // Three resident blocks per SM worth of (sequence, kv head, split) blocks
+  // (the tensor-core decode kernel fits three per SM).
+  const long long target = 3LL * sms;
   long long n = (target + units - 1) / units;
   if (n > pages) n = pages;
   if (n > kMaxSplits) n = kMaxSplits;

@@ -7,8 +7,9 @@
 // Splits that saw no key carry (m = -inf, l = 0) and get weight 0; a head with
 // no key at all gets O = 0.
 //
-// Grid (head_dim / 64, n_heads, batch), 64 threads: one output dim per thread,
-// every split's row read coalesced.  Launched as a programmatic dependent of
+// Grid (head_dim / 64, n_heads, batch); eight warps share the splits of one
+// (head, 64-dim slice), each lane two adjacent dims, four independent loads in
+// flight per lane; the eight warp sums meet in shared memory.  Launched as a programmatic dependent of
 // the partial kernel so its launch overlaps the partial kernel's tail; it waits
 // on the grid dependency before touching the partials.
 
@@ -19,11 +20,14 @@
 namespace int8kv {
 namespace {
 
-__global__ void __launch_bounds__(64) decode_combine_kernel(const DecodeArgs a) {
+constexpr int kCombineWarps = 8;   // split range cut into 8 slices, one per warp
+
+__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeArgs a) {
   const int dchunk = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
   const int D = a.pool.D, S = a.n_splits;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ float w[kMaxSplits];
+  __shared__ float2 part[kCombineWarps][32];
   ptx::grid_dependency_wait();
   const size_t h = (size_t)b * a.H + hq;
   const float2* ml = a.ws.part_ml + h * S;
@@ -45,14 +49,37 @@ __global__ void __launch_bounds__(64) decode_combine_kernel(const DecodeArgs a) 
     }
   }
   __syncthreads();
-  const int d = dchunk * 64 + threadIdx.x;
+  // warp `warp` sums splits warp, warp + 8, ...; each lane two adjacent dims
+  const int d = dchunk * 64 + 2 * lane;
   const float* po = a.ws.part_o + h * S * D + d;
-  float O = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const float ws = w[s];
-    if (ws != 0.f) O = fmaf(ws, po[(size_t)s * D], O);
+  float2 acc[4] = {};
+  int s = warp, k = 0;
+  for (; s + 3 * kCombineWarps < S; s += 4 * kCombineWarps) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float2 v = *reinterpret_cast<const float2*>(po + (size_t)(s + u * kCombineWarps) * D);
+      const float ws = w[s + u * kCombineWarps];
+      acc[u].x = fmaf(ws, v.x, acc[u].x);
+      acc[u].y = fmaf(ws, v.y, acc[u].y);
+    }
   }
-  a.out[h * D + d] = O;
+  for (; s < S; s += kCombineWarps, k = (k + 1) & 3) {
+    const float2 v = *reinterpret_cast<const float2*>(po + (size_t)s * D);
+    acc[k].x = fmaf(w[s], v.x, acc[k].x);
+    acc[k].y = fmaf(w[s], v.y, acc[k].y);
+  }
+  part[warp][lane] = make_float2(acc[0].x + acc[1].x + acc[2].x + acc[3].x,
+                                 acc[0].y + acc[1].y + acc[2].y + acc[3].y);
+  __syncthreads();
+  if (warp == 0) {
+    float2 o = part[0][lane];
+#pragma unroll
+    for (int q = 1; q < kCombineWarps; ++q) {
+      o.x += part[q][lane].x;
+      o.y += part[q][lane].y;
+    }
+    *reinterpret_cast<float2*>(a.out + h * D + d) = o;
+  }
 }
 
 }  // namespace
@@ -60,7 +87,7 @@ __global__ void __launch_bounds__(64) decode_combine_kernel(const DecodeArgs a) 
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.pool.D / 64, a.H, a.B);
-  cfg.blockDim = dim3(64);
+  cfg.blockDim = dim3(kCombineWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -61,7 +61,7 @@ namespace int8kv {
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kThreads = kConsumerWarps * 32;
 constexpr int kPage = 64;                  // page size served by this kernel
 constexpr int kBoxBytes = kPage * 128;     // one swizzled TMA box: 64 rows x 128 B
 constexpr uint32_t kMaxPolls = 1u << 22;   // bounded mbarrier waits (well over any copy time)
@@ -82,9 +82,9 @@ struct Layout {
   static constexpr int VS_OFF = KS_OFF + (KI8 ? SCALE_BYTES : 0);
   static constexpr int RAW = VS_OFF + (VI8 ? SCALE_BYTES : 0);
   static constexpr int STAGE = (RAW + 1023) / 1024 * 1024;
-  static constexpr int NS_FIT = (110 * 1024) / STAGE;
+  static constexpr int NS_FIT = (70 * 1024) / STAGE;          // three blocks per SM when it fits
   static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 4 ? 4 : NS_FIT);
-  static constexpr int MERGE = kConsumerWarps * 8 * D * 4;   // epilogue buffer (reuses stages)
+  static constexpr int MERGE = kConsumerWarps * 8 * (D + 1) * 4;   // epilogue buffer (reuses stages)
   static constexpr int BARS = NS * STAGE;
   static constexpr int SMEM = 1024 + BARS + 2 * NS * 8 + NS * 4 + 64;
   static_assert(MERGE <= NS * STAGE, "merge buffer must fit in the stages");
@@ -116,7 +116,35 @@ __device__ __forceinline__ int exponent_of(float x) {   // floor(log2 x), x > 0 
 }
 
 template <int D, bool KI8, bool VI8>
-__global__ void __launch_bounds__(kThreads, 2)
+__device__ __forceinline__ void issue_page(unsigned char* smem, uint64_t* full, int* stage_page,
+                                           int st, int page, int row, const PoolView& p, int kvh,
+                                           const CUtensorMap* tmk, const CUtensorMap* tmv) {
+  using LY = Layout<D, KI8, VI8>;
+  stage_page[st] = page;
+  if (page < 0) {
+    ptx::mbar_arrive(&full[st]);
+    return;
+  }
+  const int ng = p.ng;
+  const uint32_t tx = LY::KBYTES + LY::VBYTES + (KI8 ? kPage * ng * 2 : 0) +
+                      (VI8 ? kPage * ng * 2 : 0);
+  ptx::mbar_arrive_expect_tx(&full[st], tx);
+  unsigned char* sb = smem + st * LY::STAGE;
+  constexpr int KX = KI8 ? 128 : 64;   // box width in elements
+  constexpr int VX = VI8 ? 128 : 64;
+#pragma unroll
+  for (int bx = 0; bx < LY::KBOXES; ++bx)
+    ptx::tma_load_2d(sb + LY::K_OFF + bx * kBoxBytes, tmk, bx * KX, row, &full[st]);
+#pragma unroll
+  for (int bx = 0; bx < LY::VBOXES; ++bx)
+    ptx::tma_load_2d(sb + LY::V_OFF + bx * kBoxBytes, tmv, bx * VX, row, &full[st]);
+  const size_t srow = ((size_t)page * p.Hkv + kvh) * kPage * ng;
+  if (KI8) ptx::bulk_load(sb + LY::KS_OFF, p.ks + srow, kPage * ng * 2, &full[st]);
+  if (VI8) ptx::bulk_load(sb + LY::VS_OFF, p.vs + srow, kPage * ng * 2, &full[st]);
+}
+
+template <int D, bool KI8, bool VI8>
+__global__ void __launch_bounds__(kThreads, 3)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, int layer_page0) {
   using LY = Layout<D, KI8, VI8>;
@@ -129,7 +157,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   uint64_t* empty = full + LY::NS;
   int* stage_page = (int*)(empty + LY::NS);
   __shared__ float s_m[kConsumerWarps][8], s_l[kConsumerWarps][8];
-  __shared__ int s_abort;
+  __shared__ float s_f[kConsumerWarps][8], s_inv[8];
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -141,7 +169,6 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], kConsumerWarps);
     }
-    s_abort = 0;
     ptx::fence_mbar_init();
   }
   __syncthreads();
@@ -157,42 +184,17 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   const int p_first = j0 / kPage;
   const int n_pg = j1 > j0 ? (j1 - 1) / kPage - p_first + 1 : 0;
 
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------- producer
-    if (lane == 0) {
-      ptx::prefetch_tensormap(&tmk);
-      ptx::prefetch_tensormap(&tmv);
-      const int32_t* ptrow = a.page_table + (size_t)b * a.max_pages;
-      const uint32_t tx = LY::KBYTES + LY::VBYTES + (KI8 ? kPage * ng * 2 : 0) +
-                          (VI8 ? kPage * ng * 2 : 0);
-      for (int i = 0; i < n_pg; ++i) {
-        const int st = i % LY::NS;
-        if (i >= LY::NS && !ptx::mbar_wait(&empty[st], ((i / LY::NS) - 1) & 1, kMaxPolls)) {
-          flag_error(p.err, INT8KV_DEVERR_TIMEOUT);
-          s_abort = 1;
-          break;
-        }
-        const int page = lookup_page(ptrow, p_first + i, a.max_pages, p);
-        stage_page[st] = page;
-        if (page < 0) {
-          ptx::mbar_arrive(&full[st]);
-          continue;
-        }
-        ptx::mbar_arrive_expect_tx(&full[st], tx);
-        unsigned char* sb = smem + st * LY::STAGE;
-        const int row = ((layer_page0 + page) * p.Hkv + kvh) * kPage;
-        constexpr int KX = KI8 ? 128 : 64;   // box width in elements
-        constexpr int VX = VI8 ? 128 : 64;
-#pragma unroll
-        for (int bx = 0; bx < LY::KBOXES; ++bx)
-          ptx::tma_load_2d(sb + LY::K_OFF + bx * kBoxBytes, &tmk, bx * KX, row, &full[st]);
-#pragma unroll
-        for (int bx = 0; bx < LY::VBOXES; ++bx)
-          ptx::tma_load_2d(sb + LY::V_OFF + bx * kBoxBytes, &tmv, bx * VX, row, &full[st]);
-        const size_t srow = ((size_t)page * p.Hkv + kvh) * kPage * ng;
-        if (KI8) ptx::bulk_load(sb + LY::KS_OFF, p.ks + srow, kPage * ng * 2, &full[st]);
-        if (VI8) ptx::bulk_load(sb + LY::VS_OFF, p.vs + srow, kPage * ng * 2, &full[st]);
-      }
+  // Thread 0 keeps the ring full: the first NS pages now, page i + NS as soon as
+  // every warp has released page i.
+  const int32_t* ptrow = a.page_table + (size_t)b * a.max_pages;
+  auto page_row = [&](int page) { return ((layer_page0 + page) * p.Hkv + kvh) * kPage; };
+  if (threadIdx.x == 0) {
+    ptx::prefetch_tensormap(&tmk);
+    ptx::prefetch_tensormap(&tmv);
+    for (int i = 0; i < n_pg && i < LY::NS; ++i) {
+      const int page = lookup_page(ptrow, p_first + i, a.max_pages, p);
+      issue_page<D, KI8, VI8>(smem, full, stage_page, i, page, page_row(page), p, kvh, &tmk,
+                              &tmv);
     }
   }
 
@@ -204,32 +206,32 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
 #pragma unroll
   for (int i = 0; i < MTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-  if (warp < kConsumerWarps) {
+  {
     // q of head r (B operand columns = heads), in the slot order of the K loads
     uint32_t qf[KSTEPS][2];
     {
       const bool live = r < G;
-      const __half* qh = reinterpret_cast<const __half*>(a.q) + ((size_t)b * a.H + (size_t)kvh * G +
-                                                                 (live ? r : 0)) * D;
+      const uint16_t* qh = a.q + ((size_t)b * a.H + (size_t)kvh * G + (live ? r : 0)) * D;
+      if constexpr (KI8) {
 #pragma unroll
-      for (int ks = 0; ks < KSTEPS; ++ks) {
-        int d0, d1, d2, d3;
-        if (KI8) {
-          d0 = (ks >> 2) * 64 + 16 * t + 4 * (ks & 3);
-          d1 = d0 + 2;
-          d2 = d0 + 1;
-          d3 = d0 + 3;
-        } else {
-          d0 = ks * 16 + 2 * t;
-          d1 = d0 + 1;
-          d2 = d0 + 8;
-          d3 = d0 + 9;
+        for (int mc = 0; mc < MACROS; ++mc) {
+          // dims 64mc + 16t .. +16: k-step i takes (4i, 4i+2) and (4i+1, 4i+3)
+          const uint4 x = live ? ptx::ldg128(qh + mc * 64 + 16 * t) : make_uint4(0, 0, 0, 0);
+          const uint4 y = live ? ptx::ldg128(qh + mc * 64 + 16 * t + 8) : make_uint4(0, 0, 0, 0);
+          const uint32_t w[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            qf[mc * 4 + i][0] = ptx::prmt(w[2 * i], w[2 * i + 1], 0x5410);
+            qf[mc * 4 + i][1] = ptx::prmt(w[2 * i], w[2 * i + 1], 0x7632);
+          }
         }
-        const __half z = __ushort_as_half(0);
-        const __half2 x = live ? __halves2half2(qh[d0], qh[d1]) : __halves2half2(z, z);
-        const __half2 y = live ? __halves2half2(qh[d2], qh[d3]) : __halves2half2(z, z);
-        qf[ks][0] = *reinterpret_cast<const uint32_t*>(&x);
-        qf[ks][1] = *reinterpret_cast<const uint32_t*>(&y);
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qh);
+          qf[ks][0] = live ? __ldg(q32 + (ks * 16 + 2 * t) / 2) : 0u;
+          qf[ks][1] = live ? __ldg(q32 + (ks * 16 + 8 + 2 * t) / 2) : 0u;
+        }
       }
     }
     const int rowA = rho(r), rowB = rho(r) + 8;          // q.K^T rows of this thread
@@ -239,7 +241,6 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       const int st = i % LY::NS;
       if (!ptx::mbar_wait(&full[st], (i / LY::NS) & 1, kMaxPolls)) {
         flag_error(p.err, INT8KV_DEVERR_TIMEOUT);
-        s_abort = 1;
         break;
       }
       const int page = stage_page[st];
@@ -318,12 +319,12 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
         const float base0 = mn0 == -INFINITY ? 0.f : mn0;
         const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = exp2f(m0 - base0), al1 = exp2f(m1 - base1);
+        const float al0 = ptx::ex2(m0 - base0), al1 = ptx::ex2(m1 - base1);
         float pr[4];
-        pr[0] = exp2f(s[0] - base0);
-        pr[1] = exp2f(s[1] - base1);
-        pr[2] = exp2f(s[2] - base0);
-        pr[3] = exp2f(s[3] - base1);
+        pr[0] = ptx::ex2(s[0] - base0);
+        pr[1] = ptx::ex2(s[1] - base1);
+        pr[2] = ptx::ex2(s[2] - base0);
+        pr[3] = ptx::ex2(s[3] - base1);
         l0 = fmaf(l0, al0, pr[0] + pr[2]);
         l1 = fmaf(l1, al1, pr[1] + pr[3]);
         m0 = mn0;
@@ -393,6 +394,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
               const int tk[4] = {warp * 16 + tokS0, warp * 16 + tokS1, warp * 16 + 8 + tokS0,
                                  warp * 16 + 8 + tokS1};
               uint2 w[4];
+              uint32_t af[4][4];
 #pragma unroll
               for (int j = 0; j < 4; ++j)
                 w[j] = ptx::lds64(bb + tk[j] * 128 + (((c16 ^ (tk[j] & 7)) << 4) | h8));
@@ -401,14 +403,15 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                 const int kb = 2 * (mt & 1);
                 const uint32_t x0 = (mt >> 1) ? w[0].y : w[0].x, x1 = (mt >> 1) ? w[1].y : w[1].x;
                 const uint32_t x2 = (mt >> 1) ? w[2].y : w[2].x, x3 = (mt >> 1) ? w[3].y : w[3].x;
-                uint32_t af[4];
-                af[0] = v_pair(x0, x1, kb);
-                af[1] = v_pair(x0, x1, kb + 1);
-                af[2] = v_pair(x2, x3, kb);
-                af[3] = v_pair(x2, x3, kb + 1);
-                ptx::mma_f16(o[mc * 4 + mt], af, bh0, bh1);
-                ptx::mma_f16(o[mc * 4 + mt], af, bl0, bl1);
+                af[mt][0] = v_pair(x0, x1, kb);
+                af[mt][1] = v_pair(x0, x1, kb + 1);
+                af[mt][2] = v_pair(x2, x3, kb);
+                af[mt][3] = v_pair(x2, x3, kb + 1);
               }
+#pragma unroll
+              for (int mt = 0; mt < 4; ++mt) ptx::mma_f16(o[mc * 4 + mt], af[mt], bh0, bh1);
+#pragma unroll
+              for (int mt = 0; mt < 4; ++mt) ptx::mma_f16(o[mc * 4 + mt], af[mt], bl0, bl1);
             } else {
 #pragma unroll
               for (int mt = 0; mt < 4; ++mt) {
@@ -441,6 +444,16 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&empty[st]);
+      if (threadIdx.x == 0 && i + LY::NS < n_pg) {
+        if (!ptx::mbar_wait(&empty[st], (i / LY::NS) & 1, kMaxPolls)) {
+          flag_error(p.err, INT8KV_DEVERR_TIMEOUT);
+        } else {
+          const int page = lookup_page(ptrow, p_first + i + LY::NS, a.max_pages, p);
+          issue_page<D, KI8, VI8>(smem, full, stage_page, st, page, page_row(page), p, kvh,
+                                  &tmk, &tmv);
+        }
+      }
+      __syncwarp();
     }
     l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
@@ -451,59 +464,66 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   }
   __syncthreads();   // every stage consumed: the stage memory becomes the merge buffer
 
-  float* s_o = reinterpret_cast<float*>(smem);   // [warp][head 8][D]
-  if (warp < kConsumerWarps) {
-    if (r == 0) {
-      s_m[warp][2 * t] = m0;
-      s_m[warp][2 * t + 1] = m1;
-      s_l[warp][2 * t] = l0;
-      s_l[warp][2 * t + 1] = l1;
-    }
+  constexpr int DP = D + 1;                      // padded row: fewer bank conflicts
+  float* s_o = reinterpret_cast<float*>(smem);   // [warp][head 8][D + 1]
+  if (r == 0) {
+    s_m[warp][2 * t] = m0;
+    s_m[warp][2 * t + 1] = m1;
+    s_l[warp][2 * t] = l0;
+    s_l[warp][2 * t + 1] = l1;
+  }
 #pragma unroll
-    for (int j = 0; j < MTILES; ++j) {
-      const int mc = j >> 2, mt = j & 3;
-      int dx, dy;
-      float u;
-      if constexpr (VI8) {
-        dx = mc * 64 + 8 * r + 2 * mt;
-        dy = dx + 1;
-        const int g = (mc * 64) / gs;
-        u = vexp[g] == INT_MIN ? 0.f : pow2f(vexp[g] - kPShift);
-      } else {
-        dx = mc * 64 + mt * 16 + r;
-        dy = dx + 8;
-        u = pow2f(-kPShift);
-      }
-      float* h0 = s_o + ((size_t)warp * 8 + 2 * t) * D;
-      float* h1 = h0 + D;
-      h0[dx] = o[j][0] * u;
-      h1[dx] = o[j][1] * u;
-      h0[dy] = o[j][2] * u;
-      h1[dy] = o[j][3] * u;
+  for (int j = 0; j < MTILES; ++j) {
+    const int mc = j >> 2, mt = j & 3;
+    int dx, dy;
+    float u;
+    if constexpr (VI8) {
+      dx = mc * 64 + 8 * r + 2 * mt;
+      dy = dx + 1;
+      const int g = (mc * 64) / gs;
+      u = vexp[g] == INT_MIN ? 0.f : pow2f(vexp[g] - kPShift);
+    } else {
+      dx = mc * 64 + mt * 16 + r;
+      dy = dx + 8;
+      u = pow2f(-kPShift);
     }
+    float* h0 = s_o + ((size_t)warp * 8 + 2 * t) * DP;
+    float* h1 = h0 + DP;
+    h0[dx] = o[j][0] * u;
+    h1[dx] = o[j][1] * u;
+    h0[dy] = o[j][2] * u;
+    h1[dy] = o[j][3] * u;
+  }
+  __syncthreads();
+  if (threadIdx.x < 8) {   // per-head merge weights of the four warps
+    const int g = threadIdx.x;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w][g]);
+    float Ls = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float f = M == -INFINITY ? 0.f : ptx::ex2(s_m[w][g] - M);
+      s_f[w][g] = f;
+      Ls = fmaf(s_l[w][g], f, Ls);
+    }
+    s_inv[g] = Ls;
+    s_m[0][g] = M;   // warp 0's entry is no longer needed: keep the block max there
   }
   __syncthreads();
 
   for (int e = threadIdx.x; e < G * D; e += kThreads) {
     const int g = e / D, d = e - g * D;
-    float M = -INFINITY;
+    float O = 0.f;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w][g]);
-    float Ls = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float f = exp2f(s_m[w][g] - M);
-        Ls = fmaf(s_l[w][g], f, Ls);
-        O = fmaf(s_o[((size_t)w * 8 + g) * D + d], f, O);
-      }
-    }
+    for (int w = 0; w < kConsumerWarps; ++w) O = fmaf(s_o[((size_t)w * 8 + g) * DP + d], s_f[w][g], O);
+    const float Ls = s_inv[g];
     const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
     if (a.n_splits == 1) {
       a.out[h * D + d] = Ls > 0.f ? O / Ls : 0.f;
     } else {
       a.ws.part_o[(h * a.n_splits + split) * D + d] = O;
-      if (d == 0) a.ws.part_ml[h * a.n_splits + split] = make_float2(M, Ls);
+      if (d == 0) a.ws.part_ml[h * a.n_splits + split] = make_float2(s_m[0][g], Ls);
     }
   }
 }
