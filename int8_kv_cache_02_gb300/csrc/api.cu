@@ -92,19 +92,20 @@ namespace int8kv {
 
 size_t decode_workspace_layout(int B, int H, int Hkv, int D, int n_splits, DecodeWorkspace* ws,
                                void* base) {
-  (void)Hkv;
   if (n_splits <= 1) {
-    if (ws) *ws = DecodeWorkspace{nullptr, nullptr};
+    if (ws) *ws = DecodeWorkspace{nullptr, nullptr, nullptr};
     return 0;
   }
   const size_t o_bytes = round_up((size_t)B * H * n_splits * D * sizeof(float), 256);
   const size_t ml_bytes = round_up((size_t)B * H * n_splits * sizeof(float2), 256);
+  const size_t c_bytes = round_up((size_t)B * Hkv * sizeof(unsigned), 256);
   if (ws) {
     char* p = (char*)base;
     ws->part_o = (float*)p;
     ws->part_ml = (float2*)(p + o_bytes);
+    ws->counters = (unsigned*)(p + o_bytes + ml_bytes);
   }
-  return o_bytes + ml_bytes;
+  return o_bytes + ml_bytes + c_bytes;
 }
 
 }  // namespace int8kv
@@ -231,6 +232,7 @@ int attn_decode_n_splits(int batch, int n_kv_heads, int max_ctx, int page_size, 
   long long n = (target + units - 1) / units;
   if (n > pages) n = pages;
   if (n > kMaxSplits) n = kMaxSplits;
+  if (n >= 8) n -= n % 8;   // whole clusters of 8 splits for the tensor-core kernel
   if (n < 1) n = 1;
   return (int)n;
 }
@@ -312,11 +314,12 @@ cudaError_t launch_decode(const int8kv_pool* pool, int layer, const DecodeArgs& 
                           cudaStream_t stream) {
   bool k8, v8;
   variant_int8(pool->variant, &k8, &v8);
-  cudaError_t e;
+  // The tensor-core kernel combines its splits itself (cluster + last-cluster
+  // reduce); the CUDA-core kernel leaves them to the combine kernel.
   if (pool->has_tmaps && decode_mma_supported(a.pool, a.G))
-    e = launch_decode_mma(a, k8, v8, pool->tmap_k, pool->tmap_v, layer * pool->n_pages, stream);
-  else
-    e = launch_decode_simt(a, k8, v8, stream);
+    return launch_decode_mma(a, k8, v8, pool->tmap_k, pool->tmap_v, layer * pool->n_pages,
+                             stream);
+  const cudaError_t e = launch_decode_simt(a, k8, v8, stream);
   if (e != cudaSuccess || a.n_splits == 1) return e;
   return launch_decode_combine(a, stream);
 }

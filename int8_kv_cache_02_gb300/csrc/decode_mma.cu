@@ -50,6 +50,7 @@
 
 #include <climits>
 
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -57,10 +58,13 @@
 #include "decode_common.cuh"
 #include "ptx.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace int8kv {
 namespace {
 
 constexpr int kConsumerWarps = 4;
+constexpr int kMaxCluster = 8;             // splits reduced together through DSMEM
 constexpr int kThreads = kConsumerWarps * 32;
 constexpr int kPage = 64;                  // page size served by this kernel
 constexpr int kBoxBytes = kPage * 128;     // one swizzled TMA box: 64 rows x 128 B
@@ -84,7 +88,8 @@ struct Layout {
   static constexpr int STAGE = (RAW + 1023) / 1024 * 1024;
   static constexpr int NS_FIT = (70 * 1024) / STAGE;          // three blocks per SM when it fits
   static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 4 ? 4 : NS_FIT);
-  static constexpr int MERGE = kConsumerWarps * 8 * (D + 1) * 4;   // epilogue buffer (reuses stages)
+  // epilogue buffers (reuse the stages): warp partials, block partial, last-step weights
+  static constexpr int MERGE = kConsumerWarps * 8 * (D + 1) * 4 + 8 * D * 4 + kMaxSplits * 8 * 4;
   static constexpr int BARS = NS * STAGE;
   static constexpr int SMEM = 1024 + BARS + 2 * NS * 8 + NS * 4 + 64;
   static_assert(MERGE <= NS * STAGE, "merge buffer must fit in the stages");
@@ -158,6 +163,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   int* stage_page = (int*)(empty + LY::NS);
   __shared__ float s_m[kConsumerWarps][8], s_l[kConsumerWarps][8];
   __shared__ float s_f[kConsumerWarps][8], s_inv[8];
+  __shared__ float s_cm[8][8], s_cl[8][8], s_cM[8], s_cL[8];
+  __shared__ int s_last;
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -264,9 +271,10 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
           if constexpr (KI8) {
             const int box = mc >> 1, chunk = (mc & 1) * 4 + t;
-            const uint32_t bb = kbase + box * kBoxBytes;
-            const uint4 wa = ptx::lds128(bb + trA * 128 + ((chunk ^ (trA & 7)) << 4));
-            const uint4 wb = ptx::lds128(bb + trB * 128 + ((chunk ^ (trB & 7)) << 4));
+            const uint4 wa = *reinterpret_cast<const uint4*>(
+                sb + LY::K_OFF + box * kBoxBytes + trA * 128 + ((chunk ^ (trA & 7)) << 4));
+            const uint4 wb = *reinterpret_cast<const uint4*>(
+                sb + LY::K_OFF + box * kBoxBytes + trB * 128 + ((chunk ^ (trB & 7)) << 4));
             const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
             const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
@@ -389,7 +397,6 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
             if (mc < g * macros_per_group || mc >= (g + 1) * macros_per_group) continue;
             if constexpr (VI8) {
               const int box = mc >> 1;
-              const uint32_t bb = vbase + box * kBoxBytes;
               const int c16 = (mc & 1) * 4 + (r >> 1), h8 = (r & 1) << 3;
               const int tk[4] = {warp * 16 + tokS0, warp * 16 + tokS1, warp * 16 + 8 + tokS0,
                                  warp * 16 + 8 + tokS1};
@@ -397,7 +404,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
               uint32_t af[4][4];
 #pragma unroll
               for (int j = 0; j < 4; ++j)
-                w[j] = ptx::lds64(bb + tk[j] * 128 + (((c16 ^ (tk[j] & 7)) << 4) | h8));
+                w[j] = *reinterpret_cast<const uint2*>(sb + LY::V_OFF + box * kBoxBytes + tk[j] * 128 +
+                                                       (((c16 ^ (tk[j] & 7)) << 4) | h8));
 #pragma unroll
               for (int mt = 0; mt < 4; ++mt) {
                 const int kb = 2 * (mt & 1);
@@ -512,20 +520,107 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   }
   __syncthreads();
 
+  // ---- this block's partial (M, L, O~): O~ to shared memory for the cluster
+  float* cta_o = s_o + kConsumerWarps * 8 * DP;   // [8][D]
+  float* s_w = cta_o + 8 * D;                     // [n_partials][8] weights of the last step
   for (int e = threadIdx.x; e < G * D; e += kThreads) {
     const int g = e / D, d = e - g * D;
     float O = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) O = fmaf(s_o[((size_t)w * 8 + g) * DP + d], s_f[w][g], O);
-    const float Ls = s_inv[g];
+    cta_o[g * D + d] = O;
+  }
+
+  // ---- cluster reduce: block `rank` combines dims [rank*D/CS, (rank+1)*D/CS) over
+  // the CS splits of its cluster, reading their partials from distributed shared memory
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CS = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
+  cluster.sync();
+  if (threadIdx.x < CS * 8) {
+    const int j = threadIdx.x >> 3, g = threadIdx.x & 7;
+    s_cm[j][g] = *cluster.map_shared_rank(&s_m[0][g], j);
+    s_cl[j][g] = *cluster.map_shared_rank(&s_inv[g], j);
+  }
+  __syncthreads();
+  if (threadIdx.x < 8) {
+    const int g = threadIdx.x;
+    float M = -INFINITY;
+    for (int j = 0; j < CS; ++j) M = fmaxf(M, s_cm[j][g]);
+    float Ls = 0.f;
+    for (int j = 0; j < CS; ++j) {
+      const float f = (M == -INFINITY || s_cl[j][g] == 0.f) ? 0.f : ptx::ex2(s_cm[j][g] - M);
+      s_cm[j][g] = f;   // now the weight of block j
+      Ls = fmaf(s_cl[j][g], f, Ls);
+    }
+    s_cM[g] = M;
+    s_cL[g] = Ls;
+  }
+  __syncthreads();
+  const int n_part = a.n_splits / CS, cid = split / CS;
+  const int slice = D / CS, d0 = rank * slice;
+  for (int e = threadIdx.x; e < G * slice; e += kThreads) {
+    const int g = e / slice, d = d0 + (e - g * slice);
+    float O = 0.f;
+    for (int j = 0; j < CS; ++j) {
+      const float f = s_cm[j][g];
+      if (f != 0.f) O = fmaf(f, *cluster.map_shared_rank(&cta_o[g * D + d], j), O);
+    }
     const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
-    if (a.n_splits == 1) {
+    const float Ls = s_cL[g];
+    if (n_part == 1) {
       a.out[h * D + d] = Ls > 0.f ? O / Ls : 0.f;
     } else {
-      a.ws.part_o[(h * a.n_splits + split) * D + d] = O;
-      if (d == 0) a.ws.part_ml[h * a.n_splits + split] = make_float2(s_m[0][g], Ls);
+      a.ws.part_o[(h * n_part + cid) * D + d] = O;
+      if (rank == 0 && e - g * slice == 0)
+        a.ws.part_ml[h * n_part + cid] = make_float2(s_cM[g], Ls);
     }
   }
+  if (n_part == 1) {
+    cluster.sync();   // no block leaves while others read its shared memory
+    return;
+  }
+
+  // ---- the last cluster of this (sequence, kv head) to finish combines the
+  // cluster partials (atomic ticket, nobody waits for anybody)
+  __threadfence();
+  cluster.sync();
+  if (rank == 0 && threadIdx.x == 0) {
+    const unsigned t = atomicAdd(a.ws.counters + (size_t)b * p.Hkv + kvh, 1u);
+    const int last = t == (unsigned)n_part - 1;
+    for (int j = 0; j < CS; ++j) *cluster.map_shared_rank(&s_last, j) = last;
+  }
+  cluster.sync();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x < 8 && threadIdx.x < G) {
+    const int g = threadIdx.x;
+    const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
+    const float2* ml = a.ws.part_ml + h * n_part;
+    float M = -INFINITY;
+    for (int c = 0; c < n_part; ++c) M = fmaxf(M, __ldcg(ml + c).x);
+    float Ls = 0.f;
+    for (int c = 0; c < n_part; ++c) {
+      const float2 v = __ldcg(ml + c);
+      const float f = (M == -INFINITY || v.y == 0.f) ? 0.f : ptx::ex2(v.x - M);
+      s_w[c * 8 + g] = f;
+      Ls = fmaf(v.y, f, Ls);
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    for (int c = 0; c < n_part; ++c) s_w[c * 8 + g] *= inv;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < G * slice; e += kThreads) {
+    const int g = e / slice, d = d0 + (e - g * slice);
+    const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
+    const float* po = a.ws.part_o + h * n_part * D + d;
+    float O = 0.f;
+    for (int c = 0; c < n_part; ++c) {
+      const float w = s_w[c * 8 + g];
+      if (w != 0.f) O = fmaf(w, __ldcg(po + (size_t)c * D), O);
+    }
+    a.out[h * D + d] = O;
+  }
+  if (rank == 0 && threadIdx.x == 0) a.ws.counters[(size_t)b * p.Hkv + kvh] = 0u;
 }
 
 template <int D, bool KI8, bool VI8>
@@ -547,11 +642,17 @@ cudaError_t launch_typed(const DecodeArgs& a, const CUtensorMap& tmk, const CUte
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = LY::SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  int cs = kMaxCluster;   // largest power of two <= 8 dividing n_splits
+  while (a.n_splits % cs) cs >>= 1;
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cs;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, a, tmk, tmv, layer_page0);
 }
 
