@@ -186,7 +186,7 @@ class DecodeState:
         self.lens = torch.tensor([ctx], dtype=torch.int32, device="cuda")
         self.q = w["q"].cuda()
         self.out = torch.zeros((1, self.h, d), dtype=torch.float32, device="cuda")
-        self.n_splits = binding.attn_decode_n_splits(1, hkv, ctx, PS)
+        self.n_splits = binding.attn_decode_n_splits(self.pool, 1, ctx)
         self.ws = self.pool.decode_workspace(1, self.h, self.n_splits)
         self.append_token = append_token
         torch.cuda.synchronize()

@@ -133,11 +133,13 @@ int kv_quant_append(const int8kv_pool* pool, int layer, const uint16_t* k_new,
                     const uint16_t* v_new, int n_seqs, int n_new, const int32_t* seq_pos,
                     const int32_t* page_table, int max_pages_per_seq, void* stream);
 
-/* Splits the library picks for a decode of this shape on `device` when
- * attn_decode_int8 gets n_splits = 0: enough (sequence, kv head, split) blocks
- * to fill the device's SMs, each split at least one page.  Returns >= 1, or a
- * negative status. */
-int attn_decode_n_splits(int batch, int n_kv_heads, int max_ctx, int page_size, int device);
+/* Splits the library picks when attn_decode_int8 gets n_splits = 0, for a
+ * batch of `batch` sequences of at most max_ctx positions on this pool: as
+ * many (sequence, kv head, split) blocks as the decode kernel keeps resident
+ * on the pool's device at once (queried once per pool), each split at least
+ * one page, rounded down to a multiple of 8 when >= 8 (clusters of 8 splits).
+ * Returns >= 1, or a negative status (NULL_PTR, INVALID_ARG). */
+int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx);
 
 /* Workspace bytes attn_decode_int8 needs for this shape (0 when n_splits == 1).
  * Errors: INVALID_ARG. */

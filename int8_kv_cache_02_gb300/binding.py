@@ -29,7 +29,7 @@ _SIGS = {
     "kv_pool_create": (_c_int, [ctypes.POINTER(_vp)] + [_c_int] * 7 + [_vp] * 5),
     "kv_pool_destroy": (None, [_vp]),
     "kv_quant_append": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _c_int, _vp, _vp, _c_int, _vp]),
-    "attn_decode_n_splits": (_c_int, [_c_int] * 5),
+    "attn_decode_n_splits": (_c_int, [_vp, _c_int, _c_int]),
     "attn_decode_workspace_bytes": (_c_int, [_c_int] * 5 + [ctypes.POINTER(_c_size)]),
     "attn_decode_int8": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _c_int, _c_int,
                                   _c_float, _c_int, _vp, _vp, _c_size, _vp]),
@@ -129,9 +129,8 @@ def kv_quant_append(pool, layer, k_new, v_new, seq_pos, page_table, stream=None)
                                  page_table.shape[1], _stream(stream)), "kv_quant_append")
 
 
-def attn_decode_n_splits(batch, n_kv_heads, max_ctx, page_size, device=None):
-    dev = torch.cuda.current_device() if device is None else device
-    n = lib().attn_decode_n_splits(batch, n_kv_heads, max_ctx, page_size, dev)
+def attn_decode_n_splits(pool, batch, max_ctx):
+    n = lib().attn_decode_n_splits(pool.handle, batch, max_ctx)
     if n < 0:
         raise Int8KVError(n, "attn_decode_n_splits")
     return n

@@ -188,6 +188,7 @@ int kv_pool_create(int8kv_pool** out, int n_layers, int n_kv_heads, int head_dim
   p->device = dev;
   p->num_sms = sms;
   p->has_tmaps = false;
+  p->resident = 0;
   if (page_size == 64 && (head_dim == 128 || head_dim == 256)) {
     const size_t rows = (size_t)n_layers * n_pages * n_kv_heads * page_size;
     if (rows >= (1ull << 31) || !make_store_map(&p->tmap_k, k_store, k8, head_dim, rows) ||
@@ -218,18 +219,29 @@ int kv_quant_append(const int8kv_pool* pool, int layer, const uint16_t* k_new,
   return e == cudaSuccess ? INT8KV_OK : INT8KV_ERR_CUDA;
 }
 
-int attn_decode_n_splits(int batch, int n_kv_heads, int max_ctx, int page_size, int device) {
-  if (batch <= 0 || n_kv_heads <= 0 || max_ctx < 0 || !valid_page_size(page_size))
-    return INT8KV_ERR_INVALID_ARG;
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
-    return INT8KV_ERR_CUDA;
-  const long long units = (long long)batch * n_kv_heads;
-  const int pages = max_ctx > 0 ? (max_ctx + page_size - 1) / page_size : 1;
-  // Three resident blocks per SM worth of (sequence, kv head, split) blocks
-  // (the tensor-core decode kernel fits three per SM).
-  const long long target = 3LL * sms;
-  long long n = (target + units - 1) / units;
+int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx) {
+  if (!pool) return INT8KV_ERR_NULL_PTR;
+  if (batch <= 0 || max_ctx < 0) return INT8KV_ERR_INVALID_ARG;
+  if (pool->resident == 0) {
+    // Blocks the decode kernel keeps resident at once: the tensor-core kernel
+    // is launched in clusters of 8 (about three blocks per SM before cluster
+    // packing); the CUDA-core kernel is taken as three per SM.
+    int8kv_pool* mp = const_cast<int8kv_pool*>(pool);
+    int n = 0;
+    if (pool->has_tmaps && pool->group_size >= 64) {
+      int prev = -1;
+      if (cudaGetDevice(&prev) == cudaSuccess && prev != pool->device)
+        cudaSetDevice(pool->device);
+      n = decode_mma_resident_blocks(pool->head_dim, pool->k_int8, pool->v_int8,
+                                     pool->n_groups);
+      if (prev >= 0 && prev != pool->device) cudaSetDevice(prev);
+    }
+    mp->resident = n > 0 ? n : 3 * pool->num_sms;
+  }
+  const long long units = (long long)batch * pool->n_kv_heads;
+  const int ps = pool->page_size;
+  const int pages = max_ctx > 0 ? (max_ctx + ps - 1) / ps : 1;
+  long long n = (pool->resident + units - 1) / units;
   if (n > pages) n = pages;
   if (n > kMaxSplits) n = kMaxSplits;
   if (n >= 8) n -= n % 8;   // whole clusters of 8 splits for the tensor-core kernel
@@ -264,9 +276,7 @@ int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int 
   if (!q || !seq_lens || !page_table || !out) return INT8KV_ERR_NULL_PTR;
   if (!aligned16(q) || !aligned16(out)) return INT8KV_ERR_ALIGNMENT;
   if (n_splits == 0) {
-    n_splits = attn_decode_n_splits(batch, pool->n_kv_heads,
-                                    max_pages_per_seq * pool->page_size, pool->page_size,
-                                    pool->device);
+    n_splits = attn_decode_n_splits(pool, batch, max_pages_per_seq * pool->page_size);
     if (n_splits < 0) return n_splits;
   }
   DecodeArgs a;

@@ -148,7 +148,7 @@ __device__ __forceinline__ void issue_page(unsigned char* smem, uint64_t* full, 
   if (VI8) ptx::bulk_load(sb + LY::VS_OFF, p.vs + srow, kPage * ng * 2, &full[st]);
 }
 
-template <int D, bool KI8, bool VI8>
+template <int D, bool KI8, bool VI8, int NG>
 __global__ void __launch_bounds__(kThreads, 3)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, int layer_page0) {
@@ -169,7 +169,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const PoolView& p = a.pool;
-  const int G = a.G, ng = p.ng, gs = p.gs;
+  const int G = a.G;
+  constexpr int ng = NG, gs = D / NG;   // scale groups per row and their width (>= 64)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < LY::NS; ++s) {
@@ -209,7 +210,9 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   const int r = lane >> 2, t = lane & 3;
   float o[MTILES][4];
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  int vexp[4] = {INT_MIN, INT_MIN, INT_MIN, INT_MIN};   // per V group: 2^vexp > every scale seen
+  int vexp[NG];   // per V group: 2^vexp > every V scale this warp has seen
+#pragma unroll
+  for (int g = 0; g < NG; ++g) vexp[g] = INT_MIN;
 #pragma unroll
   for (int i = 0; i < MTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
@@ -348,8 +351,9 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
         }
 
         // ---- P.V, one V scale group at a time
-        const int ngv = VI8 ? ng : 1;
-        const int macros_per_group = VI8 ? gs / 64 : MACROS;
+        constexpr int ngv = VI8 ? NG : 1;
+        constexpr int macros_per_group = MACROS / ngv;
+#pragma unroll
         for (int g = 0; g < ngv; ++g) {
           float wA = 0.f, wB = 0.f;     // token weight: s_v * 2^(kPShift - e_g)
           if constexpr (VI8) {
@@ -364,7 +368,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
               const int ne = exponent_of(mx) + 1;
               if (vexp[g] != INT_MIN) {
                 const float f = pow2f(vexp[g] - ne);
-                const int j_lo = g * macros_per_group * 4, j_hi = j_lo + macros_per_group * 4;
+                constexpr int span = macros_per_group * 4;
+                const int j_lo = g * span, j_hi = j_lo + span;
 #pragma unroll
                 for (int j = 0; j < MTILES; ++j)
                   if (j >= j_lo && j < j_hi) {
@@ -560,11 +565,14 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   const int slice = D / CS, d0 = rank * slice;
   for (int e = threadIdx.x; e < G * slice; e += kThreads) {
     const int g = e / slice, d = d0 + (e - g * slice);
+    float v[kMaxCluster];
+#pragma unroll
+    for (int j = 0; j < kMaxCluster; ++j)   // all remote loads in flight at once
+      v[j] = j < CS ? *cluster.map_shared_rank(&cta_o[g * D + d], j) : 0.f;
     float O = 0.f;
-    for (int j = 0; j < CS; ++j) {
-      const float f = s_cm[j][g];
-      if (f != 0.f) O = fmaf(f, *cluster.map_shared_rank(&cta_o[g * D + d], j), O);
-    }
+#pragma unroll
+    for (int j = 0; j < kMaxCluster; ++j)
+      if (j < CS) O = fmaf(s_cm[j][g], v[j], O);
     const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
     const float Ls = s_cL[g];
     if (n_part == 1) {
@@ -592,42 +600,59 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   cluster.sync();
   if (!s_last) return;
   __threadfence();
-  if (threadIdx.x < 8 && threadIdx.x < G) {
-    const int g = threadIdx.x;
+  // one warp per head: weights of the cluster partials, every lane's loads in flight
+  for (int g = warp; g < G; g += kConsumerWarps) {
     const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
     const float2* ml = a.ws.part_ml + h * n_part;
-    float M = -INFINITY;
-    for (int c = 0; c < n_part; ++c) M = fmaxf(M, __ldcg(ml + c).x);
-    float Ls = 0.f;
-    for (int c = 0; c < n_part; ++c) {
-      const float2 v = __ldcg(ml + c);
-      const float f = (M == -INFINITY || v.y == 0.f) ? 0.f : ptx::ex2(v.x - M);
-      s_w[c * 8 + g] = f;
-      Ls = fmaf(v.y, f, Ls);
+    float2 v[kMaxSplits / 32];
+#pragma unroll
+    for (int k = 0; k < kMaxSplits / 32; ++k) {
+      const int c = lane + 32 * k;
+      v[k] = c < n_part ? __ldcg(ml + c) : make_float2(-INFINITY, 0.f);
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kMaxSplits / 32; ++k) M = fmaxf(M, v[k].x);
+    M = warp_max(M);
+    float f[kMaxSplits / 32], Ls = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxSplits / 32; ++k) {
+      f[k] = (M == -INFINITY || v[k].y == 0.f) ? 0.f : ptx::ex2(v[k].x - M);
+      Ls = fmaf(v[k].y, f[k], Ls);
+    }
+    Ls = warp_sum(Ls);
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    for (int c = 0; c < n_part; ++c) s_w[c * 8 + g] *= inv;
+#pragma unroll
+    for (int k = 0; k < kMaxSplits / 32; ++k) {
+      const int c = lane + 32 * k;
+      if (c < n_part) s_w[c * 8 + g] = f[k] * inv;
+    }
   }
   __syncthreads();
   for (int e = threadIdx.x; e < G * slice; e += kThreads) {
     const int g = e / slice, d = d0 + (e - g * slice);
     const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
     const float* po = a.ws.part_o + h * n_part * D + d;
-    float O = 0.f;
-    for (int c = 0; c < n_part; ++c) {
-      const float w = s_w[c * 8 + g];
-      if (w != 0.f) O = fmaf(w, __ldcg(po + (size_t)c * D), O);
+    float acc[8] = {};
+    int c = 0;
+    for (; c + 8 <= n_part; c += 8) {   // eight independent loads per round
+      float x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] = __ldcg(po + (size_t)(c + u) * D);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] = fmaf(s_w[(c + u) * 8 + g], x[u], acc[u]);
     }
-    a.out[h * D + d] = O;
+    for (; c < n_part; ++c) acc[0] = fmaf(s_w[c * 8 + g], __ldcg(po + (size_t)c * D), acc[0]);
+    a.out[h * D + d] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
   }
   if (rank == 0 && threadIdx.x == 0) a.ws.counters[(size_t)b * p.Hkv + kvh] = 0u;
 }
 
-template <int D, bool KI8, bool VI8>
+template <int D, bool KI8, bool VI8, int NG>
 cudaError_t launch_typed(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                          int layer_page0, cudaStream_t stream) {
   using LY = Layout<D, KI8, VI8>;
-  auto kern = decode_mma_kernel<D, KI8, VI8>;
+  auto kern = decode_mma_kernel<D, KI8, VI8, NG>;
   static bool configured[64] = {};   // per device: the attribute belongs to the device's function
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -662,16 +687,77 @@ bool decode_mma_supported(const PoolView& p, int G) {
   return G <= 8 && p.ps == kPage && (p.D == 128 || p.D == 256) && p.gs >= 64 && p.gs % 64 == 0;
 }
 
+template <int D, bool KI8, bool VI8>
+cudaError_t launch_ng(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                      int layer_page0, cudaStream_t stream) {
+  switch (a.pool.ng) {
+    case 1: return launch_typed<D, KI8, VI8, 1>(a, tmk, tmv, layer_page0, stream);
+    case 2: return launch_typed<D, KI8, VI8, 2>(a, tmk, tmv, layer_page0, stream);
+    case 4:
+      if constexpr (D == 256) return launch_typed<D, KI8, VI8, 4>(a, tmk, tmv, layer_page0, stream);
+      return cudaErrorNotSupported;
+    default: return cudaErrorNotSupported;
+  }
+}
+
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool k8, bool v8, const CUtensorMap& tmk,
                               const CUtensorMap& tmv, int layer_page0, cudaStream_t stream) {
   if (a.pool.D == 256) {
-    if (k8 && v8) return launch_typed<256, true, true>(a, tmk, tmv, layer_page0, stream);
-    if (k8) return launch_typed<256, true, false>(a, tmk, tmv, layer_page0, stream);
-    return launch_typed<256, false, true>(a, tmk, tmv, layer_page0, stream);
+    if (k8 && v8) return launch_ng<256, true, true>(a, tmk, tmv, layer_page0, stream);
+    if (k8) return launch_ng<256, true, false>(a, tmk, tmv, layer_page0, stream);
+    return launch_ng<256, false, true>(a, tmk, tmv, layer_page0, stream);
   }
-  if (k8 && v8) return launch_typed<128, true, true>(a, tmk, tmv, layer_page0, stream);
-  if (k8) return launch_typed<128, true, false>(a, tmk, tmv, layer_page0, stream);
-  return launch_typed<128, false, true>(a, tmk, tmv, layer_page0, stream);
+  if (k8 && v8) return launch_ng<128, true, true>(a, tmk, tmv, layer_page0, stream);
+  if (k8) return launch_ng<128, true, false>(a, tmk, tmv, layer_page0, stream);
+  return launch_ng<128, false, true>(a, tmk, tmv, layer_page0, stream);
+}
+
+template <int D, bool KI8, bool VI8, int NG>
+int resident_typed() {
+  using LY = Layout<D, KI8, VI8>;
+  auto kern = decode_mma_kernel<D, KI8, VI8, NG>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kMaxCluster * 64, 1, 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = LY::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kMaxCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) return 0;
+  return clusters * kMaxCluster;
+}
+
+template <int D, bool KI8, bool VI8>
+int resident_ng(int ng) {
+  if (ng == 1) return resident_typed<D, KI8, VI8, 1>();
+  if (ng == 2) return resident_typed<D, KI8, VI8, 2>();
+  if constexpr (D == 256)
+    if (ng == 4) return resident_typed<D, KI8, VI8, 4>();
+  return 0;
+}
+
+// Blocks of the tensor-core kernel for this shape that the current device keeps
+// resident at once, launched in clusters of 8; 0 if unknown.
+int decode_mma_resident_blocks(int D, bool k8, bool v8, int ng) {
+  if (D == 256) {
+    if (k8 && v8) return resident_ng<256, true, true>(ng);
+    if (k8) return resident_ng<256, true, false>(ng);
+    return resident_ng<256, false, true>(ng);
+  }
+  if (D == 128) {
+    if (k8 && v8) return resident_ng<128, true, true>(ng);
+    if (k8) return resident_ng<128, true, false>(ng);
+    return resident_ng<128, false, true>(ng);
+  }
+  return 0;
 }
 
 }  // namespace int8kv

@@ -21,6 +21,7 @@ struct int8kv_pool {
   int device;        // CUDA device the pool was created on
   int num_sms;       // its SM count (split heuristic)
   bool has_tmaps;    // TMA descriptors below are valid (shapes the tensor-core decode serves)
+  int resident;      // blocks of its decode kernel resident at once (0 = not yet queried)
   CUtensorMap tmap_k;              // K store as [rows][head_dim], 64-row x 128-byte swizzled boxes
   CUtensorMap tmap_v;              // V store, same
 };

@@ -39,8 +39,7 @@ def _decode(dev, layer, q, lens, pt, window=0, n_splits=0, scale=0.0, ws=None):
     from int8_kv_cache_02_gb300 import binding
     B, H, D = q.shape
     if n_splits == 0:
-        n_splits = binding.attn_decode_n_splits(B, dev.n_kv_heads, pt.shape[1] * dev.page_size,
-                                                dev.page_size)
+        n_splits = binding.attn_decode_n_splits(dev, B, pt.shape[1] * dev.page_size)
     if ws is None:
         ws = dev.decode_workspace(B, H, n_splits)
     out = torch.full((B, H, D), float("nan"), dtype=torch.float32, device="cuda")
