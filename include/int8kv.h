@@ -169,6 +169,31 @@ int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int 
                      int max_pages_per_seq, int window, float softmax_scale, int n_splits,
                      float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* attn_decode_int8 for callers that cannot allocate device memory where they
+ * decode (inside a graph-capture region of a framework that forbids
+ * allocation, runtimes that reserve all device memory up front, plugins that
+ * receive only the tensors their host owns).  Same arguments and result as
+ * attn_decode_int8 without the workspace: the split partials live in a fixed
+ * 4 MiB scratch array inside the library, which every GPU that loads the
+ * library holds until the process exits.  No cudaMalloc, cudaFree or other
+ * allocating call is made.
+ *   - The first call on a device, with that device current, looks up the
+ *     scratch's device address; make that first call before any stream
+ *     capture.  The pool's device must be the current device.
+ *   - Every call on a device shares the one scratch and leaves its contents
+ *     there; each call clears the part that must start at zero (the arrival
+ *     tickets) on `stream` before the kernel.  Calls that overlap on the GPU
+ *     (other streams, other host threads) race on the scratch: serialise them.
+ *   - A shape whose workspace (attn_decode_workspace_bytes) exceeds 4 MiB is
+ *     rejected with INT8KV_ERR_CAPACITY; lower n_splits or the batch.
+ * The source pages have no counterpart of this call.
+ * Errors: those of attn_decode_int8, and CAPACITY, INVALID_ARG (pool not on the
+ * current device), CUDA. */
+int attn_decode_int8_noalloc(const int8kv_pool* pool, int layer, const uint16_t* q, int batch,
+                             int n_heads, const int32_t* seq_lens, const int32_t* page_table,
+                             int max_pages_per_seq, int window, float softmax_scale,
+                             int n_splits, float* out, void* stream);
+
 /* Copy the pool's device error word into *out (host) and clear it.  Blocks
  * until `stream` has finished.  Errors: NULL_PTR (no word given), CUDA. */
 int kv_pool_read_device_error(const int8kv_pool* pool, int32_t* out, void* stream);

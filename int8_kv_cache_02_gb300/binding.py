@@ -34,6 +34,8 @@ _SIGS = {
     "attn_decode_int8": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _c_int, _c_int,
                                   _c_float, _c_int, _vp, _vp, _c_size, _vp]),
     "kv_pool_read_device_error": (_c_int, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
+    "attn_decode_int8_noalloc": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _c_int,
+                                          _c_int, _c_float, _c_int, _vp, _vp]),
 }
 
 _lib = None
@@ -156,6 +158,19 @@ def attn_decode_int8(pool, layer, q, seq_lens, page_table, out, workspace=None, 
                                   page_table.shape[1], window, float(softmax_scale), n_splits,
                                   _dev(out, torch.float32, "out"), ws, nbytes, _stream(stream)),
            "attn_decode_int8")
+
+
+def attn_decode_int8_noalloc(pool, layer, q, seq_lens, page_table, out, window=0,
+                             softmax_scale=0.0, n_splits=0, stream=None):
+    """attn_decode_int8 without a workspace: the partials use the library's own
+    fixed scratch (for callers that cannot allocate device memory)."""
+    B, H = q.shape[0], q.shape[1]
+    _check(lib().attn_decode_int8_noalloc(pool.handle, layer, _dev(q, torch.float16, "q"), B, H,
+                                          _dev(seq_lens, torch.int32, "seq_lens"),
+                                          _dev(page_table, torch.int32, "page_table"),
+                                          page_table.shape[1], window, float(softmax_scale),
+                                          n_splits, _dev(out, torch.float32, "out"),
+                                          _stream(stream)), "attn_decode_int8_noalloc")
 
 
 def kv_pool_read_device_error(pool, stream=None):

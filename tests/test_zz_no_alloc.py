@@ -1,0 +1,73 @@
+"""The allocation-free decode entry point (attn_decode_int8_noalloc).
+
+Callers that cannot allocate device memory where they decode use this entry
+point: it keeps the split partials in a fixed scratch array inside the library
+instead of a caller workspace.  These tests call it through the C ABI and check
+that two calls in a row give the output of attn_decode_int8 (which takes a
+workspace) within the attention tolerance of the other tests (2e-3 max abs,
+1e-4 max rel-L2), and that an oversized request is refused.  The file is named
+to be collected last.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from int8_kv_cache_02_gb300 import inputs
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(L=3000, seed=901):
+    q, ks, vs = inputs.random_case(seed, 2, 16, 2, 256, [L, L // 3], outliers=True)
+    lens = [L, L // 3]
+    pt, n_pages = inputs.page_table(lens, 64, seed=3)
+    dev, orc = gu.make_pools(1, 2, 256, 64, 64, n_pages, 0)
+    for b in range(2):
+        gu.fill_sequence(dev, orc, 0, ks[b], vs[b], pt[b], oracle=False)
+    return q.cuda(), torch.tensor(lens, dtype=torch.int32, device="cuda"), pt.cuda(), dev
+
+
+def _raw_noalloc(L, dev, q, lens, pt, out, n_splits):
+    return L.attn_decode_int8_noalloc(dev.handle, 0, ctypes.c_void_p(q.data_ptr()), q.shape[0],
+                                      q.shape[1], ctypes.c_void_p(lens.data_ptr()),
+                                      ctypes.c_void_p(pt.data_ptr()), pt.shape[1], 0,
+                                      ctypes.c_float(0.0), n_splits,
+                                      ctypes.c_void_p(out.data_ptr()),
+                                      ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+@pytest.mark.parametrize("n_splits", [16, 0, 1])
+def test_noalloc_matches_the_workspace_entry_point_on_two_calls(n_splits):
+    from int8_kv_cache_02_gb300 import binding
+    gu.lib_ready()
+    L = binding.lib()
+    q, lens, pt, dev = _case()
+    ns = n_splits or binding.attn_decode_n_splits(dev, 2, pt.shape[1] * 64)
+    ref = torch.empty((2, 16, 256), dtype=torch.float32, device="cuda")
+    binding.attn_decode_int8(dev, 0, q, lens, pt, ref, dev.decode_workspace(2, 16, ns), n_splits=ns)
+    torch.cuda.synchronize()
+    for call in range(2):
+        out = torch.full((2, 16, 256), float("nan"), dtype=torch.float32, device="cuda")
+        assert _raw_noalloc(L, dev, q, lens, pt, out, n_splits) == 0
+        torch.cuda.synchronize()
+        gu.assert_attention_close(out.cpu().numpy(), ref.cpu().numpy().astype(np.float64),
+                                  f"call {call}")
+    assert binding.kv_pool_read_device_error(dev) == 0
+
+
+def test_noalloc_refuses_a_workspace_beyond_its_scratch():
+    from int8_kv_cache_02_gb300 import binding
+    gu.lib_ready()
+    L = binding.lib()
+    # 64 sequences x 32 heads x 16 splits x 128 dims x 4 B = 16 MiB of partials > 4 MiB
+    dev, _ = gu.make_pools(1, 8, 128, 128, 64, 64, 0)
+    q = torch.zeros((64, 32, 128), dtype=torch.float16, device="cuda")
+    lens = torch.full((64,), 64, dtype=torch.int32, device="cuda")
+    pt = torch.zeros((64, 1), dtype=torch.int32, device="cuda")
+    out = torch.zeros((64, 32, 128), dtype=torch.float32, device="cuda")
+    assert _raw_noalloc(L, dev, q, lens, pt, out, 16) == -5          # INT8KV_ERR_CAPACITY
+    assert binding.int8kv_status_string(-5).startswith("request exceeds")
