@@ -49,8 +49,9 @@ __device__ __forceinline__ int clamp_length(int L, int max_pages, const PoolView
   return L < 0 ? 0 : L;
 }
 
-// Page-aligned split of the key range [lo, hi): split s covers
-// [p0*ps + s*per, p0*ps + (s+1)*per) ∩ [lo, hi), per = ps * ceil(pages / n_splits).
+// Page-aligned, balanced split of the key range [lo, hi): with P pages from
+// page p0 = lo / ps on, split s covers pages [p0 + s*P/S, p0 + (s+1)*P/S)
+// (integer division: page counts differ by at most one), clipped to [lo, hi).
 __device__ __forceinline__ void split_range(int lo, int hi, int s, int n_splits, int ps,
                                             int* a, int* b) {
   if (hi <= lo) {
@@ -59,9 +60,9 @@ __device__ __forceinline__ void split_range(int lo, int hi, int s, int n_splits,
   }
   const int p0 = lo / ps;
   const int pages = (hi - 1) / ps + 1 - p0;
-  const int per = ((pages + n_splits - 1) / n_splits) * ps;
-  int x = p0 * ps + s * per;
-  int y = x + per;
+  const int pa = p0 + (int)(((long long)s * pages) / n_splits);
+  const int pb = p0 + (int)(((long long)(s + 1) * pages) / n_splits);
+  int x = pa * ps, y = pb * ps;
   x = x < lo ? lo : x;
   y = y > hi ? hi : y;
   *a = x;

@@ -69,7 +69,9 @@ constexpr int kThreads = kConsumerWarps * 32;
 constexpr int kPage = 64;                  // page size served by this kernel
 constexpr int kBoxBytes = kPage * 128;     // one swizzled TMA box: 64 rows x 128 B
 constexpr uint32_t kMaxPolls = 1u << 22;   // bounded mbarrier waits (well over any copy time)
-constexpr int kPShift = 14;                // P' is fed to the MMA as P' * 2^(14 - e) < 2^14
+constexpr float kTau = 8.f;                // lazy rescale: the running max moves when exceeded by > 2^8
+constexpr int kPShift = 6;
+constexpr int kPagesCached = 256;          // page ids of a block's range kept in shared memory                 // P' fed to the MMA as P' * 2^(6 - e) < 2^8 * 2^6 = 2^14
 
 __device__ __forceinline__ int rho(int r) { return (0x37156240u >> (4 * r)) & 0xF; }
 
@@ -91,7 +93,7 @@ struct Layout {
   // epilogue buffers (reuse the stages): warp partials, block partial, last-step weights
   static constexpr int MERGE = kConsumerWarps * 8 * (D + 1) * 4 + 8 * D * 4 + kMaxSplits * 8 * 4;
   static constexpr int BARS = NS * STAGE;
-  static constexpr int SMEM = 1024 + BARS + 2 * NS * 8 + NS * 4 + 64;
+  static constexpr int SMEM = 1024 + BARS + 2 * NS * 8 + NS * 4 + 64;   // stages, barriers, page ids
   static_assert(MERGE <= NS * STAGE, "merge buffer must fit in the stages");
 };
 
@@ -148,6 +150,259 @@ __device__ __forceinline__ void issue_page(unsigned char* smem, uint64_t* full, 
   if (VI8) ptx::bulk_load(sb + LY::VS_OFF, p.vs + srow, kPage * ng * 2, &full[st]);
 }
 
+// Scales of one row (token) of the page: NG fp16 values, one vector load.
+template <int NG>
+__device__ __forceinline__ void load_row_scales(const unsigned char* base, int row, float (&x)[NG]) {
+  const unsigned char* p = base + row * NG * 2;
+  if constexpr (NG == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+  } else if constexpr (NG == 2) {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v));
+    x[0] = a.x; x[1] = a.y;
+  } else {
+    x[0] = __half2float(*reinterpret_cast<const __half*>(p));
+  }
+}
+
+// One 16-token tile of one page for one warp: scores for the G heads, online
+// softmax (lazy: the reference max moves only when a score exceeds it by more
+// than 2^kTau), and the P.V accumulation.  FULL: every token of the tile is in
+// [j0, j1), so no masking.
+template <int D, bool KI8, bool VI8, int NG, bool FULL>
+__device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, int lane, int tile0,
+                                            int j0, int j1, const uint32_t (&qf)[D / 16][2],
+                                            float scale_log2, float (&o)[D / 16][4], float& m0,
+                                            float& m1, float& l0, float& l1, float (&cap)[NG],
+                                            float (&sh)[NG], int (&vexp)[NG]) {
+  using LY = Layout<D, KI8, VI8>;
+  constexpr int MACROS = D / 64, MTILES = D / 16;
+  constexpr int NGV = VI8 ? NG : 1;
+  constexpr int MPG = MACROS / NGV;   // 64-dim macros per V scale group
+  const int r = lane >> 2, t = lane & 3;
+  const int rowA = rho(r), rowB = rowA + 8;
+  const int trA = warp * 16 + rowA, trB = warp * 16 + rowB;   // rows within the page
+  const int tokS0 = rho(2 * t), tokS1 = rho(2 * t + 1);       // P.V slot tokens
+  bool vA = true, vB = true;
+  if constexpr (!FULL) {
+    vA = tile0 + rowA >= j0 && tile0 + rowA < j1;
+    vB = tile0 + rowB >= j0 && tile0 + rowB < j1;
+  }
+
+  // ---- scores: s[0..1] token A heads (2t, 2t+1); s[2..3] token B
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  if constexpr (KI8) {
+    float ka[NG], kb[NG];
+    load_row_scales<NG>(sb + LY::KS_OFF, trA, ka);
+    load_row_scales<NG>(sb + LY::KS_OFF, trB, kb);
+    const int xa0 = trA * 128 + ((t ^ rowA) << 4), xa1 = trA * 128 + (((4 + t) ^ rowA) << 4);
+    const int xb0 = trB * 128 + ((t ^ (rowB & 7)) << 4);
+    const int xb1 = trB * 128 + (((4 + t) ^ (rowB & 7)) << 4);
+#pragma unroll
+    for (int mc = 0; mc < MACROS; ++mc) {
+      const unsigned char* kb0 = sb + LY::K_OFF + (mc >> 1) * kBoxBytes;
+      const uint4 wa = *reinterpret_cast<const uint4*>(kb0 + ((mc & 1) ? xa1 : xa0));
+      const uint4 wb = *reinterpret_cast<const uint4*>(kb0 + ((mc & 1) ? xb1 : xb0));
+      const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
+      const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) {
+        uint32_t af[4];
+        af[0] = sub1152(lop_i8pair(wA[ii]));
+        af[1] = sub1152(lop_i8pair(wB[ii]));
+        af[2] = sub1152(lop_i8pair(wA[ii] >> 8));
+        af[3] = sub1152(lop_i8pair(wB[ii] >> 8));
+        ptx::mma_f16(acc, af, qf[mc * 4 + ii][0], qf[mc * 4 + ii][1]);
+      }
+      const int grp = mc / (MACROS / NG);
+      const float sa = ka[grp] * scale_log2, sbb = kb[grp] * scale_log2;
+      s[0] = fmaf(acc[0], sa, s[0]);
+      s[1] = fmaf(acc[1], sa, s[1]);
+      s[2] = fmaf(acc[2], sbb, s[2]);
+      s[3] = fmaf(acc[3], sbb, s[3]);
+    }
+  } else {
+    const int q4 = lane >> 3, rr = lane & 7;
+    const int tok = warp * 16 + rho(rr) + 8 * (q4 & 1);
+#pragma unroll
+    for (int mc = 0; mc < MACROS; ++mc) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) {
+        const int c = ii * 2 + (q4 >> 1);   // 8-half chunk within the 64-dim box row
+        uint32_t af[4];
+        ptx::ldmatrix_x4(af, ptx::smem_u32(sb + LY::K_OFF + mc * kBoxBytes + tok * 128 +
+                                           ((c ^ (tok & 7)) << 4)));
+        ptx::mma_f16(acc, af, qf[mc * 4 + ii][0], qf[mc * 4 + ii][1]);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) s[k] += acc[k];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s[k] *= scale_log2;
+  }
+  if constexpr (!FULL) {
+    if (!vA) s[0] = s[1] = -INFINITY;
+    if (!vB) s[2] = s[3] = -INFINITY;
+  }
+
+  // ---- online softmax (base 2) per head column, lazy reference max
+  float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+  }
+  if (__any_sync(0xffffffffu, mx0 > m0 + kTau || mx1 > m1 + kTau)) {
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = mn0 == -INFINITY ? 1.f : ptx::ex2(m0 - mn0);
+    const float al1 = mn1 == -INFINITY ? 1.f : ptx::ex2(m1 - mn1);
+    l0 *= al0;
+    l1 *= al1;
+#pragma unroll
+    for (int j = 0; j < MTILES; ++j) {
+      o[j][0] *= al0;
+      o[j][1] *= al1;
+      o[j][2] *= al0;
+      o[j][3] *= al1;
+    }
+    m0 = mn0;
+    m1 = mn1;
+  }
+  const float base0 = m0 == -INFINITY ? 0.f : m0, base1 = m1 == -INFINITY ? 0.f : m1;
+  float pr[4];
+  pr[0] = ptx::ex2(s[0] - base0);
+  pr[1] = ptx::ex2(s[1] - base1);
+  pr[2] = ptx::ex2(s[2] - base0);
+  pr[3] = ptx::ex2(s[3] - base1);
+  l0 += pr[0] + pr[2];
+  l1 += pr[1] + pr[3];
+
+  // ---- token weights per V group: s_v * 2^(kPShift - e_g), the range 2^e_g raised
+  // (and the group's accumulators rescaled) when a larger V scale shows up
+  float wa[NGV], wb[NGV];
+  if constexpr (VI8) {
+    float va[NG], vb[NG];
+    load_row_scales<NG>(sb + LY::VS_OFF, trA, va);
+    load_row_scales<NG>(sb + LY::VS_OFF, trB, vb);
+    bool need = false;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      if constexpr (!FULL) {
+        va[g] = vA ? va[g] : 0.f;
+        vb[g] = vB ? vb[g] : 0.f;
+      }
+      need |= (va[g] > 0.f && va[g] >= cap[g]) || (vb[g] > 0.f && vb[g] >= cap[g]);
+    }
+    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        float mx = fmaxf(va[g], vb[g]);
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (mx > 0.f && mx >= cap[g]) {
+          const int ne = exponent_of(mx) + 1;
+          if (vexp[g] != INT_MIN) {
+            const float f = pow2f(vexp[g] - ne);
+#pragma unroll
+            for (int j = g * MPG * 4; j < (g + 1) * MPG * 4; ++j) {
+              o[j][0] *= f;
+              o[j][1] *= f;
+              o[j][2] *= f;
+              o[j][3] *= f;
+            }
+          }
+          vexp[g] = ne;
+          cap[g] = pow2f(ne);
+          sh[g] = pow2f(kPShift - ne);
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      wa[g] = va[g] * sh[g];
+      wb[g] = vb[g] * sh[g];
+    }
+  } else {
+    wa[0] = (FULL || vA) ? pow2f(kPShift) : 0.f;
+    wb[0] = (FULL || vB) ? pow2f(kPShift) : 0.f;
+  }
+
+  // ---- P.V per V group: P' as an f16 hi + lo pair, transposed into the B fragment
+#pragma unroll
+  for (int g = 0; g < NGV; ++g) {
+    const float p0 = pr[0] * wa[g], p1 = pr[1] * wa[g], p2 = pr[2] * wb[g], p3 = pr[3] * wb[g];
+    const uint32_t h01 = ptx::pack_f16x2(p0, p1), h23 = ptx::pack_f16x2(p2, p3);
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+    const uint32_t e01 = ptx::pack_f16x2(p0 - f01.x, p1 - f01.y);
+    const uint32_t e23 = ptx::pack_f16x2(p2 - f23.x, p3 - f23.y);
+    const uint32_t bh0 = ptx::movmatrix_trans(h01), bh1 = ptx::movmatrix_trans(h23);
+    const uint32_t bl0 = ptx::movmatrix_trans(e01), bl1 = ptx::movmatrix_trans(e23);
+#pragma unroll
+    for (int mm = 0; mm < MPG; ++mm) {
+      const int mc = g * MPG + mm;
+      if constexpr (VI8) {
+        const unsigned char* vb0 = sb + LY::V_OFF + (mc >> 1) * kBoxBytes;
+        const int c16 = (mc & 1) * 4 + (r >> 1), h8 = (r & 1) << 3;
+        const int tk[4] = {warp * 16 + tokS0, warp * 16 + tokS1, warp * 16 + 8 + tokS0,
+                           warp * 16 + 8 + tokS1};
+        uint2 w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          w[j] = *reinterpret_cast<const uint2*>(vb0 + tk[j] * 128 + (((c16 ^ (tk[j] & 7)) << 4) | h8));
+        uint32_t af[4][4];
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          const int kbyte = 2 * (mt & 1);
+          const uint32_t x0 = (mt >> 1) ? w[0].y : w[0].x, x1 = (mt >> 1) ? w[1].y : w[1].x;
+          const uint32_t x2 = (mt >> 1) ? w[2].y : w[2].x, x3 = (mt >> 1) ? w[3].y : w[3].x;
+          af[mt][0] = v_pair(x0, x1, kbyte);
+          af[mt][1] = v_pair(x0, x1, kbyte + 1);
+          af[mt][2] = v_pair(x2, x3, kbyte);
+          af[mt][3] = v_pair(x2, x3, kbyte + 1);
+        }
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) ptx::mma_f16(o[mc * 4 + mt], af[mt], bh0, bh1);
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) ptx::mma_f16(o[mc * 4 + mt], af[mt], bl0, bl1);
+      } else {
+        const int q4 = lane >> 3, rr = lane & 7;
+        const int tok = warp * 16 + rho(rr) + 8 * (q4 >> 1);
+        uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
+        if constexpr (!FULL) {
+          // rows outside [j0, j1) may hold any bits: zero them (P' is 0 there)
+          const bool ok0 = tile0 + tokS0 >= j0 && tile0 + tokS0 < j1;
+          const bool ok1 = tile0 + tokS1 >= j0 && tile0 + tokS1 < j1;
+          const bool ok2 = tile0 + 8 + tokS0 >= j0 && tile0 + 8 + tokS0 < j1;
+          const bool ok3 = tile0 + 8 + tokS1 >= j0 && tile0 + 8 + tokS1 < j1;
+          mlo = (ok0 ? 0x0000FFFFu : 0u) | (ok1 ? 0xFFFF0000u : 0u);
+          mhi = (ok2 ? 0x0000FFFFu : 0u) | (ok3 ? 0xFFFF0000u : 0u);
+        }
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          const int c = mt * 2 + (q4 & 1);
+          uint32_t af[4];
+          ptx::ldmatrix_x4_trans(af, ptx::smem_u32(sb + LY::V_OFF + mc * kBoxBytes + tok * 128 +
+                                                   ((c ^ (tok & 7)) << 4)));
+          if constexpr (!FULL) {
+            af[0] &= mlo;
+            af[1] &= mlo;
+            af[2] &= mhi;
+            af[3] &= mhi;
+          }
+          ptx::mma_f16(o[mc * 4 + mt], af, bh0, bh1);
+          ptx::mma_f16(o[mc * 4 + mt], af, bl0, bl1);
+        }
+      }
+    }
+  }
+}
+
 template <int D, bool KI8, bool VI8, int NG>
 __global__ void __launch_bounds__(kThreads, 3)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
@@ -157,14 +412,15 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   constexpr int MACROS = D / 64;     // 64-dim groups
   constexpr int MTILES = D / 16;     // 16-dim M-tiles of P.V
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = (uint64_t*)(smem + LY::BARS);
-  uint64_t* empty = full + LY::NS;
-  int* stage_page = (int*)(empty + LY::NS);
+  int* stage_page = (int*)(full + 2 * LY::NS);
   __shared__ float s_m[kConsumerWarps][8], s_l[kConsumerWarps][8];
   __shared__ float s_f[kConsumerWarps][8], s_inv[8];
   __shared__ float s_cm[8][8], s_cl[8][8], s_cM[8], s_cL[8];
   __shared__ int s_last;
+  __shared__ int s_rel[4];                // per stage: release tickets (the last warp refills)
+  __shared__ int s_pages[kPagesCached];   // physical page of the block's first pages
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -175,7 +431,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   if (threadIdx.x == 0) {
     for (int s = 0; s < LY::NS; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], kConsumerWarps);
+      s_rel[s] = 0;
     }
     ptx::fence_mbar_init();
   }
@@ -192,15 +448,22 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   const int p_first = j0 / kPage;
   const int n_pg = j1 > j0 ? (j1 - 1) / kPage - p_first + 1 : 0;
 
-  // Thread 0 keeps the ring full: the first NS pages now, page i + NS as soon as
-  // every warp has released page i.
+  // Page ids of the block's range go to shared memory once; thread 0 fills the
+  // ring with the first NS pages, and afterwards the last warp to release a
+  // stage refills it with page i + NS at once.
   const int32_t* ptrow = a.page_table + (size_t)b * a.max_pages;
   auto page_row = [&](int page) { return ((layer_page0 + page) * p.Hkv + kvh) * kPage; };
+  for (int i = threadIdx.x; i < n_pg && i < kPagesCached; i += kThreads)
+    s_pages[i] = lookup_page(ptrow, p_first + i, a.max_pages, p);
+  __syncthreads();
+  auto page_of = [&](int i) {
+    return i < kPagesCached ? s_pages[i] : lookup_page(ptrow, p_first + i, a.max_pages, p);
+  };
   if (threadIdx.x == 0) {
     ptx::prefetch_tensormap(&tmk);
     ptx::prefetch_tensormap(&tmv);
     for (int i = 0; i < n_pg && i < LY::NS; ++i) {
-      const int page = lookup_page(ptrow, p_first + i, a.max_pages, p);
+      const int page = page_of(i);
       issue_page<D, KI8, VI8>(smem, full, stage_page, i, page, page_row(page), p, kvh, &tmk,
                               &tmv);
     }
@@ -210,9 +473,14 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   const int r = lane >> 2, t = lane & 3;
   float o[MTILES][4];
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  int vexp[NG];   // per V group: 2^vexp > every V scale this warp has seen
+  int vexp[NG];      // per V group: 2^vexp > every V scale this warp has seen
+  float cap[NG], sh[NG];   // 2^vexp and 2^(kPShift - vexp), 0 before the first scale
 #pragma unroll
-  for (int g = 0; g < NG; ++g) vexp[g] = INT_MIN;
+  for (int g = 0; g < NG; ++g) {
+    vexp[g] = INT_MIN;
+    cap[g] = 0.f;
+    sh[g] = 0.f;
+  }
 #pragma unroll
   for (int i = 0; i < MTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
@@ -244,9 +512,6 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
         }
       }
     }
-    const int rowA = rho(r), rowB = rho(r) + 8;          // q.K^T rows of this thread
-    const int tokS0 = rho(2 * t), tokS1 = rho(2 * t + 1);  // P.V slot tokens of this thread
-
     for (int i = 0; i < n_pg; ++i) {
       const int st = i % LY::NS;
       if (!ptx::mbar_wait(&full[st], (i / LY::NS) & 1, kMaxPolls)) {
@@ -255,215 +520,27 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       }
       const int page = stage_page[st];
       const int tile0 = (p_first + i) * kPage + warp * 16;   // position of the tile's token 0
-      const bool any = page >= 0 && tile0 < j1 && tile0 + 16 > j0;
-      if (any) {
+      if (page >= 0 && tile0 < j1 && tile0 + 16 > j0) {
         const unsigned char* sb = smem + st * LY::STAGE;
-        const uint32_t kbase = ptx::smem_u32(sb + LY::K_OFF);
-        const uint32_t vbase = ptx::smem_u32(sb + LY::V_OFF);
-        const __half* ks_s = reinterpret_cast<const __half*>(sb + LY::KS_OFF);
-        const __half* vs_s = reinterpret_cast<const __half*>(sb + LY::VS_OFF);
-        const int trA = warp * 16 + rowA, trB = warp * 16 + rowB;   // rows within the page
-        const bool vA = tile0 + rowA >= j0 && tile0 + rowA < j1;
-        const bool vB = tile0 + rowB >= j0 && tile0 + rowB < j1;
-        const bool full_tile = tile0 >= j0 && tile0 + 16 <= j1;
-
-        // ---- scores: s[0..1] token A heads (2t, 2t+1); s[2..3] token B
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int mc = 0; mc < MACROS; ++mc) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          if constexpr (KI8) {
-            const int box = mc >> 1, chunk = (mc & 1) * 4 + t;
-            const uint4 wa = *reinterpret_cast<const uint4*>(
-                sb + LY::K_OFF + box * kBoxBytes + trA * 128 + ((chunk ^ (trA & 7)) << 4));
-            const uint4 wb = *reinterpret_cast<const uint4*>(
-                sb + LY::K_OFF + box * kBoxBytes + trB * 128 + ((chunk ^ (trB & 7)) << 4));
-            const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
-            const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-              uint32_t af[4];
-              af[0] = sub1152(lop_i8pair(wA[ii]));
-              af[1] = sub1152(lop_i8pair(wB[ii]));
-              af[2] = sub1152(lop_i8pair(wA[ii] >> 8));
-              af[3] = sub1152(lop_i8pair(wB[ii] >> 8));
-              ptx::mma_f16(acc, af, qf[mc * 4 + ii][0], qf[mc * 4 + ii][1]);
-            }
-            const int grp = (mc * 64) / gs;
-            const float sa = __half2float(ks_s[trA * ng + grp]) * a.scale_log2;
-            const float sbb = __half2float(ks_s[trB * ng + grp]) * a.scale_log2;
-            s[0] = fmaf(acc[0], sa, s[0]);
-            s[1] = fmaf(acc[1], sa, s[1]);
-            s[2] = fmaf(acc[2], sbb, s[2]);
-            s[3] = fmaf(acc[3], sbb, s[3]);
-          } else {
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-              const int k0 = mc * 64 + ii * 16;          // 16 dims of this k-step
-              const int q4 = lane >> 3, rr = lane & 7;
-              const int tok = warp * 16 + rho(rr) + 8 * (q4 & 1);
-              const int c = ((k0 & 63) >> 3) + (q4 >> 1);
-              uint32_t af[4];
-              ptx::ldmatrix_x4(af, kbase + (k0 >> 6) * kBoxBytes + tok * 128 + ((c ^ (tok & 7)) << 4));
-              ptx::mma_f16(acc, af, qf[mc * 4 + ii][0], qf[mc * 4 + ii][1]);
-            }
-            s[0] += acc[0];
-            s[1] += acc[1];
-            s[2] += acc[2];
-            s[3] += acc[3];
-          }
-        }
-        if constexpr (!KI8) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) s[k] *= a.scale_log2;
-        }
-        if (!vA) s[0] = s[1] = -INFINITY;
-        if (!vB) s[2] = s[3] = -INFINITY;
-
-        // ---- online softmax (base 2) per head column
-        float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = ptx::ex2(m0 - base0), al1 = ptx::ex2(m1 - base1);
-        float pr[4];
-        pr[0] = ptx::ex2(s[0] - base0);
-        pr[1] = ptx::ex2(s[1] - base1);
-        pr[2] = ptx::ex2(s[2] - base0);
-        pr[3] = ptx::ex2(s[3] - base1);
-        l0 = fmaf(l0, al0, pr[0] + pr[2]);
-        l1 = fmaf(l1, al1, pr[1] + pr[3]);
-        m0 = mn0;
-        m1 = mn1;
-        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-          for (int j = 0; j < MTILES; ++j) {
-            o[j][0] *= al0;
-            o[j][1] *= al1;
-            o[j][2] *= al0;
-            o[j][3] *= al1;
-          }
-        }
-
-        // ---- P.V, one V scale group at a time
-        constexpr int ngv = VI8 ? NG : 1;
-        constexpr int macros_per_group = MACROS / ngv;
-#pragma unroll
-        for (int g = 0; g < ngv; ++g) {
-          float wA = 0.f, wB = 0.f;     // token weight: s_v * 2^(kPShift - e_g)
-          if constexpr (VI8) {
-            const float sva = vA ? __half2float(vs_s[trA * ng + g]) : 0.f;
-            const float svb = vB ? __half2float(vs_s[trB * ng + g]) : 0.f;
-            const float cap = vexp[g] == INT_MIN ? 0.f : pow2f(vexp[g]);
-            if (__any_sync(0xffffffffu, (sva >= cap && sva > 0.f) || (svb >= cap && svb > 0.f))) {
-              float mx = fmaxf(sva, svb);
-#pragma unroll
-              for (int off = 1; off < 32; off <<= 1)
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-              const int ne = exponent_of(mx) + 1;
-              if (vexp[g] != INT_MIN) {
-                const float f = pow2f(vexp[g] - ne);
-                constexpr int span = macros_per_group * 4;
-                const int j_lo = g * span, j_hi = j_lo + span;
-#pragma unroll
-                for (int j = 0; j < MTILES; ++j)
-                  if (j >= j_lo && j < j_hi) {
-                    o[j][0] *= f;
-                    o[j][1] *= f;
-                    o[j][2] *= f;
-                    o[j][3] *= f;
-                  }
-              }
-              vexp[g] = ne;
-            }
-            const float sh = vexp[g] == INT_MIN ? 0.f : pow2f(kPShift - vexp[g]);
-            wA = sva * sh;
-            wB = svb * sh;
-          } else {
-            wA = vA ? pow2f(kPShift) : 0.f;
-            wB = vB ? pow2f(kPShift) : 0.f;
-          }
-          const float p0 = pr[0] * wA, p1 = pr[1] * wA, p2 = pr[2] * wB, p3 = pr[3] * wB;
-          const uint32_t h01 = ptx::pack_f16x2(p0, p1), h23 = ptx::pack_f16x2(p2, p3);
-          const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-          const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-          const uint32_t e01 = ptx::pack_f16x2(p0 - f01.x, p1 - f01.y);
-          const uint32_t e23 = ptx::pack_f16x2(p2 - f23.x, p3 - f23.y);
-          const uint32_t bh0 = ptx::movmatrix_trans(h01), bh1 = ptx::movmatrix_trans(h23);
-          const uint32_t bl0 = ptx::movmatrix_trans(e01), bl1 = ptx::movmatrix_trans(e23);
-
-#pragma unroll
-          for (int mc = 0; mc < MACROS; ++mc) {
-            if (mc < g * macros_per_group || mc >= (g + 1) * macros_per_group) continue;
-            if constexpr (VI8) {
-              const int box = mc >> 1;
-              const int c16 = (mc & 1) * 4 + (r >> 1), h8 = (r & 1) << 3;
-              const int tk[4] = {warp * 16 + tokS0, warp * 16 + tokS1, warp * 16 + 8 + tokS0,
-                                 warp * 16 + 8 + tokS1};
-              uint2 w[4];
-              uint32_t af[4][4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                w[j] = *reinterpret_cast<const uint2*>(sb + LY::V_OFF + box * kBoxBytes + tk[j] * 128 +
-                                                       (((c16 ^ (tk[j] & 7)) << 4) | h8));
-#pragma unroll
-              for (int mt = 0; mt < 4; ++mt) {
-                const int kb = 2 * (mt & 1);
-                const uint32_t x0 = (mt >> 1) ? w[0].y : w[0].x, x1 = (mt >> 1) ? w[1].y : w[1].x;
-                const uint32_t x2 = (mt >> 1) ? w[2].y : w[2].x, x3 = (mt >> 1) ? w[3].y : w[3].x;
-                af[mt][0] = v_pair(x0, x1, kb);
-                af[mt][1] = v_pair(x0, x1, kb + 1);
-                af[mt][2] = v_pair(x2, x3, kb);
-                af[mt][3] = v_pair(x2, x3, kb + 1);
-              }
-#pragma unroll
-              for (int mt = 0; mt < 4; ++mt) ptx::mma_f16(o[mc * 4 + mt], af[mt], bh0, bh1);
-#pragma unroll
-              for (int mt = 0; mt < 4; ++mt) ptx::mma_f16(o[mc * 4 + mt], af[mt], bl0, bl1);
-            } else {
-#pragma unroll
-              for (int mt = 0; mt < 4; ++mt) {
-                const int d0 = mc * 64 + mt * 16;
-                const int q4 = lane >> 3, rr = lane & 7;
-                const int tok = warp * 16 + rho(rr) + 8 * (q4 >> 1);
-                const int c = ((d0 & 63) >> 3) + (q4 & 1);
-                uint32_t af[4];
-                ptx::ldmatrix_x4_trans(af, vbase + (d0 >> 6) * kBoxBytes + tok * 128 +
-                                               ((c ^ (tok & 7)) << 4));
-                if (!full_tile) {
-                  // rows outside [j0, j1) may hold any bits: zero them (P' is 0 there)
-                  const bool ok0 = tile0 + tokS0 >= j0 && tile0 + tokS0 < j1;
-                  const bool ok1 = tile0 + tokS1 >= j0 && tile0 + tokS1 < j1;
-                  const bool ok2 = tile0 + 8 + tokS0 >= j0 && tile0 + 8 + tokS0 < j1;
-                  const bool ok3 = tile0 + 8 + tokS1 >= j0 && tile0 + 8 + tokS1 < j1;
-                  const uint32_t mlo = (ok0 ? 0x0000FFFFu : 0u) | (ok1 ? 0xFFFF0000u : 0u);
-                  const uint32_t mhi = (ok2 ? 0x0000FFFFu : 0u) | (ok3 ? 0xFFFF0000u : 0u);
-                  af[0] &= mlo;
-                  af[1] &= mlo;
-                  af[2] &= mhi;
-                  af[3] &= mhi;
-                }
-                ptx::mma_f16(o[mc * 4 + mt], af, bh0, bh1);
-                ptx::mma_f16(o[mc * 4 + mt], af, bl0, bl1);
-              }
-            }
-          }
-        }
+        if (tile0 >= j0 && tile0 + 16 <= j1)
+          decode_tile<D, KI8, VI8, NG, true>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
+                                             m0, m1, l0, l1, cap, sh, vexp);
+        else
+          decode_tile<D, KI8, VI8, NG, false>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
+                                              m0, m1, l0, l1, cap, sh, vexp);
       }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&empty[st]);
-      if (threadIdx.x == 0 && i + LY::NS < n_pg) {
-        if (!ptx::mbar_wait(&empty[st], (i / LY::NS) & 1, kMaxPolls)) {
-          flag_error(p.err, INT8KV_DEVERR_TIMEOUT);
-        } else {
-          const int page = lookup_page(ptrow, p_first + i + LY::NS, a.max_pages, p);
-          issue_page<D, KI8, VI8>(smem, full, stage_page, st, page, page_row(page), p, kvh,
-                                  &tmk, &tmv);
+      __syncwarp();   // every lane of this warp is done reading stage st
+      if (lane == 0) {
+        __threadfence_block();
+        // tickets only grow: the last warp of every round of four refills
+        if ((atomicAdd(&s_rel[st], 1) & (kConsumerWarps - 1)) == kConsumerWarps - 1) {
+          __threadfence_block();
+          if (i + LY::NS < n_pg) {
+            ptx::fence_proxy_async();   // generic reads of the stage before the async writes
+            const int page = page_of(i + LY::NS);
+            issue_page<D, KI8, VI8>(smem, full, stage_page, st, page, page_row(page), p, kvh,
+                                    &tmk, &tmv);
+          }
         }
       }
       __syncwarp();
