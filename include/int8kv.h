@@ -169,6 +169,35 @@ int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int 
                      int max_pages_per_seq, int window, float softmax_scale, int n_splits,
                      float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Blocks of the prefill-chunk kernel per (128-row query tile, kv head): about one
+ * block per SM in total, at least 1, at most the pages of the context.  Returns
+ * >= 1, or NULL_PTR, INVALID_ARG, UNSUPPORTED. */
+int attn_prefill_n_splits(const int8kv_pool* pool, int n_new, int n_heads, int start_pos);
+
+/* Workspace bytes attn_prefill_chunk_int8 needs (0 when n_splits == 1). */
+int attn_prefill_workspace_bytes(int n_new, int n_heads, int n_kv_heads, int head_dim,
+                                 int n_splits, size_t* out_bytes);
+
+/* Causal attention of a chunk of n_new queries over the int8 cache of one
+ * sequence (Strata #2698 "What it does": the prompt chunk dequantizes the cache
+ * on the fly; genie-ai-runtime v1.3.1: fused query-tiled kernel for chunks).
+ * Query i sits at position start_pos + i and attends keys 0 .. start_pos + i,
+ * all read from the pool: append the chunk's own K/V with kv_quant_append
+ * first.
+ *   q           device fp16 [n_new][n_heads][head_dim]
+ *   page_table  device int32 [max_pages_per_seq] of the sequence
+ *   softmax_scale 0 -> 1/sqrt(head_dim); n_splits 0 -> attn_prefill_n_splits
+ *   out         device fp32 [n_new][n_heads][head_dim]
+ *   workspace   device, >= attn_prefill_workspace_bytes (any contents)
+ * Built for page_size 64, head_dim 128/256, group_size >= 64 and
+ * n_heads / n_kv_heads in {1, 2, 4, 8}; other shapes return UNSUPPORTED.
+ * Errors: NULL_PTR, INVALID_ARG, UNSUPPORTED, CAPACITY (start_pos + n_new beyond
+ * the page-table row), WORKSPACE, ALIGNMENT, CUDA. */
+int attn_prefill_chunk_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int n_new,
+                            int n_heads, int start_pos, const int32_t* page_table,
+                            int max_pages_per_seq, float softmax_scale, int n_splits,
+                            float* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* attn_decode_int8 for callers that cannot allocate device memory where they
  * decode (inside a graph-capture region of a framework that forbids
  * allocation, runtimes that reserve all device memory up front, plugins that

@@ -34,6 +34,10 @@ _SIGS = {
     "attn_decode_int8": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _c_int, _c_int,
                                   _c_float, _c_int, _vp, _vp, _c_size, _vp]),
     "kv_pool_read_device_error": (_c_int, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
+    "attn_prefill_n_splits": (_c_int, [_vp, _c_int, _c_int, _c_int]),
+    "attn_prefill_workspace_bytes": (_c_int, [_c_int] * 5 + [ctypes.POINTER(_c_size)]),
+    "attn_prefill_chunk_int8": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _c_int, _vp, _c_int,
+                                         _c_float, _c_int, _vp, _vp, _c_size, _vp]),
     "attn_decode_int8_noalloc": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _c_int,
                                           _c_int, _c_float, _c_int, _vp, _vp]),
 }
@@ -171,6 +175,33 @@ def attn_decode_int8_noalloc(pool, layer, q, seq_lens, page_table, out, window=0
                                           page_table.shape[1], window, float(softmax_scale),
                                           n_splits, _dev(out, torch.float32, "out"),
                                           _stream(stream)), "attn_decode_int8_noalloc")
+
+
+def attn_prefill_n_splits(pool, n_new, n_heads, start_pos):
+    n = lib().attn_prefill_n_splits(pool.handle, n_new, n_heads, start_pos)
+    if n < 0:
+        raise Int8KVError(n, "attn_prefill_n_splits")
+    return n
+
+
+def attn_prefill_workspace_bytes(n_new, n_heads, n_kv_heads, head_dim, n_splits):
+    out = _c_size(0)
+    _check(lib().attn_prefill_workspace_bytes(n_new, n_heads, n_kv_heads, head_dim, n_splits,
+                                              ctypes.byref(out)), "attn_prefill_workspace_bytes")
+    return out.value
+
+
+def attn_prefill_chunk_int8(pool, layer, q, start_pos, page_table, out, workspace=None,
+                            softmax_scale=0.0, n_splits=0, stream=None):
+    """q fp16 [n_new][H][D]; page_table int32 [max_pages] (one sequence); out fp32 [n_new][H][D]."""
+    n_new, H = q.shape[0], q.shape[1]
+    ws = _dev(workspace, torch.uint8, "workspace") if workspace is not None else None
+    nbytes = workspace.numel() if workspace is not None else 0
+    _check(lib().attn_prefill_chunk_int8(pool.handle, layer, _dev(q, torch.float16, "q"), n_new,
+                                         H, start_pos, _dev(page_table, torch.int32, "page_table"),
+                                         page_table.shape[-1], float(softmax_scale), n_splits,
+                                         _dev(out, torch.float32, "out"), ws, nbytes,
+                                         _stream(stream)), "attn_prefill_chunk_int8")
 
 
 def kv_pool_read_device_error(pool, stream=None):

@@ -304,6 +304,73 @@ int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int 
   return e == cudaSuccess ? INT8KV_OK : INT8KV_ERR_CUDA;
 }
 
+int attn_prefill_n_splits(const int8kv_pool* pool, int n_new, int n_heads, int start_pos) {
+  if (!pool) return INT8KV_ERR_NULL_PTR;
+  if (n_new <= 0 || n_heads <= 0 || start_pos < 0 || n_heads % pool->n_kv_heads != 0)
+    return INT8KV_ERR_INVALID_ARG;
+  const int G = n_heads / pool->n_kv_heads;
+  if (G > 8) return INT8KV_ERR_UNSUPPORTED;
+  // one block per SM: (query tiles of 128 rows) x kv heads x splits ~ SM count
+  const long long tiles = (n_new + 128 / G - 1) / (128 / G);
+  const long long units = tiles * pool->n_kv_heads;
+  long long n = pool->num_sms / units;
+  const int pages = (start_pos + n_new + pool->page_size - 1) / pool->page_size;
+  if (n > pages) n = pages;
+  if (n > kMaxSplits) n = kMaxSplits;
+  if (n < 1) n = 1;
+  return (int)n;
+}
+
+int attn_prefill_workspace_bytes(int n_new, int n_heads, int n_kv_heads, int head_dim,
+                                 int n_splits, size_t* out_bytes) {
+  return attn_decode_workspace_bytes(n_new, n_heads, n_kv_heads, head_dim, n_splits, out_bytes);
+}
+
+int attn_prefill_chunk_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int n_new,
+                            int n_heads, int start_pos, const int32_t* page_table,
+                            int max_pages_per_seq, float softmax_scale, int n_splits, float* out,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  if (!pool) return INT8KV_ERR_NULL_PTR;
+  if (layer < 0 || layer >= pool->n_layers || n_new < 0 || n_heads <= 0 || start_pos < 0 ||
+      max_pages_per_seq <= 0 || n_splits < 0 || n_splits > kMaxSplits ||
+      !std::isfinite(softmax_scale) || n_heads % pool->n_kv_heads != 0)
+    return INT8KV_ERR_INVALID_ARG;
+  const int G = n_heads / pool->n_kv_heads;
+  if (!prefill_supported(pool, G)) return INT8KV_ERR_UNSUPPORTED;
+  if (n_new == 0) return INT8KV_OK;
+  if ((long long)start_pos + n_new > (long long)max_pages_per_seq * pool->page_size)
+    return INT8KV_ERR_CAPACITY;
+  if (!q || !page_table || !out) return INT8KV_ERR_NULL_PTR;
+  if (!aligned16(q) || !aligned16(out)) return INT8KV_ERR_ALIGNMENT;
+  if (n_splits == 0) {
+    n_splits = attn_prefill_n_splits(pool, n_new, n_heads, start_pos);
+    if (n_splits < 0) return n_splits;
+  }
+  PrefillArgs a;
+  const size_t need = decode_workspace_layout(n_new, n_heads, pool->n_kv_heads, pool->head_dim,
+                                              n_splits, &a.ws, workspace);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return INT8KV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return INT8KV_ERR_ALIGNMENT;
+  }
+  a.pool = layer_view(pool, layer);
+  a.q = q;
+  a.page_table = page_table;
+  a.out = out;
+  a.n_new = n_new;
+  a.H = n_heads;
+  a.G = G;
+  a.start = start_pos;
+  a.max_pages = max_pages_per_seq;
+  a.n_splits = n_splits;
+  const float scale =
+      softmax_scale != 0.f ? softmax_scale : 1.0f / std::sqrt((float)pool->head_dim);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const cudaError_t e = launch_prefill(pool, layer, a, (cudaStream_t)stream);
+  if (e == cudaErrorNotSupported) return INT8KV_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? INT8KV_OK : INT8KV_ERR_CUDA;
+}
+
 int kv_pool_read_device_error(const int8kv_pool* pool, int32_t* out, void* stream) {
   if (!pool || !out || !pool->dev_error) return INT8KV_ERR_NULL_PTR;
   cudaStream_t s = (cudaStream_t)stream;

@@ -56,6 +56,7 @@
 
 #include "common.cuh"
 #include "decode_common.cuh"
+#include "mma_common.cuh"
 #include "ptx.cuh"
 
 namespace cg = cooperative_groups;
@@ -66,46 +67,30 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kMaxCluster = 8;             // splits reduced together through DSMEM
 constexpr int kThreads = kConsumerWarps * 32;
-constexpr int kPage = 64;                  // page size served by this kernel
-constexpr int kBoxBytes = kPage * 128;     // one swizzled TMA box: 64 rows x 128 B
-constexpr uint32_t kMaxPolls = 1u << 22;   // bounded mbarrier waits (well over any copy time)
 constexpr float kTau = 8.f;                // lazy rescale: the running max moves when exceeded by > 2^8
-constexpr int kPShift = 6;
-constexpr int kPagesCached = 256;          // page ids of a block's range kept in shared memory                 // P' fed to the MMA as P' * 2^(6 - e) < 2^8 * 2^6 = 2^14
+constexpr int kPShift = 6;                 // P' fed to the MMA as P' * 2^(6 - e) < 2^8 * 2^6 = 2^14
+constexpr int kPagesCached = 256;          // page ids of a block's range kept in shared memory
+using mma::kPage;
+using mma::kBoxBytes;
+using mma::kMaxPolls;
+using mma::lop_i8pair;
+using mma::sub1152;
+using mma::pow2f;
+using mma::exponent_of;
 
 __device__ __forceinline__ int rho(int r) { return (0x37156240u >> (4 * r)) & 0xF; }
 
 template <int D, bool KI8, bool VI8>
-struct Layout {
-  static constexpr int KBYTES = KI8 ? D * kPage : 2 * D * kPage;
-  static constexpr int VBYTES = VI8 ? D * kPage : 2 * D * kPage;
-  static constexpr int KBOXES = KBYTES / kBoxBytes;
-  static constexpr int VBOXES = VBYTES / kBoxBytes;
-  static constexpr int SCALE_BYTES = kPage * 4 * 2;   // up to 4 groups per row
-  static constexpr int K_OFF = 0;
-  static constexpr int V_OFF = KBYTES;
-  static constexpr int KS_OFF = KBYTES + VBYTES;
-  static constexpr int VS_OFF = KS_OFF + (KI8 ? SCALE_BYTES : 0);
-  static constexpr int RAW = VS_OFF + (VI8 ? SCALE_BYTES : 0);
-  static constexpr int STAGE = (RAW + 1023) / 1024 * 1024;
-  static constexpr int NS_FIT = (70 * 1024) / STAGE;          // three blocks per SM when it fits
+struct Layout : mma::StagedPage<D, KI8, VI8> {
+  using SP = mma::StagedPage<D, KI8, VI8>;
+  static constexpr int NS_FIT = (70 * 1024) / SP::STAGE;          // three blocks per SM when it fits
   static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 4 ? 4 : NS_FIT);
   // epilogue buffers (reuse the stages): warp partials, block partial, last-step weights
   static constexpr int MERGE = kConsumerWarps * 8 * (D + 1) * 4 + 8 * D * 4 + kMaxSplits * 8 * 4;
-  static constexpr int BARS = NS * STAGE;
+  static constexpr int BARS = NS * SP::STAGE;
   static constexpr int SMEM = 1024 + BARS + 2 * NS * 8 + NS * 4 + 64;   // stages, barriers, page ids
-  static_assert(MERGE <= NS * STAGE, "merge buffer must fit in the stages");
+  static_assert(MERGE <= NS * SP::STAGE, "merge buffer must fit in the stages");
 };
-
-__device__ __forceinline__ uint32_t lop_i8pair(uint32_t x) {
-  // bytes 0 and 2 of x (int8 codes) -> fp16 pair (1152 + c): 0x6400 | (c ^ 0x80)
-  return (x & 0x00FF00FFu) ^ 0x64806480u;
-}
-
-__device__ __forceinline__ uint32_t sub1152(uint32_t h2) {
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h2), __half2half2(__ushort_as_half(0x6480)));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
 
 // Codes at byte k of W0 and W1 -> exact f16x2 (lo = W0's, hi = W1's).
 __device__ __forceinline__ uint32_t v_pair(uint32_t w0, uint32_t w1, int k) {
@@ -114,43 +99,14 @@ __device__ __forceinline__ uint32_t v_pair(uint32_t w0, uint32_t w1, int k) {
   return sub1152(lop_i8pair(ptx::prmt(w0, w1, sel)));
 }
 
-__device__ __forceinline__ float pow2f(int e) {   // 2^e for e in [-126, 127]
-  return __uint_as_float((uint32_t)(127 + e) << 23);
-}
-
-__device__ __forceinline__ int exponent_of(float x) {   // floor(log2 x), x > 0 normal
-  return (int)((__float_as_uint(x) >> 23) & 0xFF) - 127;
-}
-
 template <int D, bool KI8, bool VI8>
 __device__ __forceinline__ void issue_page(unsigned char* smem, uint64_t* full, int* stage_page,
                                            int st, int page, int row, const PoolView& p, int kvh,
                                            const CUtensorMap* tmk, const CUtensorMap* tmv) {
-  using LY = Layout<D, KI8, VI8>;
-  stage_page[st] = page;
-  if (page < 0) {
-    ptx::mbar_arrive(&full[st]);
-    return;
-  }
-  const int ng = p.ng;
-  const uint32_t tx = LY::KBYTES + LY::VBYTES + (KI8 ? kPage * ng * 2 : 0) +
-                      (VI8 ? kPage * ng * 2 : 0);
-  ptx::mbar_arrive_expect_tx(&full[st], tx);
-  unsigned char* sb = smem + st * LY::STAGE;
-  constexpr int KX = KI8 ? 128 : 64;   // box width in elements
-  constexpr int VX = VI8 ? 128 : 64;
-#pragma unroll
-  for (int bx = 0; bx < LY::KBOXES; ++bx)
-    ptx::tma_load_2d(sb + LY::K_OFF + bx * kBoxBytes, tmk, bx * KX, row, &full[st]);
-#pragma unroll
-  for (int bx = 0; bx < LY::VBOXES; ++bx)
-    ptx::tma_load_2d(sb + LY::V_OFF + bx * kBoxBytes, tmv, bx * VX, row, &full[st]);
-  const size_t srow = ((size_t)page * p.Hkv + kvh) * kPage * ng;
-  if (KI8) ptx::bulk_load(sb + LY::KS_OFF, p.ks + srow, kPage * ng * 2, &full[st]);
-  if (VI8) ptx::bulk_load(sb + LY::VS_OFF, p.vs + srow, kPage * ng * 2, &full[st]);
+  mma::issue_page<D, KI8, VI8>(smem + st * Layout<D, KI8, VI8>::STAGE, &full[st], &stage_page[st],
+                               page, row, p, kvh, tmk, tmv);
 }
 
-// Scales of one row (token) of the page: NG fp16 values, one vector load.
 template <int NG>
 __device__ __forceinline__ void load_row_scales(const unsigned char* base, int row, float (&x)[NG]) {
   const unsigned char* p = base + row * NG * 2;

@@ -79,6 +79,16 @@ struct DecodeArgs {
   float scale_log2;         // softmax_scale * log2(e)
 };
 
+struct PrefillArgs {
+  PoolView pool;
+  const uint16_t* q;          // [n_new][H][D] fp16
+  const int32_t* page_table;  // [max_pages] of the sequence
+  float* out;                 // [n_new][H][D]
+  DecodeWorkspace ws;         // partials [n_new][H][n_splits][D] when n_splits > 1
+  int n_new, H, G, start, max_pages, n_splits;
+  float scale_log2;           // softmax_scale * log2(e)
+};
+
 cudaError_t launch_quant_append(const PoolView& pool, const uint16_t* k_new, const uint16_t* v_new,
                                 int n_seqs, int n_new, const int32_t* seq_pos,
                                 const int32_t* page_table, int max_pages, bool k_int8,
@@ -88,5 +98,11 @@ cudaError_t launch_quant_append(const PoolView& pool, const uint16_t* k_new, con
 // n_splits > 1, the combine.  cudaErrorNotSupported when no kernel fits.
 cudaError_t launch_decode(const int8kv_pool* pool, int layer, const DecodeArgs& a,
                           cudaStream_t stream);
+
+// Prefill-chunk kernel (and, with n_splits > 1, the combine).  cudaErrorNotSupported
+// when no kernel fits the shape.
+cudaError_t launch_prefill(const int8kv_pool* pool, int layer, const PrefillArgs& a,
+                           cudaStream_t stream);
+bool prefill_supported(const int8kv_pool* pool, int G);
 
 }  // namespace int8kv

@@ -1,0 +1,91 @@
+// Pieces shared by the tensor-core decode and prefill kernels: the staged page
+// layout in shared memory, the TMA issue of one page, exact int8 -> fp16
+// conversion, and power-of-two helpers.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace int8kv {
+namespace mma {
+
+constexpr int kPage = 64;                  // page size served by the tensor-core kernels
+constexpr int kBoxBytes = kPage * 128;     // one swizzled TMA box: 64 rows x 128 B
+constexpr uint32_t kMaxPolls = 1u << 22;   // bounded mbarrier waits (well over any copy time)
+
+// One staged page of one kv head: K rows, V rows (int8: 128-dim boxes; fp16:
+// 64-dim boxes; each box 64 rows x 128 B, 128-byte swizzle), then the K and V
+// scales rows ([64][ng] fp16) of an int8 store.
+template <int D, bool KI8, bool VI8>
+struct StagedPage {
+  static constexpr int KBYTES = KI8 ? D * kPage : 2 * D * kPage;
+  static constexpr int VBYTES = VI8 ? D * kPage : 2 * D * kPage;
+  static constexpr int KBOXES = KBYTES / kBoxBytes;
+  static constexpr int VBOXES = VBYTES / kBoxBytes;
+  static constexpr int SCALE_BYTES = kPage * 4 * 2;   // up to 4 groups per row
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = KBYTES;
+  static constexpr int KS_OFF = KBYTES + VBYTES;
+  static constexpr int VS_OFF = KS_OFF + (KI8 ? SCALE_BYTES : 0);
+  static constexpr int RAW = VS_OFF + (VI8 ? SCALE_BYTES : 0);
+  static constexpr int STAGE = (RAW + 1023) / 1024 * 1024;
+};
+
+// Bytes 0 and 2 of x (int8 codes c) -> fp16 pair holding 1152 + c: the fp16 with
+// bit pattern 0x6400 | u is 1024 + u for u in [0, 255] (the magic-number method
+// of Kim et al., "Who Says Elephants Can't Run", 2022), u = c ^ 0x80 = c + 128.
+__device__ __forceinline__ uint32_t lop_i8pair(uint32_t x) {
+  return (x & 0x00FF00FFu) ^ 0x64806480u;
+}
+
+// (1152 + c) - 1152 = c, exact in fp16.
+__device__ __forceinline__ uint32_t sub1152(uint32_t h2) {
+  const __half2 r =
+      __hsub2(*reinterpret_cast<const __half2*>(&h2), __half2half2(__ushort_as_half(0x6480)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ float pow2f(int e) {   // 2^e for e in [-126, 127]
+  return __uint_as_float((uint32_t)(127 + e) << 23);
+}
+
+__device__ __forceinline__ int exponent_of(float x) {   // floor(log2 x), x > 0 normal
+  return (int)((__float_as_uint(x) >> 23) & 0xFF) - 127;
+}
+
+// Issue the copies of one page (or, for a page id flagged invalid, complete the
+// stage's barrier with no bytes) into stage `st`.
+template <int D, bool KI8, bool VI8>
+__device__ __forceinline__ void issue_page(unsigned char* stage, uint64_t* full_bar, int* stage_page,
+                                           int page, int row, const PoolView& p, int kvh,
+                                           const CUtensorMap* tmk, const CUtensorMap* tmv) {
+  using SP = StagedPage<D, KI8, VI8>;
+  *stage_page = page;
+  if (page < 0) {
+    ptx::mbar_arrive(full_bar);
+    return;
+  }
+  const int ng = p.ng;
+  const uint32_t tx = SP::KBYTES + SP::VBYTES + (KI8 ? kPage * ng * 2 : 0) +
+                      (VI8 ? kPage * ng * 2 : 0);
+  ptx::mbar_arrive_expect_tx(full_bar, tx);
+  constexpr int KX = KI8 ? 128 : 64;   // box width in elements
+  constexpr int VX = VI8 ? 128 : 64;
+#pragma unroll
+  for (int bx = 0; bx < SP::KBOXES; ++bx)
+    ptx::tma_load_2d(stage + SP::K_OFF + bx * kBoxBytes, tmk, bx * KX, row, full_bar);
+#pragma unroll
+  for (int bx = 0; bx < SP::VBOXES; ++bx)
+    ptx::tma_load_2d(stage + SP::V_OFF + bx * kBoxBytes, tmv, bx * VX, row, full_bar);
+  const size_t srow = ((size_t)page * p.Hkv + kvh) * kPage * ng;
+  if (KI8) ptx::bulk_load(stage + SP::KS_OFF, p.ks + srow, kPage * ng * 2, full_bar);
+  if (VI8) ptx::bulk_load(stage + SP::VS_OFF, p.vs + srow, kPage * ng * 2, full_bar);
+}
+
+}  // namespace mma
+}  // namespace int8kv
