@@ -478,6 +478,56 @@ def run_prefill(n_iter=20):
                     "cache (34 MB) is L2-resident; bound by the tensor pipe"}
 
 
+def run_batched(n_iter=20):
+    """Batched decode over a paged pool: 64 sequences, lengths uniform in [1024, 32768],
+    32 query / 8 kv heads, head_dim 128, one scale per (position, kv head); layer 0
+    full context, layer 1 a 512-position window.  Decode kernel alone per layer."""
+    import torch
+
+    from int8_kv_cache_02_gb300 import binding, inputs
+    lens, qs = inputs.batched_lengths_and_q()
+    lens = [int(x) for x in lens]
+    pt, n_pages = inputs.page_table(lens, PS, seed=11)
+    pool = binding.KVPool(2, 8, 128, 128, PS, n_pages, binding.K8V8)
+    ptd = pt.cuda()
+    zero = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for layer in (0, 1):
+        for b, L in enumerate(lens):
+            k, v = inputs.batched_kv(layer, b, L)
+            binding.kv_quant_append(pool, layer, k.reshape(1, L, 8, 128).cuda(),
+                                    v.reshape(1, L, 8, 128).cuda(), zero, ptd[b:b + 1])
+    lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = torch.empty((64, 32, 128), dtype=torch.float32, device="cuda")
+    res = {"total_ctx": sum(lens)}
+    per_pos = 8 * 128 * 2 + 8 * 2 * 2        # int8 K, V rows + fp16 scales, all kv heads
+    qo = 64 * 32 * 128 * (2 + 4)
+    for layer, window in ((0, 0), (1, 512)):
+        ns = binding.attn_decode_n_splits(pool, 64, window + PS if window else pt.shape[1] * PS)
+        ws = pool.decode_workspace(64, 32, ns)
+        q = qs[layer].cuda()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                binding.attn_decode_int8(pool, layer, q, lens_d, ptd, out, ws, window=window,
+                                         n_splits=ns)
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(n_iter):
+                binding.attn_decode_int8(pool, layer, q, lens_d, ptd, out, ws, window=window,
+                                         n_splits=ns)
+        time_graph(g)
+        us = min(time_graph(g) for _ in range(3)) / n_iter * 1e3
+        vis = sum(min(L, window) if window else L for L in lens)
+        byt = vis * per_pos + qo
+        res["layer%d_window%d" % (layer, window)] = {
+            "us_per_step": us, "n_splits": ns, "GBps": byt / (us * 1e-6) / 1e9, "algorithmic_bytes": byt,
+            "l2": "HBM-resident (pool 4.5 GB)" if not window else "window of 512 per sequence "
+                  "(68 MB: partly L2-resident)"}
+    return res
+
+
 def run_extra(args):
     """128K-context decode (k8v8 and k8v16), decode kernel alone, L2 defeated by copies;
     and the prefill chunk."""
@@ -540,6 +590,8 @@ def main():
     ap.add_argument("--copies", type=int, default=0, help="pool copies (0: enough to defeat L2)")
     ap.add_argument("--no-extra", action="store_true", help="skip the 128K measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--batched", action="store_true",
+                    help="with --extra-only: also the 64-sequence paged batch (slow setup)")
     ap.add_argument("--extra-only", action="store_true",
                     help="run only the 128K measurements and print them (profiling aid)")
     args = ap.parse_args()
@@ -562,7 +614,10 @@ def main():
             from int8_kv_cache_02_gb300 import build
             build.build()
             torch.cuda.set_device(local)
-            print(json.dumps(run_extra(args)), flush=True)
+            res = run_extra(args)
+            if args.batched:
+                res["batched"] = run_batched()
+            print(json.dumps(res), flush=True)
         elif args.impl == "reference":
             run_reference(args, rank, world, local)
         else:

@@ -136,8 +136,9 @@ int kv_quant_append(const int8kv_pool* pool, int layer, const uint16_t* k_new,
 /* Splits the library picks when attn_decode_int8 gets n_splits = 0, for a
  * batch of `batch` sequences of at most max_ctx positions on this pool: as
  * many (sequence, kv head, split) blocks as the decode kernel keeps resident
- * on the pool's device at once (queried once per pool), each split at least
- * one page, rounded down to a multiple of 8 when >= 8 (clusters of 8 splits).
+ * on the pool's device at once (queried once per pool), and at least enough
+ * that a split of a max_ctx sequence holds no more than 64 pages; each split at
+ * least one page; rounded down to a multiple of 8 when >= 8 (clusters of 8 splits).
  * Returns >= 1, or a negative status (NULL_PTR, INVALID_ARG). */
 int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx);
 
@@ -154,7 +155,8 @@ int attn_decode_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head
  *   page_table   device int32 [batch][max_pages_per_seq]
  *   window       0 = full context; W > 0 = only the last W positions L-W..L-1
  *   softmax_scale 0 -> 1/sqrt(head_dim)
- *   n_splits     0 -> attn_decode_n_splits(); 1 -> single pass, no workspace;
+ *   n_splits     0 -> attn_decode_n_splits() for the longest context the page
+ *                table holds (or the window plus one page); 1 -> single pass;
  *                otherwise the key range [lo, L) is cut page-aligned into
  *                n_splits pieces of ceil(pages/n_splits) pages
  *   out          device fp32 [batch][n_heads][head_dim]

@@ -242,6 +242,10 @@ int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx) {
   const int ps = pool->page_size;
   const int pages = max_ctx > 0 ? (max_ctx + ps - 1) / ps : 1;
   long long n = (pool->resident + units - 1) / units;
+  // with more units than resident blocks, still cut long sequences so that no
+  // block holds more than 64 pages: ragged batches then balance over the waves
+  const long long by_length = (pages + 63) / 64;
+  if (n < by_length) n = by_length;
   if (n > pages) n = pages;
   if (n > kMaxSplits) n = kMaxSplits;
   if (n >= 8) n -= n % 8;   // whole clusters of 8 splits for the tensor-core kernel
@@ -276,7 +280,9 @@ int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int 
   if (!q || !seq_lens || !page_table || !out) return INT8KV_ERR_NULL_PTR;
   if (!aligned16(q) || !aligned16(out)) return INT8KV_ERR_ALIGNMENT;
   if (n_splits == 0) {
-    n_splits = attn_decode_n_splits(pool, batch, max_pages_per_seq * pool->page_size);
+    int ctx = max_pages_per_seq * pool->page_size;
+    if (window > 0 && window + pool->page_size < ctx) ctx = window + pool->page_size;
+    n_splits = attn_decode_n_splits(pool, batch, ctx);
     if (n_splits < 0) return n_splits;
   }
   DecodeArgs a;

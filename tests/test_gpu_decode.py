@@ -278,3 +278,53 @@ def test_mma_path_ignores_garbage_beyond_the_context(variant):
     assert np.isfinite(out).all()
     gu.assert_attention_close(out, _oracle(orc, 0, q, [L], pt), "garbage")
     assert binding.kv_pool_read_device_error(dev) == 0
+
+
+@pytest.mark.slow
+def test_batched_workload_full_size_sampled():
+    """64 sequences of 1024..32768 positions (8 kv heads, head_dim 128, one scale per
+    (position, kv head), pages of 64), two layers: layer 0 full context, layer 1 a
+    512-position window.  The whole pool is built through the kernel; a sample of
+    sequences is checked against the oracle (codes, scales and attention)."""
+    from int8_kv_cache_02_gb300 import binding
+    from oracle import quant
+    lens, qs = inputs.batched_lengths_and_q()
+    lens = [int(x) for x in lens]
+    pt, n_pages = inputs.page_table(lens, 64, seed=11)
+    dev = binding.KVPool(2, 8, 128, 128, 64, n_pages, binding.K8V8)
+    ptd = pt.cuda()
+    zero = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sample = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 7, 40})
+    kv = {}
+    for layer in (0, 1):
+        for b, L in enumerate(lens):
+            k, v = inputs.batched_kv(layer, b, L)
+            binding.kv_quant_append(dev, layer, k.reshape(1, L, 8, 128).cuda(),
+                                    v.reshape(1, L, 8, 128).cuda(), zero, ptd[b:b + 1])
+            if b in sample:
+                kv[(layer, b)] = (k, v)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    ns = binding.attn_decode_n_splits(dev, 64, pt.shape[1] * 64)
+    ws = dev.decode_workspace(64, 32, ns)
+    for layer, window in ((0, 0), (1, 512)):
+        out = torch.empty((64, 32, 128), dtype=torch.float32, device="cuda")
+        binding.attn_decode_int8(dev, layer, qs[layer].cuda(), lens_d, ptd, out, ws,
+                                 window=window, n_splits=ns)
+        torch.cuda.synchronize()
+        out = out.cpu().numpy()
+        assert np.isfinite(out).all()
+        kstore = dev.k_store[layer].cpu().numpy()
+        kscale = dev.k_scales[layer].cpu().numpy()
+        for b in sample:
+            k, v = kv[(layer, b)]
+            L = lens[b]
+            kc, ks = quant.quantize(k.numpy(), 128)
+            vc, vs = quant.quantize(v.numpy(), 128)
+            pos = np.arange(L)
+            pages = pt[b].numpy()[pos // 64]
+            assert np.array_equal(kstore[pages, :, pos % 64, :], kc)
+            assert np.array_equal(kscale[pages, :, pos % 64, :].view(np.uint16), ks.view(np.uint16))
+            ref = oatt.decode(qs[layer][b].numpy(), quant.dequantize(kc, ks, 128),
+                              quant.dequantize(vc, vs, 128), L, window=window)
+            gu.assert_attention_close(out[b], ref, f"layer {layer} seq {b} L {L}")
+    assert binding.kv_pool_read_device_error(dev) == 0
