@@ -139,11 +139,13 @@ def dist_env():
 
 
 def max_over_ranks(x, world):
+    """Max of a host float over all ranks (NCCL on the GPUs, gloo on the CPU)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
