@@ -40,7 +40,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("INT8-KV decode attn: achieved HBM GB/s (% of ~8 TB/s), μs/step at "
           "8K–128K ctx")
-WORKLOAD = ("decode step (append 1 token + split-K GQA decode + combine): batch 1, 16 q heads, "
+WORKLOAD = ("decode step (append 1 token + split-K GQA decode + combine, one fused kernel): "
+            "batch 1, 16 q heads, "
             "2 kv heads, head_dim 256, fp16 scale per 64 values, ctx 8192, k8v8, outlier K "
             "channels")
 
@@ -194,8 +195,13 @@ class DecodeState:
         torch.cuda.synchronize()
 
     def step(self, c, append=True, decode=True):
+        """append only, decode only, or both (one fused kernel: attn_decode_append_int8)."""
         b = self.binding
         pt = self.pt[c:c + 1]
+        if append and decode and self.append_token:
+            b.attn_decode_append_int8(self.pool, 0, self.q, self.k_new[0], self.v_new[0],
+                                      self.lens, pt, self.out, self.ws, n_splits=self.n_splits)
+            return
         if append and self.append_token:
             b.kv_quant_append(self.pool, 0, self.k_new, self.v_new, self.pos, pt)
         if decode:
@@ -362,8 +368,8 @@ def run_ours(args, rank, world, local):
     def e2e_step(c):
         din.copy_(hin, non_blocking=True)
         pt = st.pt[c:c + 1]
-        binding.kv_quant_append(st.pool, 0, dk, dv, st.pos, pt)
-        binding.attn_decode_int8(st.pool, 0, dq, st.lens, pt, st.out, st.ws, n_splits=st.n_splits)
+        binding.attn_decode_append_int8(st.pool, 0, dq, dk[0], dv[0], st.lens, pt, st.out, st.ws,
+                                        n_splits=st.n_splits)
         hout.copy_(st.out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -415,12 +421,13 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": round(step_bytes() * n_e2e * world / e2e_s / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": e2e_s / n_e2e * 1e6, "steps": n_e2e},
-        "roofline": {"bound": "hbm", "kernel": "attn_decode_int8 (split-K partial + combine)",
+        "roofline": {"bound": "hbm", "kernel": "decode_mma_kernel (attn_decode_int8: split-K "
+                                               "partials + in-kernel combine)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": traffic, "algorithmic_bytes": decode_bytes(),
                      "us_per_launch": dec_s * 1e6, "kernel_src_sha": src_sha},
-        "gpu_launches": 2 * K,
+        "gpu_launches": K,
         "clocks": clocks,
         "cpu_baseline": cpu,
         "extra": extra,

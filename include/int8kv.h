@@ -171,6 +171,22 @@ int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int 
                      int max_pages_per_seq, int window, float softmax_scale, int n_splits,
                      float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* One decode step with its append fused: the new token's K and V rows
+ *   k_new, v_new  device fp16 [batch][n_kv_heads][head_dim]
+ * are quantized (as kv_quant_append does) into position seq_lens[b] - 1 of each
+ * sequence, then attn_decode_int8 runs over positions 0 .. seq_lens[b] - 1.  On
+ * the tensor-core path the block whose key range holds the new position writes
+ * it before streaming its pages, so the whole step is one kernel; otherwise the
+ * append kernel runs first on the same stream.  Same arguments, workspace and
+ * errors as attn_decode_int8 (a length beyond the page-table row skips the
+ * append and is flagged).  Bit-identical to kv_quant_append followed by
+ * attn_decode_int8. */
+int attn_decode_append_int8(const int8kv_pool* pool, int layer, const uint16_t* q,
+                            const uint16_t* k_new, const uint16_t* v_new, int batch, int n_heads,
+                            const int32_t* seq_lens, const int32_t* page_table,
+                            int max_pages_per_seq, int window, float softmax_scale, int n_splits,
+                            float* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Blocks of the prefill-chunk kernel per (128-row query tile, kv head): about one
  * block per SM in total, at least 1, at most the pages of the context.  Returns
  * >= 1, or NULL_PTR, INVALID_ARG, UNSUPPORTED. */

@@ -34,6 +34,9 @@ _SIGS = {
     "attn_decode_int8": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _c_int, _c_int,
                                   _c_float, _c_int, _vp, _vp, _c_size, _vp]),
     "kv_pool_read_device_error": (_c_int, [_vp, ctypes.POINTER(ctypes.c_int32), _vp]),
+    "attn_decode_append_int8": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp,
+                                         _c_int, _c_int, _c_float, _c_int, _vp, _vp, _c_size,
+                                         _vp]),
     "attn_prefill_n_splits": (_c_int, [_vp, _c_int, _c_int, _c_int]),
     "attn_prefill_workspace_bytes": (_c_int, [_c_int] * 5 + [ctypes.POINTER(_c_size)]),
     "attn_prefill_chunk_int8": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _c_int, _vp, _c_int,
@@ -175,6 +178,22 @@ def attn_decode_int8_noalloc(pool, layer, q, seq_lens, page_table, out, window=0
                                           page_table.shape[1], window, float(softmax_scale),
                                           n_splits, _dev(out, torch.float32, "out"),
                                           _stream(stream)), "attn_decode_int8_noalloc")
+
+
+def attn_decode_append_int8(pool, layer, q, k_new, v_new, seq_lens, page_table, out,
+                            workspace=None, window=0, softmax_scale=0.0, n_splits=0, stream=None):
+    """Append k_new, v_new (fp16 [B][Hkv][D]) at position seq_lens[b] - 1, then decode."""
+    B, H = q.shape[0], q.shape[1]
+    ws = _dev(workspace, torch.uint8, "workspace") if workspace is not None else None
+    nbytes = workspace.numel() if workspace is not None else 0
+    _check(lib().attn_decode_append_int8(pool.handle, layer, _dev(q, torch.float16, "q"),
+                                         _dev(k_new, torch.float16, "k_new"),
+                                         _dev(v_new, torch.float16, "v_new"), B, H,
+                                         _dev(seq_lens, torch.int32, "seq_lens"),
+                                         _dev(page_table, torch.int32, "page_table"),
+                                         page_table.shape[1], window, float(softmax_scale),
+                                         n_splits, _dev(out, torch.float32, "out"), ws, nbytes,
+                                         _stream(stream)), "attn_decode_append_int8")
 
 
 def attn_prefill_n_splits(pool, n_new, n_heads, start_pos):

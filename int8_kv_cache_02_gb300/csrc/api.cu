@@ -264,10 +264,38 @@ int attn_decode_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head
   return INT8KV_OK;
 }
 
+static int decode_entry(const int8kv_pool* pool, int layer, const uint16_t* q,
+                        const uint16_t* k_new, const uint16_t* v_new, int batch, int n_heads,
+                        const int32_t* seq_lens, const int32_t* page_table,
+                        int max_pages_per_seq, int window, float softmax_scale, int n_splits,
+                        float* out, void* workspace, size_t workspace_bytes, void* stream);
+
 int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int batch,
                      int n_heads, const int32_t* seq_lens, const int32_t* page_table,
                      int max_pages_per_seq, int window, float softmax_scale, int n_splits,
                      float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_entry(pool, layer, q, nullptr, nullptr, batch, n_heads, seq_lens, page_table,
+                      max_pages_per_seq, window, softmax_scale, n_splits, out, workspace,
+                      workspace_bytes, stream);
+}
+
+int attn_decode_append_int8(const int8kv_pool* pool, int layer, const uint16_t* q,
+                            const uint16_t* k_new, const uint16_t* v_new, int batch, int n_heads,
+                            const int32_t* seq_lens, const int32_t* page_table,
+                            int max_pages_per_seq, int window, float softmax_scale, int n_splits,
+                            float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch > 0 && (!k_new || !v_new)) return INT8KV_ERR_NULL_PTR;
+  if (!aligned16(k_new) || !aligned16(v_new)) return INT8KV_ERR_ALIGNMENT;
+  return decode_entry(pool, layer, q, k_new, v_new, batch, n_heads, seq_lens, page_table,
+                      max_pages_per_seq, window, softmax_scale, n_splits, out, workspace,
+                      workspace_bytes, stream);
+}
+
+static int decode_entry(const int8kv_pool* pool, int layer, const uint16_t* q,
+                        const uint16_t* k_new, const uint16_t* v_new, int batch, int n_heads,
+                        const int32_t* seq_lens, const int32_t* page_table,
+                        int max_pages_per_seq, int window, float softmax_scale, int n_splits,
+                        float* out, void* workspace, size_t workspace_bytes, void* stream) {
   if (!pool) return INT8KV_ERR_NULL_PTR;
   if (layer < 0 || layer >= pool->n_layers || batch < 0 || n_heads <= 0 ||
       max_pages_per_seq <= 0 || window < 0 || n_splits < 0 || n_splits > kMaxSplits ||
@@ -294,6 +322,8 @@ int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int 
   }
   a.pool = layer_view(pool, layer);
   a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
   a.seq_lens = seq_lens;
   a.page_table = page_table;
   a.out = out;
@@ -393,10 +423,18 @@ int kv_pool_read_device_error(const int8kv_pool* pool, int32_t* out, void* strea
 
 namespace int8kv {
 
-cudaError_t launch_decode(const int8kv_pool* pool, int layer, const DecodeArgs& a,
+cudaError_t launch_decode(const int8kv_pool* pool, int layer, const DecodeArgs& a_in,
                           cudaStream_t stream) {
   bool k8, v8;
   variant_int8(pool->variant, &k8, &v8);
+  DecodeArgs a = a_in;
+  if (a.k_new && !(pool->has_tmaps && decode_mma_supported(a.pool, a.G))) {
+    // the CUDA-core kernel has no fused append: append first, at seq_lens[b] - 1
+    const cudaError_t e0 = launch_quant_append(a.pool, a.k_new, a.v_new, a.B, 1, a.seq_lens,
+                                               a.page_table, a.max_pages, k8, v8, stream, -1);
+    if (e0 != cudaSuccess) return e0;
+    a.k_new = a.v_new = nullptr;
+  }
   // The tensor-core kernel combines its splits itself (cluster + last-cluster
   // reduce); the CUDA-core kernel leaves them to the combine kernel.
   if (pool->has_tmaps && decode_mma_supported(a.pool, a.G))

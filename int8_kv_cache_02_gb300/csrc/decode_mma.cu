@@ -57,6 +57,7 @@
 #include "common.cuh"
 #include "decode_common.cuh"
 #include "mma_common.cuh"
+#include "quant_row.cuh"
 #include "ptx.cuh"
 
 namespace cg = cooperative_groups;
@@ -397,7 +398,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   ptx::grid_dependency_wait();
   ptx::grid_launch_dependents();
 
-  const int L = clamp_length(__ldg(a.seq_lens + b), a.max_pages, p);
+  const int L_raw = __ldg(a.seq_lens + b);
+  const int L = clamp_length(L_raw, a.max_pages, p);
   const int lo_pos = a.window > 0 ? max(0, L - a.window) : 0;
   int j0, j1;
   split_range(lo_pos, L, split, a.n_splits, kPage, &j0, &j1);
@@ -411,6 +413,24 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   auto page_row = [&](int page) { return ((layer_page0 + page) * p.Hkv + kvh) * kPage; };
   for (int i = threadIdx.x; i < n_pg && i < kPagesCached; i += kThreads)
     s_pages[i] = lookup_page(ptrow, p_first + i, a.max_pages, p);
+  // Fused append: the block whose range holds the new token (position L-1)
+  // quantizes its K and V rows into the pool before any copy of that page is
+  // issued; no other block reads the page.
+  if (a.k_new != nullptr && L == L_raw && L > 0 && L - 1 >= j0 && L - 1 < j1 && warp < 2) {
+    const int pos = L - 1;
+    const int page = lookup_page(ptrow, pos / kPage, a.max_pages, p);
+    if (page >= 0) {
+      constexpr int VPL = D / 32;
+      const size_t row = row_index(p, page, kvh, pos % kPage);
+      const uint16_t* src = (warp == 0 ? a.k_new : a.v_new) + ((size_t)b * p.Hkv + kvh) * D;
+      if (warp == 0 ? KI8 : VI8)
+        quantize_row<VPL>(src, (int8_t*)(warp == 0 ? p.k : p.v) + row * D,
+                          (uint16_t*)(warp == 0 ? p.ks : p.vs) + row * NG, lane, (D / NG) / VPL);
+      else
+        copy_row<VPL>(src, (uint16_t*)(warp == 0 ? p.k : p.v) + row * D, lane);
+      ptx::fence_proxy_async_global();   // visible to the tensor copies that follow
+    }
+  }
   __syncthreads();
   auto page_of = [&](int i) {
     return i < kPagesCached ? s_pages[i] : lookup_page(ptrow, p_first + i, a.max_pages, p);

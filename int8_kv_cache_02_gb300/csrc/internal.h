@@ -74,6 +74,8 @@ struct DecodeArgs {
   const int32_t* seq_lens;  // [B]
   const int32_t* page_table;// [B][max_pages]
   float* out;               // [B][H][D]
+  const uint16_t* k_new;    // [B][Hkv][D] fp16 token appended at seq_lens[b]-1, or null
+  const uint16_t* v_new;
   DecodeWorkspace ws;
   int B, H, G, max_pages, window, n_splits;
   float scale_log2;         // softmax_scale * log2(e)
@@ -89,10 +91,11 @@ struct PrefillArgs {
   float scale_log2;           // softmax_scale * log2(e)
 };
 
+// Token i of sequence b goes to position seq_pos[b] + pos_offset + i.
 cudaError_t launch_quant_append(const PoolView& pool, const uint16_t* k_new, const uint16_t* v_new,
                                 int n_seqs, int n_new, const int32_t* seq_pos,
                                 const int32_t* page_table, int max_pages, bool k_int8,
-                                bool v_int8, cudaStream_t stream);
+                                bool v_int8, cudaStream_t stream, int pos_offset = 0);
 
 // Partial kernel (tensor-core when the shape allows, else CUDA-core) and, with
 // n_splits > 1, the combine.  cudaErrorNotSupported when no kernel fits.

@@ -17,69 +17,17 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "quant_row.cuh"
 
 namespace int8kv {
 namespace {
 
 template <int VPL>
-struct Vec;
-template <>
-struct Vec<2> { using H = uint32_t; using B = uint16_t; };
-template <>
-struct Vec<4> { using H = uint2; using B = uint32_t; };
-template <>
-struct Vec<8> { using H = uint4; using B = uint2; };
-
-template <int VPL>
-__device__ __forceinline__ void load_halves(const uint16_t* src, float (&x)[VPL]) {
-  typename Vec<VPL>::H raw = *reinterpret_cast<const typename Vec<VPL>::H*>(src);
-  const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-  for (int i = 0; i < VPL / 2; ++i) {
-    const float2 f = __half22float2(h2[i]);
-    x[2 * i] = f.x;
-    x[2 * i + 1] = f.y;
-  }
-}
-
-template <int VPL>
-__device__ __forceinline__ void quantize_row(const uint16_t* src, int8_t* dst_codes,
-                                             uint16_t* dst_scales, int lane, int lanes_per_group) {
-  float x[VPL];
-  load_halves<VPL>(src + lane * VPL, x);
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  for (int off = 1; off < lanes_per_group; off <<= 1)
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
-  const float s = __half2float(s16);
-  union { typename Vec<VPL>::B v; int8_t c[VPL]; } out;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    int c = 0;
-    if (s != 0.f) {
-      c = __float2int_rn(__fdiv_rn(x[i], s));  // round half to even
-      c = max(-127, min(127, c));
-    }
-    out.c[i] = (int8_t)c;
-  }
-  *reinterpret_cast<typename Vec<VPL>::B*>(dst_codes + lane * VPL) = out.v;
-  if ((lane % lanes_per_group) == 0) dst_scales[(lane * VPL) / (lanes_per_group * VPL)] =
-      __half_as_ushort(s16);
-}
-
-template <int VPL>
-__device__ __forceinline__ void copy_row(const uint16_t* src, uint16_t* dst, int lane) {
-  *reinterpret_cast<typename Vec<VPL>::H*>(dst + lane * VPL) =
-      *reinterpret_cast<const typename Vec<VPL>::H*>(src + lane * VPL);
-}
-
-template <int VPL>
 __global__ void __launch_bounds__(256) quant_append_kernel(
     PoolView p, const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
     int n_seqs, int n_new, const int32_t* __restrict__ seq_pos,
-    const int32_t* __restrict__ page_table, int max_pages, bool k_int8, bool v_int8) {
+    const int32_t* __restrict__ page_table, int max_pages, bool k_int8, bool v_int8,
+    int pos_offset) {
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const long long n_rows = (long long)n_seqs * n_new * p.Hkv;
@@ -88,7 +36,7 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
   const long long bi = row / p.Hkv;      // b * n_new + i
   const int i = (int)(bi % n_new);
   const int b = (int)(bi / n_new);
-  const int pos = __ldg(seq_pos + b) + i;
+  const int pos = __ldg(seq_pos + b) + pos_offset + i;
   if (pos < 0) {
     if (lane == 0) flag_error(p.err, INT8KV_DEVERR_LENGTH);
     return;
@@ -115,7 +63,7 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
 cudaError_t launch_quant_append(const PoolView& pool, const uint16_t* k_new, const uint16_t* v_new,
                                 int n_seqs, int n_new, const int32_t* seq_pos,
                                 const int32_t* page_table, int max_pages, bool k_int8,
-                                bool v_int8, cudaStream_t stream) {
+                                bool v_int8, cudaStream_t stream, int pos_offset) {
   const long long rows = (long long)n_seqs * n_new * pool.Hkv;
   if (rows == 0) return cudaSuccess;
   const int warps = 8;
@@ -124,17 +72,17 @@ cudaError_t launch_quant_append(const PoolView& pool, const uint16_t* k_new, con
     case 64:
       quant_append_kernel<2><<<grid, warps * 32, 0, stream>>>(pool, k_new, v_new, n_seqs, n_new,
                                                               seq_pos, page_table, max_pages,
-                                                              k_int8, v_int8);
+                                                              k_int8, v_int8, pos_offset);
       break;
     case 128:
       quant_append_kernel<4><<<grid, warps * 32, 0, stream>>>(pool, k_new, v_new, n_seqs, n_new,
                                                               seq_pos, page_table, max_pages,
-                                                              k_int8, v_int8);
+                                                              k_int8, v_int8, pos_offset);
       break;
     case 256:
       quant_append_kernel<8><<<grid, warps * 32, 0, stream>>>(pool, k_new, v_new, n_seqs, n_new,
                                                               seq_pos, page_table, max_pages,
-                                                              k_int8, v_int8);
+                                                              k_int8, v_int8, pos_offset);
       break;
     default:
       return cudaErrorNotSupported;

@@ -328,3 +328,49 @@ def test_batched_workload_full_size_sampled():
                               quant.dequantize(vc, vs, 128), L, window=window)
             gu.assert_attention_close(out[b], ref, f"layer {layer} seq {b} L {L}")
     assert binding.kv_pool_read_device_error(dev) == 0
+
+
+@pytest.mark.parametrize("D,gs,ps,variant", [(256, 64, 64, 0), (128, 128, 64, 1), (256, 128, 64, 2),
+                                             (64, 32, 16, 0)])
+@pytest.mark.parametrize("window", [0, 100])
+def test_decode_append_equals_append_then_decode(D, gs, ps, variant, window):
+    """attn_decode_append_int8 (append fused into the decode kernel where the tensor-core
+    path serves the shape) is bit-identical to kv_quant_append + attn_decode_int8."""
+    from int8_kv_cache_02_gb300 import binding
+    lens = [777, 64, 1, 300]
+    B, H, Hkv = len(lens), 8, 2
+    q, ks, vs = inputs.random_case(611 + D + variant, B, H, Hkv, D, lens, outliers=True)
+    pt, n_pages = inputs.page_table(lens, ps, seed=21)
+    outs, pools = [], []
+    for fused in (False, True):
+        dev, orc = gu.make_pools(1, Hkv, D, gs, ps, n_pages, variant)
+        for b, L in enumerate(lens):
+            if L > 1:
+                gu.fill_sequence(dev, orc, 0, ks[b][:L - 1], vs[b][:L - 1], pt[b], oracle=False)
+        kn = torch.stack([ks[b][L - 1] for b, L in enumerate(lens)]).cuda()   # [B][Hkv][D]
+        vn = torch.stack([vs[b][L - 1] for b, L in enumerate(lens)]).cuda()
+        lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        ns = 4
+        ws = dev.decode_workspace(B, H, ns)
+        out = torch.full((B, H, D), float("nan"), dtype=torch.float32, device="cuda")
+        if fused:
+            binding.attn_decode_append_int8(dev, 0, q.cuda(), kn, vn, lens_d, pt.cuda(), out, ws,
+                                            window=window, n_splits=ns)
+        else:
+            binding.kv_quant_append(dev, 0, kn[:, None].contiguous(), vn[:, None].contiguous(),
+                                    lens_d - 1, pt.cuda())
+            binding.attn_decode_int8(dev, 0, q.cuda(), lens_d, pt.cuda(), out, ws, window=window,
+                                     n_splits=ns)
+        torch.cuda.synchronize()
+        assert binding.kv_pool_read_device_error(dev) == 0
+        outs.append(out.cpu().numpy())
+        pools.append(dev)
+    assert np.array_equal(outs[0], outs[1])
+    for name in ("k_store", "v_store", "k_scales", "v_scales"):
+        a, b = getattr(pools[0], name), getattr(pools[1], name)
+        assert (a is None and b is None) or torch.equal(a, b), name
+    # and against the oracle
+    orc = gu.opool.Pool(1, Hkv, D, gs, ps, n_pages, variant)
+    for b, L in enumerate(lens):
+        orc.append_contiguous(0, ks[b].numpy(), vs[b].numpy(), 0, pt[b].numpy())
+    gu.assert_attention_close(outs[1], _oracle(orc, 0, q, lens, pt, window=window), "fused")
