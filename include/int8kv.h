@@ -138,7 +138,7 @@ int kv_quant_append(const int8kv_pool* pool, int layer, const uint16_t* k_new,
  * many (sequence, kv head, split) blocks as the decode kernel keeps resident
  * on the pool's device at once (queried once per pool), and at least enough
  * that a split of a max_ctx sequence holds no more than 64 pages; each split at
- * least one page; rounded down to a multiple of 8 when >= 8 (clusters of 8 splits).
+ * least one page.
  * Returns >= 1, or a negative status (NULL_PTR, INVALID_ARG). */
 int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx);
 
@@ -160,10 +160,12 @@ int attn_decode_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head
  *                otherwise the key range [lo, L) is cut page-aligned into
  *                n_splits pieces of ceil(pages/n_splits) pages
  *   out          device fp32 [batch][n_heads][head_dim]
- *   workspace    device, >= attn_decode_workspace_bytes, 16-byte aligned, and
- *                ZERO-FILLED before its first use; every completed call leaves
- *                it ready for the next one.  Calls sharing one workspace must
- *                not overlap on the device.
+ *   workspace    device, >= attn_decode_workspace_bytes, 16-byte aligned, any
+ *                contents (every partial a call reads, it writes first).  Calls
+ *                sharing one workspace must not overlap on the device.
+ * Up to 8 splits are combined inside the decode kernel (the splits of a
+ * (sequence, kv head) form one thread-block cluster and reduce through
+ * distributed shared memory); with more, a combine kernel follows on the stream.
  * n_heads must be a multiple of n_kv_heads with n_heads / n_kv_heads <= 8.
  * Errors: NULL_PTR, INVALID_ARG, UNSUPPORTED, WORKSPACE, CAPACITY, CUDA. */
 int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int batch,
@@ -228,8 +230,7 @@ int attn_prefill_chunk_int8(const int8kv_pool* pool, int layer, const uint16_t* 
  *     scratch's device address; make that first call before any stream
  *     capture.  The pool's device must be the current device.
  *   - Every call on a device shares the one scratch and leaves its contents
- *     there; each call clears the part that must start at zero (the arrival
- *     tickets) on `stream` before the kernel.  Calls that overlap on the GPU
+ *     there; nothing in it has to start at zero.  Calls that overlap on the GPU
  *     (other streams, other host threads) race on the scratch: serialise them.
  *   - A shape whose workspace (attn_decode_workspace_bytes) exceeds 4 MiB is
  *     rejected with INT8KV_ERR_CAPACITY; lower n_splits or the batch.

@@ -92,20 +92,19 @@ namespace int8kv {
 
 size_t decode_workspace_layout(int B, int H, int Hkv, int D, int n_splits, DecodeWorkspace* ws,
                                void* base) {
+  (void)Hkv;
   if (n_splits <= 1) {
-    if (ws) *ws = DecodeWorkspace{nullptr, nullptr, nullptr};
+    if (ws) *ws = DecodeWorkspace{nullptr, nullptr};
     return 0;
   }
   const size_t o_bytes = round_up((size_t)B * H * n_splits * D * sizeof(float), 256);
   const size_t ml_bytes = round_up((size_t)B * H * n_splits * sizeof(float2), 256);
-  const size_t c_bytes = round_up((size_t)B * Hkv * sizeof(unsigned), 256);
   if (ws) {
     char* p = (char*)base;
     ws->part_o = (float*)p;
     ws->part_ml = (float2*)(p + o_bytes);
-    ws->counters = (unsigned*)(p + o_bytes + ml_bytes);
   }
-  return o_bytes + ml_bytes + c_bytes;
+  return o_bytes + ml_bytes;
 }
 
 }  // namespace int8kv
@@ -223,9 +222,8 @@ int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx) {
   if (!pool) return INT8KV_ERR_NULL_PTR;
   if (batch <= 0 || max_ctx < 0) return INT8KV_ERR_INVALID_ARG;
   if (pool->resident == 0) {
-    // Blocks the decode kernel keeps resident at once: the tensor-core kernel
-    // is launched in clusters of 8 (about three blocks per SM before cluster
-    // packing); the CUDA-core kernel is taken as three per SM.
+    // Blocks the decode kernel keeps resident at once (three per SM for the
+    // tensor-core kernel's shapes); the CUDA-core kernel is taken as three per SM.
     int8kv_pool* mp = const_cast<int8kv_pool*>(pool);
     int n = 0;
     if (pool->has_tmaps && pool->group_size >= 64) {
@@ -248,7 +246,6 @@ int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx) {
   if (n < by_length) n = by_length;
   if (n > pages) n = pages;
   if (n > kMaxSplits) n = kMaxSplits;
-  if (n >= 8) n -= n % 8;   // whole clusters of 8 splits for the tensor-core kernel
   if (n < 1) n = 1;
   return (int)n;
 }
@@ -435,11 +432,15 @@ cudaError_t launch_decode(const int8kv_pool* pool, int layer, const DecodeArgs& 
     if (e0 != cudaSuccess) return e0;
     a.k_new = a.v_new = nullptr;
   }
-  // The tensor-core kernel combines its splits itself (cluster + last-cluster
-  // reduce); the CUDA-core kernel leaves them to the combine kernel.
-  if (pool->has_tmaps && decode_mma_supported(a.pool, a.G))
-    return launch_decode_mma(a, k8, v8, pool->tmap_k, pool->tmap_v, layer * pool->n_pages,
-                             stream);
+  // The tensor-core kernel combines up to 8 splits itself (one cluster); more
+  // splits, and the CUDA-core kernel's, go through the combine kernel.
+  if (pool->has_tmaps && decode_mma_supported(a.pool, a.G)) {
+    const cudaError_t e = launch_decode_mma(a, k8, v8, pool->tmap_k, pool->tmap_v,
+                                            layer * pool->n_pages, stream);
+    // up to 8 splits are combined inside the kernel (one cluster)
+    if (e != cudaSuccess || a.n_splits <= 8) return e;
+    return launch_decode_combine(a, stream);
+  }
   const cudaError_t e = launch_decode_simt(a, k8, v8, stream);
   if (e != cudaSuccess || a.n_splits == 1) return e;
   return launch_decode_combine(a, stream);

@@ -8,8 +8,10 @@
 // no key at all gets O = 0.
 //
 // Grid (head_dim / 64, n_heads, batch); eight warps share the splits of one
-// (head, 64-dim slice), each lane two adjacent dims, four independent loads in
-// flight per lane; the eight warp sums meet in shared memory.  Launched as a programmatic dependent of
+// (head, 64-dim slice), each lane two adjacent dims.  Every lane issues all its
+// partial loads before the split weights are known (warp 0 computes those from
+// the (m, l) pairs meanwhile), so the two round trips to L2 overlap; the eight
+// warp sums meet in shared memory.  Launched as a programmatic dependent of
 // the partial kernel so its launch overlaps the partial kernel's tail; it waits
 // on the grid dependency before touching the partials.
 
@@ -20,7 +22,8 @@
 namespace int8kv {
 namespace {
 
-constexpr int kCombineWarps = 8;   // split range cut into 8 slices, one per warp
+constexpr int kCombineWarps = 8;       // splits cut into 8 slices, one per warp
+constexpr int kPerLane = kMaxSplits / kCombineWarps;   // splits a lane may hold (32)
 
 __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeArgs a) {
   const int dchunk = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
@@ -30,46 +33,53 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
   __shared__ float2 part[kCombineWarps][32];
   ptx::grid_dependency_wait();
   const size_t h = (size_t)b * a.H + hq;
-  const float2* ml = a.ws.part_ml + h * S;
-  if (warp == 0) {
+  // every lane first puts its partial rows in flight (they do not depend on the
+  // weights): warp `warp` takes splits warp, warp + 8, ...; a lane two dims
+  const int d = dchunk * 64 + 2 * lane;
+  const float* po = a.ws.part_o + h * S * D + d;
+  float2 x[kPerLane];
+#pragma unroll
+  for (int k = 0; k < kPerLane; ++k) {
+    const int s = warp + k * kCombineWarps;
+    x[k] = s < S ? *reinterpret_cast<const float2*>(po + (size_t)s * D) : make_float2(0.f, 0.f);
+  }
+  if (warp == 0) {   // split weights 2^(m_s - M) / L
+    const float2* ml = a.ws.part_ml + h * S;
+    float2 v[kMaxSplits / 32];
+#pragma unroll
+    for (int k = 0; k < kMaxSplits / 32; ++k) {
+      const int s = lane + 32 * k;
+      v[k] = s < S ? ml[s] : make_float2(-INFINITY, 0.f);
+    }
     float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, ml[s].x);
+#pragma unroll
+    for (int k = 0; k < kMaxSplits / 32; ++k) M = fmaxf(M, v[k].x);
     M = warp_max(M);
-    float Ls = 0.f;
-    if (M != -INFINITY)
-      for (int s = lane; s < S; s += 32) {
-        const float2 v = ml[s];
-        if (v.y > 0.f) Ls = fmaf(v.y, exp2f(v.x - M), Ls);
-      }
+    float f[kMaxSplits / 32], Ls = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxSplits / 32; ++k) {
+      f[k] = (M == -INFINITY || v[k].y == 0.f) ? 0.f : exp2f(v[k].x - M);
+      Ls = fmaf(v[k].y, f[k], Ls);
+    }
     Ls = warp_sum(Ls);
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    for (int s = lane; s < S; s += 32) {
-      const float2 v = ml[s];
-      w[s] = (v.y > 0.f && M != -INFINITY) ? exp2f(v.x - M) * inv : 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxSplits / 32; ++k) {
+      const int s = lane + 32 * k;
+      if (s < S) w[s] = f[k] * inv;
     }
   }
   __syncthreads();
-  // warp `warp` sums splits warp, warp + 8, ...; each lane two adjacent dims
-  const int d = dchunk * 64 + 2 * lane;
-  const float* po = a.ws.part_o + h * S * D + d;
-  float2 acc[4] = {};
-  int s = warp, k = 0;
-  for (; s + 3 * kCombineWarps < S; s += 4 * kCombineWarps) {
+  float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float2 v = *reinterpret_cast<const float2*>(po + (size_t)(s + u * kCombineWarps) * D);
-      const float ws = w[s + u * kCombineWarps];
-      acc[u].x = fmaf(ws, v.x, acc[u].x);
-      acc[u].y = fmaf(ws, v.y, acc[u].y);
+  for (int k = 0; k < kPerLane; ++k) {
+    const int s = warp + k * kCombineWarps;
+    if (s < S) {
+      acc.x = fmaf(w[s], x[k].x, acc.x);
+      acc.y = fmaf(w[s], x[k].y, acc.y);
     }
   }
-  for (; s < S; s += kCombineWarps, k = (k + 1) & 3) {
-    const float2 v = *reinterpret_cast<const float2*>(po + (size_t)s * D);
-    acc[k].x = fmaf(w[s], v.x, acc[k].x);
-    acc[k].y = fmaf(w[s], v.y, acc[k].y);
-  }
-  part[warp][lane] = make_float2(acc[0].x + acc[1].x + acc[2].x + acc[3].x,
-                                 acc[0].y + acc[1].y + acc[2].y + acc[3].y);
+  part[warp][lane] = acc;
   __syncthreads();
   if (warp == 0) {
     float2 o = part[0][lane];

@@ -87,7 +87,7 @@ struct Layout : mma::StagedPage<D, KI8, VI8> {
   static constexpr int NS_FIT = (70 * 1024) / SP::STAGE;          // three blocks per SM when it fits
   static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 4 ? 4 : NS_FIT);
   // epilogue buffers (reuse the stages): warp partials, block partial, last-step weights
-  static constexpr int MERGE = kConsumerWarps * 8 * (D + 1) * 4 + 8 * D * 4 + kMaxSplits * 8 * 4;
+  static constexpr int MERGE = kConsumerWarps * 8 * (D + 4) * 4 + 8 * D * 4;
   static constexpr int BARS = NS * SP::STAGE;
   static constexpr int SMEM = 1024 + BARS + 2 * NS * 8 + NS * 4 + 64;   // stages, barriers, page ids
   static_assert(MERGE <= NS * SP::STAGE, "merge buffer must fit in the stages");
@@ -374,8 +374,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   int* stage_page = (int*)(full + 2 * LY::NS);
   __shared__ float s_m[kConsumerWarps][8], s_l[kConsumerWarps][8];
   __shared__ float s_f[kConsumerWarps][8], s_inv[8];
-  __shared__ float s_cm[8][8], s_cl[8][8], s_cM[8], s_cL[8];
-  __shared__ int s_last;
+  __shared__ float s_cm[8][8], s_cl[8][8], s_cL[8];
   __shared__ int s_rel[4];                // per stage: release tickets (the last warp refills)
   __shared__ int s_pages[kPagesCached];   // physical page of the block's first pages
 
@@ -386,6 +385,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   constexpr int ng = NG, gs = D / NG;   // scale groups per row and their width (>= 64)
 
   if (threadIdx.x == 0) {
+    ptx::prefetch_tensormap(&tmk);   // kernel parameters: safe before the grid dependency
+    ptx::prefetch_tensormap(&tmv);
     for (int s = 0; s < LY::NS; ++s) {
       ptx::mbar_init(&full[s], 1);
       s_rel[s] = 0;
@@ -436,8 +437,6 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     return i < kPagesCached ? s_pages[i] : lookup_page(ptrow, p_first + i, a.max_pages, p);
   };
   if (threadIdx.x == 0) {
-    ptx::prefetch_tensormap(&tmk);
-    ptx::prefetch_tensormap(&tmv);
     for (int i = 0; i < n_pg && i < LY::NS; ++i) {
       const int page = page_of(i);
       issue_page<D, KI8, VI8>(smem, full, stage_page, i, page, page_row(page), p, kvh, &tmk,
@@ -530,7 +529,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   }
   __syncthreads();   // every stage consumed: the stage memory becomes the merge buffer
 
-  constexpr int DP = D + 1;                      // padded row: fewer bank conflicts
+  constexpr int DP = D + 4;                      // padded row (16-byte aligned): fewer conflicts
   float* s_o = reinterpret_cast<float*>(smem);   // [warp][head 8][D + 1]
   if (r == 0) {
     s_m[warp][2 * t] = m0;
@@ -578,9 +577,32 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   }
   __syncthreads();
 
-  // ---- this block's partial (M, L, O~): O~ to shared memory for the cluster
+  // ---- this block's partial (M, L, O~) of its split
+  if (a.n_splits > kMaxCluster) {
+    // many splits: the partial goes to the workspace and the combine kernel
+    // (launched next, as a programmatic dependent) reduces the splits.
+    // Thread: 4 consecutive dims (one 16-byte store) of heads g0, g0 + stride, ...
+    constexpr int TPH = D / 4;                    // threads per head row
+    constexpr int HSTEP = kThreads / TPH;         // heads handled in parallel
+    const int d = (threadIdx.x % TPH) * 4;
+    for (int g = threadIdx.x / TPH; g < G; g += HSTEP) {
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float4 x = *reinterpret_cast<const float4*>(s_o + ((size_t)w * 8 + g) * DP + d);
+        const float f = s_f[w][g];
+        O.x = fmaf(x.x, f, O.x);
+        O.y = fmaf(x.y, f, O.y);
+        O.z = fmaf(x.z, f, O.z);
+        O.w = fmaf(x.w, f, O.w);
+      }
+      const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
+      *reinterpret_cast<float4*>(a.ws.part_o + (h * a.n_splits + split) * D + d) = O;
+      if (d == 0) a.ws.part_ml[h * a.n_splits + split] = make_float2(s_m[0][g], s_inv[g]);
+    }
+    return;
+  }
   float* cta_o = s_o + kConsumerWarps * 8 * DP;   // [8][D]
-  float* s_w = cta_o + 8 * D;                     // [n_partials][8] weights of the last step
   for (int e = threadIdx.x; e < G * D; e += kThreads) {
     const int g = e / D, d = e - g * D;
     float O = 0.f;
@@ -589,8 +611,9 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     cta_o[g * D + d] = O;
   }
 
-  // ---- cluster reduce: block `rank` combines dims [rank*D/CS, (rank+1)*D/CS) over
-  // the CS splits of its cluster, reading their partials from distributed shared memory
+  // ---- up to 8 splits form one cluster: block `rank` combines dims
+  // [rank*D/CS, (rank+1)*D/CS) over the cluster's splits, reading their partials
+  // from distributed shared memory, and writes the output
   cg::cluster_group cluster = cg::this_cluster();
   const int CS = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
   cluster.sync();
@@ -610,14 +633,13 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       s_cm[j][g] = f;   // now the weight of block j
       Ls = fmaf(s_cl[j][g], f, Ls);
     }
-    s_cM[g] = M;
     s_cL[g] = Ls;
   }
   __syncthreads();
-  const int n_part = a.n_splits / CS, cid = split / CS;
-  const int slice = D / CS, d0 = rank * slice;
+  const int slice = (D + CS - 1) / CS, d0 = rank * slice;   // CS need not divide D
   for (int e = threadIdx.x; e < G * slice; e += kThreads) {
     const int g = e / slice, d = d0 + (e - g * slice);
+    if (d >= D) continue;
     float v[kMaxCluster];
 #pragma unroll
     for (int j = 0; j < kMaxCluster; ++j)   // all remote loads in flight at once
@@ -628,77 +650,9 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       if (j < CS) O = fmaf(s_cm[j][g], v[j], O);
     const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
     const float Ls = s_cL[g];
-    if (n_part == 1) {
-      a.out[h * D + d] = Ls > 0.f ? O / Ls : 0.f;
-    } else {
-      a.ws.part_o[(h * n_part + cid) * D + d] = O;
-      if (rank == 0 && e - g * slice == 0)
-        a.ws.part_ml[h * n_part + cid] = make_float2(s_cM[g], Ls);
-    }
+    a.out[h * D + d] = Ls > 0.f ? O / Ls : 0.f;
   }
-  if (n_part == 1) {
-    cluster.sync();   // no block leaves while others read its shared memory
-    return;
-  }
-
-  // ---- the last cluster of this (sequence, kv head) to finish combines the
-  // cluster partials (atomic ticket, nobody waits for anybody)
-  __threadfence();
-  cluster.sync();
-  if (rank == 0 && threadIdx.x == 0) {
-    const unsigned t = atomicAdd(a.ws.counters + (size_t)b * p.Hkv + kvh, 1u);
-    const int last = t == (unsigned)n_part - 1;
-    for (int j = 0; j < CS; ++j) *cluster.map_shared_rank(&s_last, j) = last;
-  }
-  cluster.sync();
-  if (!s_last) return;
-  __threadfence();
-  // one warp per head: weights of the cluster partials, every lane's loads in flight
-  for (int g = warp; g < G; g += kConsumerWarps) {
-    const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
-    const float2* ml = a.ws.part_ml + h * n_part;
-    float2 v[kMaxSplits / 32];
-#pragma unroll
-    for (int k = 0; k < kMaxSplits / 32; ++k) {
-      const int c = lane + 32 * k;
-      v[k] = c < n_part ? __ldcg(ml + c) : make_float2(-INFINITY, 0.f);
-    }
-    float M = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < kMaxSplits / 32; ++k) M = fmaxf(M, v[k].x);
-    M = warp_max(M);
-    float f[kMaxSplits / 32], Ls = 0.f;
-#pragma unroll
-    for (int k = 0; k < kMaxSplits / 32; ++k) {
-      f[k] = (M == -INFINITY || v[k].y == 0.f) ? 0.f : ptx::ex2(v[k].x - M);
-      Ls = fmaf(v[k].y, f[k], Ls);
-    }
-    Ls = warp_sum(Ls);
-    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-#pragma unroll
-    for (int k = 0; k < kMaxSplits / 32; ++k) {
-      const int c = lane + 32 * k;
-      if (c < n_part) s_w[c * 8 + g] = f[k] * inv;
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < G * slice; e += kThreads) {
-    const int g = e / slice, d = d0 + (e - g * slice);
-    const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
-    const float* po = a.ws.part_o + h * n_part * D + d;
-    float acc[8] = {};
-    int c = 0;
-    for (; c + 8 <= n_part; c += 8) {   // eight independent loads per round
-      float x[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) x[u] = __ldcg(po + (size_t)(c + u) * D);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) acc[u] = fmaf(s_w[(c + u) * 8 + g], x[u], acc[u]);
-    }
-    for (; c < n_part; ++c) acc[0] = fmaf(s_w[c * 8 + g], __ldcg(po + (size_t)c * D), acc[0]);
-    a.out[h * D + d] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-  }
-  if (rank == 0 && threadIdx.x == 0) a.ws.counters[(size_t)b * p.Hkv + kvh] = 0u;
+  cluster.sync();   // no block leaves while others read its shared memory
 }
 
 template <int D, bool KI8, bool VI8, int NG>
@@ -720,8 +674,9 @@ cudaError_t launch_typed(const DecodeArgs& a, const CUtensorMap& tmk, const CUte
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = LY::SMEM;
   cfg.stream = stream;
-  int cs = kMaxCluster;   // largest power of two <= 8 dividing n_splits
-  while (a.n_splits % cs) cs >>= 1;
+  // up to 8 splits: one cluster combines them in the kernel; more: no cluster,
+  // the combine kernel follows
+  const int cs = a.n_splits <= kMaxCluster ? a.n_splits : 1;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -772,20 +727,13 @@ int resident_typed() {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM) !=
       cudaSuccess)
     return 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kMaxCluster * 64, 1, 1);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = LY::SMEM;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kMaxCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) return 0;
-  return clusters * kMaxCluster;
+  int per_sm = 0, dev = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, LY::SMEM) !=
+          cudaSuccess ||
+      cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return per_sm * sms;
 }
 
 template <int D, bool KI8, bool VI8>
@@ -798,7 +746,7 @@ int resident_ng(int ng) {
 }
 
 // Blocks of the tensor-core kernel for this shape that the current device keeps
-// resident at once, launched in clusters of 8; 0 if unknown.
+// resident at once; 0 if unknown.
 int decode_mma_resident_blocks(int D, bool k8, bool v8, int ng) {
   if (D == 256) {
     if (k8 && v8) return resident_ng<256, true, true>(ng);

@@ -76,12 +76,8 @@ extern "C" int attn_decode_int8_noalloc(const int8kv_pool* pool, int layer, cons
   const size_t need = int8kv::decode_workspace_layout(batch, n_heads, pool->n_kv_heads,
                                                       pool->head_dim, n_splits, &ws, base);
   if (need > kNoAllocScratchBytes) return INT8KV_ERR_CAPACITY;
-  // The scratch keeps whatever the previous call left; the arrival tickets
-  // must start at zero.
-  if (need > 0 &&
-      cudaMemsetAsync(ws.counters, 0, (size_t)batch * pool->n_kv_heads * sizeof(unsigned),
-                      (cudaStream_t)stream) != cudaSuccess)
-    return INT8KV_ERR_CUDA;
+  // The scratch keeps whatever the previous call left; nothing in it has to
+  // start at zero (every partial a call reads, the same call writes first).
   return attn_decode_int8(pool, layer, q, batch, n_heads, seq_lens, page_table,
                           max_pages_per_seq, window, softmax_scale, n_splits, out,
                           need > 0 ? base : nullptr, need > 0 ? kNoAllocScratchBytes : 0, stream);

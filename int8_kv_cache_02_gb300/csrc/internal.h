@@ -57,12 +57,10 @@ inline PoolView layer_view(const int8kv_pool* p, int layer) {
 }
 
 // Workspace of the split-K decode: partial (m, l) and unnormalised o per
-// (sequence, query head, split), and one arrival ticket per (sequence, kv head)
-// for the in-kernel combine (zero between calls).
+// (sequence, query head, split); every call overwrites what it reads.
 struct DecodeWorkspace {
   float* part_o;      // [B][H][n_splits][D]
   float2* part_ml;    // [B][H][n_splits]
-  unsigned* counters; // [B][Hkv]
 };
 
 size_t decode_workspace_layout(int B, int H, int Hkv, int D, int n_splits,

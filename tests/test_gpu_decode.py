@@ -374,3 +374,16 @@ def test_decode_append_equals_append_then_decode(D, gs, ps, variant, window):
     for b, L in enumerate(lens):
         orc.append_contiguous(0, ks[b].numpy(), vs[b].numpy(), 0, pt[b].numpy())
     gu.assert_attention_close(outs[1], _oracle(orc, 0, q, lens, pt, window=window), "fused")
+
+
+@pytest.mark.parametrize("n_splits", [2, 3, 5, 7, 8, 9, 13])
+def test_split_counts_around_the_cluster_size(n_splits):
+    """Up to 8 splits combine inside the kernel (one cluster, any size); more go through
+    the combine kernel.  Cluster sizes that do not divide head_dim included."""
+    lens = [1500, 700]
+    q, pt, dev, orc = _setup(900 + n_splits, 2, 16, 2, 256, 64, lens, 0, outliers=True)
+    out = _decode(dev, 0, q, lens, pt, n_splits=n_splits)
+    gu.assert_attention_close(out, _oracle(orc, 0, q, lens, pt), f"n_splits {n_splits}")
+    q, pt, dev, orc = _setup(950 + n_splits, 1, 8, 2, 128, 128, [900], 1)
+    out = _decode(dev, 0, q, [900], pt, n_splits=n_splits)
+    gu.assert_attention_close(out, _oracle(orc, 0, q, [900], pt), f"D128 n_splits {n_splits}")
