@@ -15,18 +15,22 @@ __device__ __forceinline__ void flag_error(int32_t* err, int bits) {
 
 // Physical page of logical page `lp` of a sequence, or -1 (flagged) when the
 // table entry or the index is outside the pool.
+// A page-table entry, or -1 (flagged) when it names no page of the pool.
+__device__ __forceinline__ int check_page(int pg, const PoolView& p) {
+  if (pg < 0 || pg >= p.n_pages) {
+    flag_error(p.err, INT8KV_DEVERR_PAGE_ID);
+    return -1;
+  }
+  return pg;
+}
+
 __device__ __forceinline__ int lookup_page(const int32_t* row, int lp, int max_pages,
                                            const PoolView& p) {
   if (lp < 0 || lp >= max_pages) {
     flag_error(p.err, INT8KV_DEVERR_LENGTH);
     return -1;
   }
-  const int pg = __ldg(row + lp);
-  if (pg < 0 || pg >= p.n_pages) {
-    flag_error(p.err, INT8KV_DEVERR_PAGE_ID);
-    return -1;
-  }
-  return pg;
+  return check_page(__ldg(row + lp), p);
 }
 
 // Row index (in units of head_dim values) of (page, kv head, slot).

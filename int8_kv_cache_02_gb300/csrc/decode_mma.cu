@@ -86,8 +86,13 @@ struct Layout : mma::StagedPage<D, KI8, VI8> {
   using SP = mma::StagedPage<D, KI8, VI8>;
   static constexpr int NS_FIT = (70 * 1024) / SP::STAGE;          // three blocks per SM when it fits
   static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 4 ? 4 : NS_FIT);
-  // epilogue buffers (reuse the stages): warp partials, block partial, last-step weights
-  static constexpr int MERGE = kConsumerWarps * 8 * (D + 4) * 4 + 8 * D * 4;
+  // epilogue buffers (reuse the stages): warp partials [warp][head 8][DP], block
+  // partial [8][D].  Row pitch DP and dim placement make the warps' fragment
+  // stores conflict free: with int8 V a lane holds dims 8r + 2m (+1) of heads
+  // 2t, 2t+1, placed at d + d/32 in rows of pitch = 1 (mod 16); with fp16 V,
+  // dims r (+8) of the same heads in rows of pitch D + 4 (= 4 mod 16).
+  static constexpr int DP = VI8 ? ((D + D / 32) / 16 + 1) * 16 + 1 : D + 4;
+  static constexpr int MERGE = kConsumerWarps * 8 * DP * 4 + 8 * D * 4;
   static constexpr int BARS = NS * SP::STAGE;
   static constexpr int SMEM = 1024 + BARS + 2 * NS * 8 + NS * 4 + 64;   // stages, barriers, page ids
   static_assert(MERGE <= NS * SP::STAGE, "merge buffer must fit in the stages");
@@ -124,6 +129,62 @@ __device__ __forceinline__ void load_row_scales(const unsigned char* base, int r
     x[0] = __half2float(*reinterpret_cast<const __half*>(p));
   }
 }
+
+// The new token's K or V row as one lane of a warp holds it (values
+// [lane*VPL, (lane+1)*VPL)): its int8 codes and its group's scale, or, for an
+// fp16 store, the values themselves.
+template <int D, bool I8>
+struct NewRow {
+  static constexpr int VPL = D / 32;
+  typename Vec<VPL>::H raw;
+  typename Vec<VPL>::B codes;
+  uint16_t scale;
+
+  // The lane's values (one vector load), then, for an int8 store, their codes
+  // and their group's scale.
+  __device__ __forceinline__ void fetch(const uint16_t* src, int lane) {
+    raw = *reinterpret_cast<const typename Vec<VPL>::H*>(src + lane * VPL);
+  }
+  __device__ __forceinline__ void quantize(int lanes_per_group) {
+    if constexpr (I8) {
+      float x[VPL];
+      const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+      for (int i = 0; i < VPL / 2; ++i) {
+        const float2 f = __half22float2(h2[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+      }
+      quantize_regs<VPL>(x, lanes_per_group, codes, scale);
+    }
+  }
+  // Over row `slot` of a staged page: boxes of 64 rows x 128 B with the
+  // 128-byte swizzle, scales rows of ng fp16.
+  __device__ __forceinline__ void stage(unsigned char* boxes, unsigned char* scales, int slot,
+                                        int lane, int lanes_per_group, int ng) const {
+    constexpr int EB = I8 ? 1 : 2;   // bytes per value
+    const int byte0 = lane * VPL * EB, box = byte0 >> 7, inb = byte0 & 127;
+    unsigned char* dst =
+        boxes + box * kBoxBytes + slot * 128 + (((inb >> 4) ^ (slot & 7)) << 4) + (inb & 15);
+    if constexpr (I8) {
+      *reinterpret_cast<typename Vec<VPL>::B*>(dst) = codes;
+      if (lane % lanes_per_group == 0)
+        reinterpret_cast<uint16_t*>(scales)[slot * ng + lane / lanes_per_group] = scale;
+    } else {
+      *reinterpret_cast<typename Vec<VPL>::H*>(dst) = raw;
+    }
+  }
+  // Into pool row `row` (values row * D on, scales row * ng on).
+  __device__ __forceinline__ void store(void* values, uint16_t* scales, size_t row, int lane,
+                                        int lanes_per_group, int ng) const {
+    if constexpr (I8) {
+      *reinterpret_cast<typename Vec<VPL>::B*>((int8_t*)values + row * D + lane * VPL) = codes;
+      if (lane % lanes_per_group == 0) scales[row * ng + lane / lanes_per_group] = scale;
+    } else {
+      *reinterpret_cast<typename Vec<VPL>::H*>((uint16_t*)values + row * D + lane * VPL) = raw;
+    }
+  }
+};
 
 // One 16-token tile of one page for one warp: scores for the G heads, online
 // softmax (lazy: the reference max moves only when a score exceeds it by more
@@ -376,13 +437,15 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   __shared__ float s_f[kConsumerWarps][8], s_inv[8];
   __shared__ float s_cm[8][8], s_cl[8][8], s_cL[8];
   __shared__ int s_rel[4];                // per stage: release tickets (the last warp refills)
-  __shared__ int s_pages[kPagesCached];   // physical page of the block's first pages
+  // page ids: the sequence's whole page-table row when it has at most
+  // kPagesCached entries, else the entries of the block's first pages
+  __shared__ int s_pages[kPagesCached];
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const PoolView& p = a.pool;
   const int G = a.G;
-  constexpr int ng = NG, gs = D / NG;   // scale groups per row and their width (>= 64)
+  constexpr int gs = D / NG;   // width of a scale group (>= 64)
 
   if (threadIdx.x == 0) {
     ptx::prefetch_tensormap(&tmk);   // kernel parameters: safe before the grid dependency
@@ -399,7 +462,46 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   ptx::grid_dependency_wait();
   ptx::grid_launch_dependents();
 
-  const int L_raw = __ldg(a.seq_lens + b);
+  const int L_raw = ptx::ldg32(a.seq_lens + b);
+  // A short page-table row is read whole, along with the length (the block's
+  // pages are not known before it).
+  const int32_t* ptrow = a.page_table + (size_t)b * a.max_pages;
+  const bool row_cached = a.max_pages <= kPagesCached;
+  if (row_cached) {
+    constexpr int PER = kPagesCached / kThreads;
+    int e[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int i = threadIdx.x + k * kThreads;
+      e[k] = i < a.max_pages ? ptx::ldg32(ptrow + i) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < PER; ++k) s_pages[threadIdx.x + k * kThreads] = e[k];
+  }
+  // q of head r (B operand columns = heads): requested now, arranged in the
+  // slot order of the K loads once the pages are on their way
+  const int r = lane >> 2, t = lane & 3;
+  constexpr int QV = D / 64 * 2;   // 16-byte pieces of q a lane holds
+  uint4 qraw[QV];
+  {
+    const bool live = r < G;
+    const uint16_t* qh = a.q + ((size_t)b * a.H + (size_t)kvh * G + (live ? r : 0)) * D;
+#pragma unroll
+    for (int v = 0; v < QV; ++v) {
+      // int8 K: dims 64mc + 16t + 8h (v = 2mc + h); fp16 K: dims 16ks + 2t (+8), see below
+      if constexpr (KI8)
+        qraw[v] = live ? ptx::ldg128(qh + (v >> 1) * 64 + 16 * t + 8 * (v & 1)) : make_uint4(0, 0, 0, 0);
+    }
+    if constexpr (!KI8) {
+      const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qh);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t* w = reinterpret_cast<uint32_t*>(&qraw[ks >> 1]) + 2 * (ks & 1);
+        w[0] = live ? __ldg(q32 + (ks * 16 + 2 * t) / 2) : 0u;
+        w[1] = live ? __ldg(q32 + (ks * 16 + 8 + 2 * t) / 2) : 0u;
+      }
+    }
+  }
   const int L = clamp_length(L_raw, a.max_pages, p);
   const int lo_pos = a.window > 0 ? max(0, L - a.window) : 0;
   int j0, j1;
@@ -407,45 +509,108 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   const int p_first = j0 / kPage;
   const int n_pg = j1 > j0 ? (j1 - 1) / kPage - p_first + 1 : 0;
 
-  // Page ids of the block's range go to shared memory once; thread 0 fills the
-  // ring with the first NS pages, and afterwards the last warp to release a
-  // stage refills it with page i + NS at once.
-  const int32_t* ptrow = a.page_table + (size_t)b * a.max_pages;
+  // Fused append: when the block's range holds the new token (position L-1),
+  // it is the range's last row.  The warp whose tile holds it writes the new K
+  // row, its neighbour the new V row (loads issued here, the rest once the
+  // pages are requested).  No other block reads the row.
+  const bool appends = a.k_new != nullptr && L == L_raw && L > 0 && L - 1 >= j0 && L - 1 < j1;
+  const int app_slot = (L - 1) & (kPage - 1);
+  const bool app_k = appends && warp == app_slot / 16;
+  const bool app_v = appends && warp == ((app_slot / 16) ^ 1);
+  NewRow<D, KI8> nk;
+  NewRow<D, VI8> nv;
+  if (app_k) nk.fetch(a.k_new + ((size_t)b * p.Hkv + kvh) * D, lane);
+  if (app_v) nv.fetch(a.v_new + ((size_t)b * p.Hkv + kvh) * D, lane);
+
+  // Thread 0 fills the ring with the first NS pages; afterwards the last warp
+  // to release a stage refills it with page i + NS.  When the row is not held
+  // whole, the ids of the block's first pages go to shared memory meanwhile;
+  // no barrier is needed before the refills read them: every warp writes its
+  // share before it first releases a stage (a release the refilling warp
+  // acquires), and the consumers learn of a stage's page through its mbarrier.
   auto page_row = [&](int page) { return ((layer_page0 + page) * p.Hkv + kvh) * kPage; };
-  for (int i = threadIdx.x; i < n_pg && i < kPagesCached; i += kThreads)
-    s_pages[i] = lookup_page(ptrow, p_first + i, a.max_pages, p);
-  // Fused append: the block whose range holds the new token (position L-1)
-  // quantizes its K and V rows into the pool before any copy of that page is
-  // issued; no other block reads the page.
-  if (a.k_new != nullptr && L == L_raw && L > 0 && L - 1 >= j0 && L - 1 < j1 && warp < 2) {
-    const int pos = L - 1;
-    const int page = lookup_page(ptrow, pos / kPage, a.max_pages, p);
-    if (page >= 0) {
-      constexpr int VPL = D / 32;
-      const size_t row = row_index(p, page, kvh, pos % kPage);
-      const uint16_t* src = (warp == 0 ? a.k_new : a.v_new) + ((size_t)b * p.Hkv + kvh) * D;
-      if (warp == 0 ? KI8 : VI8)
-        quantize_row<VPL>(src, (int8_t*)(warp == 0 ? p.k : p.v) + row * D,
-                          (uint16_t*)(warp == 0 ? p.ks : p.vs) + row * NG, lane, (D / NG) / VPL);
-      else
-        copy_row<VPL>(src, (uint16_t*)(warp == 0 ? p.k : p.v) + row * D, lane);
-      ptx::fence_proxy_async_global();   // visible to the tensor copies that follow
-    }
-  }
-  __syncthreads();
-  auto page_of = [&](int i) {
-    return i < kPagesCached ? s_pages[i] : lookup_page(ptrow, p_first + i, a.max_pages, p);
+  if (row_cached) __syncthreads();
+  auto page_direct = [&](int i) {   // page i of the block's range, from the row or from memory
+    return row_cached ? check_page(s_pages[p_first + i], p)
+                      : lookup_page(ptrow, p_first + i, a.max_pages, p);
   };
   if (threadIdx.x == 0) {
-    for (int i = 0; i < n_pg && i < LY::NS; ++i) {
-      const int page = page_of(i);
-      issue_page<D, KI8, VI8>(smem, full, stage_page, i, page, page_row(page), p, kvh, &tmk,
-                              &tmv);
+    int first[LY::NS];
+#pragma unroll
+    for (int i = 0; i < LY::NS; ++i)   // independent loads, in flight together
+      first[i] = i < n_pg ? page_direct(i) : -1;
+#pragma unroll
+    for (int i = 0; i < LY::NS; ++i)
+      if (i < n_pg)
+        issue_page<D, KI8, VI8>(smem, full, stage_page, i, first[i], page_row(first[i]), p, kvh,
+                                &tmk, &tmv);
+  }
+  if (!row_cached)
+    for (int i = threadIdx.x; i < n_pg && i < kPagesCached; i += kThreads)
+      s_pages[i] = lookup_page(ptrow, p_first + i, a.max_pages, p);
+  auto page_of = [&](int i) {
+    if (row_cached) return check_page(s_pages[p_first + i], p);
+    return i < kPagesCached ? s_pages[i] : lookup_page(ptrow, p_first + i, a.max_pages, p);
+  };
+  uint32_t qf[KSTEPS][2];
+  if constexpr (KI8) {
+#pragma unroll
+    for (int mc = 0; mc < MACROS; ++mc) {
+      // dims 64mc + 16t .. +16: k-step i takes (4i, 4i+2) and (4i+1, 4i+3)
+      const uint4 x = qraw[2 * mc], y = qraw[2 * mc + 1];
+      const uint32_t w[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        qf[mc * 4 + i][0] = ptx::prmt(w[2 * i], w[2 * i + 1], 0x5410);
+        qf[mc * 4 + i][1] = ptx::prmt(w[2 * i], w[2 * i + 1], 0x7632);
+      }
     }
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(&qraw[ks >> 1]) + 2 * (ks & 1);
+      qf[ks][0] = w[0];
+      qf[ks][1] = w[1];
+    }
+  }
+  if (app_k || app_v) {
+    // If the last page was issued above, the new row is written over its
+    // staged row once it has landed (the copy brought the row's old contents)
+    // and then to the pool; otherwise it goes to the pool now, ahead of that
+    // page's copy (a refill, issued only after both warps released a stage).
+    constexpr int LPG = (D / NG) / (D / 32);   // lanes per scale group
+    if (app_k)
+      nk.quantize(LPG);
+    else
+      nv.quantize(LPG);
+    const int last = n_pg - 1;
+    int page = -1;
+    if (last < LY::NS) {
+      if (ptx::mbar_wait(&full[last], 0, kMaxPolls)) {
+        page = stage_page[last];
+        if (page >= 0) {
+          unsigned char* sw = smem + last * LY::STAGE;
+          if (app_k)
+            nk.stage(sw + LY::K_OFF, sw + LY::KS_OFF, app_slot, lane, LPG, NG);
+          else
+            nv.stage(sw + LY::V_OFF, sw + LY::VS_OFF, app_slot, lane, LPG, NG);
+        }
+      }   // a timeout is flagged by the loop's own wait on this stage
+    } else {
+      page = page_direct(last);
+    }
+    if (page >= 0) {
+      const size_t row = row_index(p, page, kvh, app_slot);
+      if (app_k)
+        nk.store((void*)p.k, (uint16_t*)p.ks, row, lane, LPG, NG);
+      else
+        nv.store((void*)p.v, (uint16_t*)p.vs, row, lane, LPG, NG);
+      if (last >= LY::NS) ptx::fence_proxy_async_global();   // visible to that copy
+    }
+    ptx::named_barrier_sync(1, 64);   // both rows in place before either warp reads them
   }
 
   // ---------------------------------------------------------------- consumers
-  const int r = lane >> 2, t = lane & 3;
   float o[MTILES][4];
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int vexp[NG];      // per V group: 2^vexp > every V scale this warp has seen
@@ -460,33 +625,6 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   for (int i = 0; i < MTILES; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
   {
-    // q of head r (B operand columns = heads), in the slot order of the K loads
-    uint32_t qf[KSTEPS][2];
-    {
-      const bool live = r < G;
-      const uint16_t* qh = a.q + ((size_t)b * a.H + (size_t)kvh * G + (live ? r : 0)) * D;
-      if constexpr (KI8) {
-#pragma unroll
-        for (int mc = 0; mc < MACROS; ++mc) {
-          // dims 64mc + 16t .. +16: k-step i takes (4i, 4i+2) and (4i+1, 4i+3)
-          const uint4 x = live ? ptx::ldg128(qh + mc * 64 + 16 * t) : make_uint4(0, 0, 0, 0);
-          const uint4 y = live ? ptx::ldg128(qh + mc * 64 + 16 * t + 8) : make_uint4(0, 0, 0, 0);
-          const uint32_t w[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            qf[mc * 4 + i][0] = ptx::prmt(w[2 * i], w[2 * i + 1], 0x5410);
-            qf[mc * 4 + i][1] = ptx::prmt(w[2 * i], w[2 * i + 1], 0x7632);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int ks = 0; ks < KSTEPS; ++ks) {
-          const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qh);
-          qf[ks][0] = live ? __ldg(q32 + (ks * 16 + 2 * t) / 2) : 0u;
-          qf[ks][1] = live ? __ldg(q32 + (ks * 16 + 8 + 2 * t) / 2) : 0u;
-        }
-      }
-    }
     for (int i = 0; i < n_pg; ++i) {
       const int st = i % LY::NS;
       if (!ptx::mbar_wait(&full[st], (i / LY::NS) & 1, kMaxPolls)) {
@@ -529,8 +667,9 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   }
   __syncthreads();   // every stage consumed: the stage memory becomes the merge buffer
 
-  constexpr int DP = D + 4;                      // padded row (16-byte aligned): fewer conflicts
-  float* s_o = reinterpret_cast<float*>(smem);   // [warp][head 8][D + 1]
+  constexpr int DP = LY::DP;
+  auto pos = [](int d) { return VI8 ? d + (d >> 5) : d; };   // place of dim d in a row
+  float* s_o = reinterpret_cast<float*>(smem);                // [warp][head 8][DP]
   if (r == 0) {
     s_m[warp][2 * t] = m0;
     s_m[warp][2 * t + 1] = m1;
@@ -554,10 +693,10 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     }
     float* h0 = s_o + ((size_t)warp * 8 + 2 * t) * DP;
     float* h1 = h0 + DP;
-    h0[dx] = o[j][0] * u;
-    h1[dx] = o[j][1] * u;
-    h0[dy] = o[j][2] * u;
-    h1[dy] = o[j][3] * u;
+    h0[pos(dx)] = o[j][0] * u;
+    h1[pos(dx)] = o[j][1] * u;
+    h0[pos(dy)] = o[j][2] * u;
+    h1[pos(dy)] = o[j][3] * u;
   }
   __syncthreads();
   if (threadIdx.x < 8) {   // per-head merge weights of the four warps
@@ -589,7 +728,12 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
-        const float4 x = *reinterpret_cast<const float4*>(s_o + ((size_t)w * 8 + g) * DP + d);
+        const float* row = s_o + ((size_t)w * 8 + g) * DP;
+        float4 x;
+        if constexpr (VI8)
+          x = make_float4(row[pos(d)], row[pos(d) + 1], row[pos(d) + 2], row[pos(d) + 3]);
+        else
+          x = *reinterpret_cast<const float4*>(row + d);
         const float f = s_f[w][g];
         O.x = fmaf(x.x, f, O.x);
         O.y = fmaf(x.y, f, O.y);
@@ -607,7 +751,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     const int g = e / D, d = e - g * D;
     float O = 0.f;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) O = fmaf(s_o[((size_t)w * 8 + g) * DP + d], s_f[w][g], O);
+    for (int w = 0; w < kConsumerWarps; ++w)
+      O = fmaf(s_o[((size_t)w * 8 + g) * DP + pos(d)], s_f[w][g], O);
     cta_o[g * D + d] = O;
   }
 

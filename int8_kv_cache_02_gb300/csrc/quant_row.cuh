@@ -4,7 +4,8 @@
 // Method: absmax/127 per group of gs values (genie-ai-runtime v0.1.0-alpha.12
 // "Path I series" I2; Strata pull request #2698 "What it does"):
 //   s = fp16_rn(fp32(absmax) / 127.0f), code = clamp(rint_even(fp32(x) / fp32(s)), -127, 127),
-//   code = 0 when s == 0.  Lane l holds values [l*VPL, (l+1)*VPL) of the row.
+//   code = 0 when s == 0, all divisions IEEE round-to-nearest.  Lane l holds
+//   values [l*VPL, (l+1)*VPL) of the row.
 #pragma once
 
 #include <cstdint>
@@ -34,11 +35,11 @@ __device__ __forceinline__ void load_halves(const uint16_t* src, float (&x)[VPL]
   }
 }
 
+// Codes and scale of the lane's VPL values x; the scale is that of the lane's
+// group (every lane of a group of lanes_per_group lanes gets it).
 template <int VPL>
-__device__ __forceinline__ void quantize_row(const uint16_t* src, int8_t* dst_codes,
-                                             uint16_t* dst_scales, int lane, int lanes_per_group) {
-  float x[VPL];
-  load_halves<VPL>(src + lane * VPL, x);
+__device__ __forceinline__ void quantize_regs(const float (&x)[VPL], int lanes_per_group,
+                                              typename Vec<VPL>::B& codes, uint16_t& scale) {
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) amax = fmaxf(amax, fabsf(x[i]));
@@ -51,14 +52,31 @@ __device__ __forceinline__ void quantize_row(const uint16_t* src, int8_t* dst_co
   for (int i = 0; i < VPL; ++i) {
     int c = 0;
     if (s != 0.f) {
-      c = __float2int_rn(__fdiv_rn(x[i], s));  // round half to even
+      // The code is rint(fl(x / s)) with the IEEE quotient.  |x / s| < 128, so
+      // __fdividef (at most 2 ulp off for these divisors) lands within 2e-5 of
+      // fl(x / s); unless that is within 1e-4 of a half-integer, both round to
+      // the same integer, and only then is the IEEE division needed.
+      float qt = __fdividef(x[i], s);
+      if (fabsf((qt - floorf(qt)) - 0.5f) < 1.0e-4f) qt = __fdiv_rn(x[i], s);
+      c = __float2int_rn(qt);  // round half to even
       c = max(-127, min(127, c));
     }
     out.c[i] = (int8_t)c;
   }
-  *reinterpret_cast<typename Vec<VPL>::B*>(dst_codes + lane * VPL) = out.v;
-  if ((lane % lanes_per_group) == 0) dst_scales[(lane * VPL) / (lanes_per_group * VPL)] =
-      __half_as_ushort(s16);
+  codes = out.v;
+  scale = __half_as_ushort(s16);
+}
+
+template <int VPL>
+__device__ __forceinline__ void quantize_row(const uint16_t* src, int8_t* dst_codes,
+                                             uint16_t* dst_scales, int lane, int lanes_per_group) {
+  float x[VPL];
+  load_halves<VPL>(src + lane * VPL, x);
+  typename Vec<VPL>::B codes;
+  uint16_t scale;
+  quantize_regs<VPL>(x, lanes_per_group, codes, scale);
+  *reinterpret_cast<typename Vec<VPL>::B*>(dst_codes + lane * VPL) = codes;
+  if ((lane % lanes_per_group) == 0) dst_scales[(lane * VPL) / (lanes_per_group * VPL)] = scale;
 }
 
 template <int VPL>

@@ -26,6 +26,10 @@ measured on):
                 come from their own generator, seed ``3_000_000 + 1000*layer + b``,
                 drawing K [L_b][8][128] then V, so any sequence can be rebuilt
                 alone.
+* ``tie_rows``  rows whose every group of gs values has the absmax 127*s0 for
+                an s0 = m * 2^e (m odd, < 8), so that the group's scale is s0
+                exactly, and whose other values are +-(k + 1/2) * s0 (x / s a
+                rounding tie) or one fp16 step away from it.
 * ``prefill``   batch 1, 16/2 heads, head_dim 256, 64-value groups; 32768
                 cached positions plus a causal chunk of 256 new queries; seed 4.
                 Draws: q [256][16][256], K [33024][2][256], V, then the outlier
@@ -145,3 +149,27 @@ def random_case(seed, B, H, Hkv, D, lengths, outliers=False, extra_pos=0):
         ks.append(k)
         vs.append(v)
     return q, ks, vs
+
+
+def tie_rows(n_rows, D, gs, seed):
+    """fp16 [n_rows][D] of values on and next to the code rounding boundaries.
+
+    Group (row, j): s0 = m * 2^e, m in {1, 3, 5, 7}, e in [-20, 4]; one value is
+    +-127*s0, every other one +-(k + 1/2)*s0 with k in [0, 126], two thirds of them
+    moved one fp16 step up or down.  All of these are exact fp16 values: (2k+1)*m
+    < 2^11 and the smallest, 2^-21, is a multiple of the subnormal step 2^-24.
+    """
+    g = torch.Generator().manual_seed(seed)
+    ng = D // gs
+    m = torch.tensor([1, 3, 5, 7])[torch.randint(0, 4, (n_rows, ng), generator=g)]
+    e = torch.randint(-20, 5, (n_rows, ng), generator=g)
+    s0 = m.double() * torch.pow(2.0, e.double())                       # [rows][ng]
+    k = torch.randint(0, 127, (n_rows, ng, gs), generator=g).double()
+    sign = torch.randint(0, 2, (n_rows, ng, gs), generator=g).double() * 2 - 1
+    x = sign * (k + 0.5) * s0[..., None]
+    top = torch.randint(0, gs, (n_rows, ng), generator=g)
+    x.scatter_(2, top[..., None], (sign.gather(2, top[..., None]) * 127.0) * s0[..., None])
+    bits = x.to(F16).view(torch.int16)
+    step = torch.randint(-1, 2, (n_rows, ng, gs), generator=g).to(torch.int16)
+    step.scatter_(2, top[..., None], torch.zeros((n_rows, ng, 1), dtype=torch.int16))
+    return (bits + step).view(F16).reshape(n_rows, D)

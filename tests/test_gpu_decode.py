@@ -376,6 +376,37 @@ def test_decode_append_equals_append_then_decode(D, gs, ps, variant, window):
     gu.assert_attention_close(outs[1], _oracle(orc, 0, q, lens, pt, window=window), "fused")
 
 
+@pytest.mark.parametrize("D,gs,variant", [(256, 64, 0), (256, 256, 0), (128, 64, 0), (256, 64, 2)])
+@pytest.mark.parametrize("ns", [4, 16])
+def test_decode_append_rounds_ties_like_the_oracle(D, gs, variant, ns):
+    """The fused append on rows of rounding ties (x / s = k + 1/2) and their fp16
+    neighbours: the pool rows it writes equal the oracle's, byte for byte, with the
+    new position the last row of a page issued at once or of one refilled later."""
+    from int8_kv_cache_02_gb300 import binding
+    lens = [2000, 129, 64, 1]
+    B, H, Hkv = len(lens), 8, 2
+    q, ks, vs = inputs.random_case(915 + D + gs + ns, B, H, Hkv, D, lens)
+    kn = inputs.tie_rows(B * Hkv, D, gs, seed=D + gs).reshape(B, Hkv, D)
+    vn = inputs.tie_rows(B * Hkv, D, gs, seed=D + gs + 5).reshape(B, Hkv, D)
+    for b, L in enumerate(lens):
+        ks[b][L - 1] = kn[b]
+        vs[b][L - 1] = vn[b]
+    pt, n_pages = inputs.page_table(lens, 64, seed=23)
+    dev, orc = gu.make_pools(1, Hkv, D, gs, 64, n_pages, variant)
+    for b, L in enumerate(lens):
+        if L > 1:
+            gu.fill_sequence(dev, orc, 0, ks[b][:L - 1], vs[b][:L - 1], pt[b])
+    orc.append(0, kn[:, None].numpy(), vn[:, None].numpy(), [L - 1 for L in lens], pt.numpy())
+    out = torch.empty((B, H, D), dtype=torch.float32, device="cuda")
+    binding.attn_decode_append_int8(dev, 0, q.cuda(), kn.cuda(), vn.cuda(),
+                                    torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                                    pt.cuda(), out, dev.decode_workspace(B, H, ns), n_splits=ns)
+    torch.cuda.synchronize()
+    assert binding.kv_pool_read_device_error(dev) == 0
+    gu.regions_equal(dev, orc)
+    gu.assert_attention_close(out.cpu().numpy(), _oracle(orc, 0, q, lens, pt), "ties")
+
+
 @pytest.mark.parametrize("n_splits", [2, 3, 5, 7, 8, 9, 13])
 def test_split_counts_around_the_cluster_size(n_splits):
     """Up to 8 splits combine inside the kernel (one cluster, any size); more go through

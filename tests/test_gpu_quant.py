@@ -46,6 +46,19 @@ def test_append_every_finite_fp16_value():
     assert (orc.k_scales.astype(np.float64) < 2.0 ** -14).any()    # subnormal scales occurred
 
 
+@pytest.mark.parametrize("D,gs", [(256, 64), (128, 128), (64, 32)])
+def test_append_rounding_ties(D, gs):
+    """Values whose quotient x / s is exactly k + 1/2 (round half to even) or one
+    fp16 step from it, for scales from 2^-20 to 7 * 2^4."""
+    n = 512
+    k = inputs.tie_rows(n, D, gs, seed=D + gs).reshape(n, 1, D)
+    v = inputs.tie_rows(n, D, gs, seed=D + gs + 1).reshape(n, 1, D)
+    pt, n_pages = inputs.page_table([n], 64, seed=2)
+    dev, orc = gu.make_pools(1, 1, D, gs, 64, n_pages, 0)
+    gu.fill_sequence(dev, orc, 0, k, v, pt[0])
+    gu.regions_equal(dev, orc)
+
+
 def test_append_batch_of_sequences_at_different_positions():
     from int8_kv_cache_02_gb300 import binding
     B, n_new, Hkv, D, gs, ps = 5, 7, 4, 128, 64, 16

@@ -11,6 +11,7 @@ import os
 import numpy as np
 import pytest
 
+from int8_kv_cache_02_gb300 import inputs
 from oracle import quant
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -139,3 +140,17 @@ def test_dequantize_exact():
     want = np.array([-127, -1, 0, 1], np.float64) * 0.00787353515625
     assert np.array_equal(d[0, :4], want)
     assert np.array_equal(d[0, 4:], np.array([127, 64, -64, 3], np.float64) * 2.0 ** -24)
+
+
+def test_tie_rows_are_rounding_ties():
+    """The tie generator's groups get the intended scale, a third of its values are
+    exact ties (x / s = k + 1/2), and those round to the even code."""
+    x = inputs.tie_rows(64, 256, 64, 7).numpy()
+    codes, scales = quant.quantize(x, 64)
+    assert np.all(np.abs(x.astype(np.float64)).reshape(64, 4, 64).max(-1) ==
+                  127 * scales.astype(np.float64))
+    qt = x.astype(np.float32) / scales.astype(np.float32).repeat(64, axis=-1)
+    ties = (qt - np.floor(qt)) == np.float32(0.5)
+    assert 0.25 < ties.mean() < 0.42
+    assert np.all(codes[ties] % 2 == 0)
+    assert np.all(np.abs(codes[ties].astype(np.float64) - qt[ties]) == 0.5)
