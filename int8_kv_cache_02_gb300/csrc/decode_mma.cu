@@ -644,12 +644,12 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       }
       __syncwarp();   // every lane of this warp is done reading stage st
       if (lane == 0) {
-        __threadfence_block();
-        // tickets only grow: the last warp of every round of four refills
-        if ((atomicAdd(&s_rel[st], 1) & (kConsumerWarps - 1)) == kConsumerWarps - 1) {
-          __threadfence_block();
+        // Tickets only grow: the last warp of every round of four refills.  The
+        // stage's reads have all returned (their values are consumed) before the
+        // release, so the copy that overwrites it needs no proxy fence.
+        if ((ptx::atom_add_acq_rel_shared(&s_rel[st], 1) & (kConsumerWarps - 1)) ==
+            kConsumerWarps - 1) {
           if (i + LY::NS < n_pg) {
-            ptx::fence_proxy_async();   // generic reads of the stage before the async writes
             const int page = page_of(i + LY::NS);
             issue_page<D, KI8, VI8>(smem, full, stage_page, st, page, page_row(page), p, kvh,
                                     &tmk, &tmv);

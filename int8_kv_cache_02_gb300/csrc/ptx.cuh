@@ -54,6 +54,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// Shared-memory counter add with acquire-release ordering at block scope;
+// returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel_shared(int* addr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old) : "r"(smem_u32(addr)), "r"(v) : "memory");
+  return old;
+}
+
 // Barrier `id` (1..15; 0 is __syncthreads) over `count` threads, whole warps.
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

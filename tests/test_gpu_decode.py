@@ -418,3 +418,30 @@ def test_split_counts_around_the_cluster_size(n_splits):
     q, pt, dev, orc = _setup(950 + n_splits, 1, 8, 2, 128, 128, [900], 1)
     out = _decode(dev, 0, q, [900], pt, n_splits=n_splits)
     gu.assert_attention_close(out, _oracle(orc, 0, q, [900], pt), f"D128 n_splits {n_splits}")
+
+
+@pytest.mark.parametrize("n_splits", [9, 16, 40, 100])
+def test_many_splits_twice_on_one_workspace(n_splits):
+    """More than 8 splits go through the combine kernel; a second call on the same
+    workspace gives the same bits."""
+    lens = [6000, 2500]
+    q, pt, dev, orc = _setup(970 + n_splits, 2, 16, 2, 256, 64, lens, 0, outliers=True)
+    ws = dev.decode_workspace(2, 16, n_splits)
+    first = _decode(dev, 0, q, lens, pt, n_splits=n_splits, ws=ws)
+    second = _decode(dev, 0, q, lens, pt, n_splits=n_splits, ws=ws)
+    assert np.array_equal(first, second)
+    from int8_kv_cache_02_gb300 import binding
+    assert binding.kv_pool_read_device_error(dev) == 0
+    gu.assert_attention_close(first, _oracle(orc, 0, q, lens, pt), f"n_splits {n_splits}")
+
+
+def test_many_splits_on_a_grid_larger_than_the_gpu():
+    """64 sequences x 8 kv heads x 16 splits: more blocks than the GPU holds at once,
+    ragged lengths; the result matches the oracle."""
+    g = torch.Generator().manual_seed(12)
+    lens = torch.randint(1, 700, (64,), generator=g).tolist()
+    q, pt, dev, orc = _setup(77, 64, 32, 8, 128, 128, lens, 0)
+    out = _decode(dev, 0, q, lens, pt, n_splits=16)
+    from int8_kv_cache_02_gb300 import binding
+    assert binding.kv_pool_read_device_error(dev) == 0
+    gu.assert_attention_close(out, _oracle(orc, 0, q, lens, pt), "combine kernel")
