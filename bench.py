@@ -266,10 +266,12 @@ def traffic_from_profiles(kernel_src_sha):
 
 
 def decode_source_sha():
+    """Hash of the sources the decode kernels are built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "int8_kv_cache_02_gb300", "csrc")
     for n in sorted(os.listdir(csrc)):
-        if n.startswith("decode") or n in ("common.cuh", "internal.h"):
+        if n.startswith("decode") or n in ("common.cuh", "internal.h", "ptx.cuh",
+                                           "mma_common.cuh", "quant_row.cuh"):
             h.update(open(os.path.join(csrc, n), "rb").read())
     return h.hexdigest()[:16]
 

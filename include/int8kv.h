@@ -157,8 +157,10 @@ int attn_decode_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head
  *   softmax_scale 0 -> 1/sqrt(head_dim)
  *   n_splits     0 -> attn_decode_n_splits() for the longest context the page
  *                table holds (or the window plus one page); 1 -> single pass;
- *                otherwise the key range [lo, L) is cut page-aligned into
- *                n_splits pieces of ceil(pages/n_splits) pages
+ *                otherwise the P pages that hold the key range [lo, L) are
+ *                cut into n_splits runs, split s taking pages
+ *                [s*P/n_splits, (s+1)*P/n_splits) (integer division: the
+ *                counts differ by at most one), clipped to [lo, L)
  *   out          device fp32 [batch][n_heads][head_dim]
  *   workspace    device, >= attn_decode_workspace_bytes, 16-byte aligned, any
  *                contents (every partial a call reads, it writes first).  Calls
