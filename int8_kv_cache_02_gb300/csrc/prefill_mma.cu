@@ -100,8 +100,12 @@ __device__ __forceinline__ void convert_page(const unsigned char* sb, unsigned c
     if (!is8) continue;
     const unsigned char* src = sb + (side == 0 ? SP::K_OFF : SP::V_OFF);
     unsigned char* dst = smem + (side == 0 ? LY::KH_OFF : LY::VH_OFF);
+    // Eight consecutive threads take one code chunk of eight consecutive rows:
+    // rows r..r+7 put the chunk at eight different swizzled positions, so both
+    // the 16-byte loads and the 16-byte fp16 stores are conflict free.
     for (int c = threadIdx.x; c < kPage * CPR; c += kThreads) {
-      const int row = c / CPR, cc = c - row * CPR;
+      const int g8 = c >> 3;
+      const int row = (g8 / CPR) * 8 + (c & 7), cc = g8 % CPR;
       const uint4 w = *reinterpret_cast<const uint4*>(src + (cc >> 3) * kBoxBytes + swz(row, cc & 7));
       uint4 lo, hi;
       codes_to_f16(w, lo, hi);
