@@ -84,7 +84,9 @@ __device__ __forceinline__ int rho(int r) { return (0x37156240u >> (4 * r)) & 0x
 template <int D, bool KI8, bool VI8>
 struct Layout : mma::StagedPage<D, KI8, VI8> {
   using SP = mma::StagedPage<D, KI8, VI8>;
-  static constexpr int NS_FIT = (70 * 1024) / SP::STAGE;          // three blocks per SM when it fits
+  // stage budget: three blocks per SM at head_dim 256, four at 128 (whose
+  // accumulators fit in the 128 registers that leaves a thread)
+  static constexpr int NS_FIT = ((D == 128 ? 52 : 70) * 1024) / SP::STAGE;
   static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 4 ? 4 : NS_FIT);
   // epilogue buffers (reuse the stages): warp partials [warp][head 8][DP], block
   // partial [8][D].  Row pitch DP and dim placement make the warps' fragment
@@ -422,7 +424,7 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
 }
 
 template <int D, bool KI8, bool VI8, int NG>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 3)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, int layer_page0) {
   using LY = Layout<D, KI8, VI8>;
