@@ -1,0 +1,628 @@
+// Causal attention of a chunk of new queries over the int8 cache (prefill
+// chunk) on the 5th-generation tensor cores: tcgen05.mma with operands in
+// shared memory and tensor memory, accumulators in tensor memory.
+//
+// Method: Strata pull request #2698, "What it does" (the prompt chunk reads the
+// int8 K/V cache dequantizing on the fly) and genie-ai-runtime v1.3.1 (a fused
+// query-tiled attention kernel for chunks).  Query i of the chunk sits at
+// absolute position start + i and sees keys 0 .. start + i; the chunk's own
+// K/V are appended (quantized) before this runs.
+//
+// Work split.  A block takes 128 query rows of one kv head -- (position, head)
+// pairs, 128 / G positions x the G heads sharing the kv head -- and a balanced
+// range of its keys (split-K; the combine kernel reduces the partials).  Row R
+// is thread R and tensor-memory lane R.
+//
+// Per page of 64 keys:
+//   1. TMA brings the K/V rows and scales (a two-stage ring).  int8 rows are
+//      converted once to fp16 tiles in shared memory (exact: |code| <= 127),
+//      laid out as 128-byte-swizzled K-major boxes [D/64][64 keys][128 B].
+//   2. Thread 0 issues S_g = Q_g K_g^T per 64-value K scale group g
+//      (M = 128 rows, N = 64 keys, K = 16 per instruction) into tensor memory.
+//   3. Two threads per row (warps w and w + 4 share tensor-memory lanes) each
+//      read half of the row's S_g (32 keys), form s = scale * sum_g s_k * S_g,
+//      mask, and run the online softmax (lazy reference max, base 2; the two
+//      halves' maxima meet in shared memory).  They write P' = p * s_v *
+//      2^(6 - e_g) per V scale group as an fp16 hi + lo pair back into tensor
+//      memory, over the S columns they have consumed.
+//   4. Thread 0 issues O += P'_hi V + P'_lo V with P' from tensor memory and V
+//      from shared memory (MN-major: dims contiguous), N = 64 dims per
+//      instruction.  O (128 rows x D fp32) lives in tensor memory throughout;
+//      the rare rescales (reference max or V range moved) read and rewrite a
+//      thread's own row.
+// Completion of each MMA batch is signalled by tcgen05.commit on an mbarrier;
+// every wait is bounded and sets a device error bit on expiry.
+
+#include <climits>
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "decode_common.cuh"
+#include "mma_common.cuh"
+#include "ptx.cuh"
+
+namespace int8kv {
+namespace {
+
+using mma::kBoxBytes;
+using mma::kMaxPolls;
+using mma::kPage;
+using mma::pow2f;
+using mma::exponent_of;
+
+constexpr int kRows = 128;            // query rows per block = tensor-memory lanes
+constexpr int kThreads = 2 * kRows;   // two threads per row: keys and output columns halved
+constexpr int kNS = 2;                // stages of the page ring
+constexpr float kTau = 8.f;           // lazy rescale threshold (log2 units)
+constexpr int kPShift = 6;            // P' < 2^8 * 2^6 in fp16
+
+template <int D, bool KI8, bool VI8, int NG>
+struct TLayout {
+  using SP = mma::StagedPage<D, KI8, VI8>;
+  static constexpr int NGK = KI8 ? NG : 1;                  // K scale groups
+  static constexpr int NGV = VI8 ? NG : 1;                  // V scale groups
+  static constexpr int QBOX = kRows * 128;                  // one 64-dim box of the Q tile
+  static constexpr int Q_OFF = 0;                           // fp16 [D/64][128 rows][128 B]
+  static constexpr int ST_OFF = Q_OFF + kRows * D * 2;      // page ring
+  static constexpr int KH_OFF = ST_OFF + kNS * SP::STAGE;   // converted K page (int8 K only)
+  static constexpr int VH_OFF = KH_OFF + (KI8 ? kPage * D * 2 : 0);   // converted V page
+  static constexpr int SC_OFF = VH_OFF + (VI8 ? kPage * D * 2 : 0);   // scales [K|V][g][64 keys]
+  static constexpr int BAR_OFF = SC_OFF + 2 * 4 * kPage * 2;
+  static constexpr int SMEM = 1024 + BAR_OFF + 128;
+  // tensor memory: S_g / P'_g region, then O
+  static constexpr int SREG = (NGK > NGV ? NGK : NGV) * 64;
+  static constexpr int OB = SREG;
+  static constexpr int TCOLS = SREG + D <= 256 ? 256 : 512;
+  static_assert(SREG + D <= 512, "tensor memory holds S and O");
+};
+
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int b_mn) {
+  // kind::f16: D f32 (bits 4-5 = 1), A and B f16, A K-major, B K- or MN-major,
+  // N >> 3 at bit 17, M >> 4 at bit 24
+  return (1u << 4) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, rows of 128 B in groups of
+// 8 (stride 1024 B), start and offsets in 16-byte units.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, bool acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.u32 p, %4, 0; "
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
+      "l"(a), "l"(b), "r"(id), "r"((uint32_t)acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                       bool acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.u32 p, %4, 0; "
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(id), "r"((uint32_t)acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          ptx::smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t ta, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(ta));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t ta, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(ta),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Multiply this lane's columns [c0, c0 + n) of tensor memory by f.
+__device__ __forceinline__ void tmem_scale(uint32_t ta, int n, float f) {
+  for (int c = 0; c < n; c += 16) {
+    uint32_t v[16];
+    tmem_ld16(ta + c, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
+    tmem_st16(ta + c, v);
+  }
+  tmem_wait_st();
+}
+
+__device__ __forceinline__ int swz(int row, int c) { return row * 128 + ((c ^ (row & 7)) << 4); }
+
+// 16 int8 codes -> 16 exact fp16 values in natural order.
+__device__ __forceinline__ void codes_to_f16(const uint4 w, uint4& lo, uint4& hi) {
+  const uint32_t in[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u,
+                          w.w ^ 0x80808080u};
+  uint32_t o[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    o[2 * k] = mma::sub1152(ptx::prmt(in[k], 0x64646464u, 0x4140));
+    o[2 * k + 1] = mma::sub1152(ptx::prmt(in[k], 0x64646464u, 0x4342));
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// int8 rows of one side (K or V) of a staged page -> fp16 boxes [D/64][64][128 B].
+// Eight consecutive threads take one code chunk of eight consecutive rows, so
+// loads and stores hit eight different swizzled positions.
+template <int D>
+__device__ __forceinline__ void convert_side(const unsigned char* src, unsigned char* dst) {
+  constexpr int CPR = D / 16;   // 16-byte code chunks per row
+  for (int c = threadIdx.x; c < kPage * CPR; c += kThreads) {
+    const int g8 = c >> 3;
+    const int row = (g8 / CPR) * 8 + (c & 7), cc = g8 % CPR;
+    const uint4 w = *reinterpret_cast<const uint4*>(src + (cc >> 3) * kBoxBytes + swz(row, cc & 7));
+    uint4 lo, hi;
+    codes_to_f16(w, lo, hi);
+    unsigned char* box = dst + (cc >> 2) * kBoxBytes;
+    const int c16 = (cc & 3) * 2;
+    *reinterpret_cast<uint4*>(box + swz(row, c16)) = lo;
+    *reinterpret_cast<uint4*>(box + swz(row, c16 + 1)) = hi;
+  }
+}
+
+// Zero the fp16 rows of a staged side whose keys fall outside [j0, j1) (they
+// may hold any bits, and 0 * NaN would reach O).
+template <int D>
+__device__ __forceinline__ void zero_rows(unsigned char* side, int key0, int j0, int j1) {
+  for (int c = threadIdx.x; c < kPage * (D / 8); c += kThreads) {
+    const int row = c / (D / 8), ch = c % (D / 8);
+    const int key = key0 + row;
+    if (key < j0 || key >= j1)
+      *reinterpret_cast<uint4*>(side + (ch >> 3) * kBoxBytes + row * 128 + ((ch & 7) << 4)) =
+          make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <int D, bool KI8, bool VI8, int NG>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, int layer_page0) {
+  using LY = TLayout<D, KI8, VI8, NG>;
+  using SP = typename LY::SP;
+  constexpr int NGK = LY::NGK, NGV = LY::NGV;
+  constexpr int KSG = D / 16 / NGK;        // 16-dim k-steps per K group
+  constexpr int BPG = D / 64 / NGV;        // 64-dim boxes per V group
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);   // [kNS]
+  uint64_t* mS = full + kNS;                                           // S batch done
+  uint64_t* mO = mS + 1;                                               // P.V batch done
+  int* stage_page = reinterpret_cast<int*>(mO + 1);                    // [kNS]
+  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(stage_page + kNS);
+  __shared__ int s_fail;
+
+  const int qt = blockIdx.x, kvh = blockIdx.y, split = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int R = tid & (kRows - 1), half = tid / kRows;   // row, and which half of it
+  const PoolView& p = a.pool;
+  const int G = a.G, ppb = kRows / G, pos0 = qt * ppb;
+
+  if (tid == 0) {
+    for (int s = 0; s < kNS; ++s) ptx::mbar_init(&full[s], 1);
+    ptx::mbar_init(mS, 1);
+    ptx::mbar_init(mO, 1);
+    ptx::fence_mbar_init();
+    s_fail = 0;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     ptx::smem_u32(taddr_s)),
+                 "r"((uint32_t)LY::TCOLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+
+  const int last_pos = min(pos0 + ppb, a.n_new) - 1;
+  const int hi_key = a.start + last_pos + 1;   // keys [0, hi_key) for this block
+  int j0, j1;
+  split_range(0, hi_key, split, a.n_splits, kPage, &j0, &j1);
+  const int p_first = j0 / kPage;
+  const int n_pg = j1 > j0 ? (j1 - 1) / kPage - p_first + 1 : 0;
+
+  // q rows -> shared memory (rows past the chunk are zero)
+  for (int c = tid; c < kRows * (D / 8); c += kThreads) {
+    const int row = c / (D / 8), ch = c - row * (D / 8);
+    const int pos = pos0 + row / G;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (pos < a.n_new)
+      v = ptx::ldg128(a.q + ((size_t)pos * a.H + (size_t)kvh * G + row % G) * D + ch * 8);
+    *reinterpret_cast<uint4*>(smem + LY::Q_OFF + (ch >> 3) * LY::QBOX + swz(row, ch & 7)) = v;
+  }
+  ptx::fence_proxy_async();   // generic writes of the Q tile before the tensor-core reads
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *taddr_s;
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;   // this warp's tensor-memory lanes
+
+  const int32_t* ptrow = a.page_table;
+  auto page_row = [&](int page) { return ((layer_page0 + page) * p.Hkv + kvh) * kPage; };
+  auto issue = [&](int i) {
+    const int st = i % kNS;
+    const int page = lookup_page(ptrow, p_first + i, a.max_pages, p);
+    mma::issue_page<D, KI8, VI8>(smem + LY::ST_OFF + st * SP::STAGE, &full[st], &stage_page[st],
+                                 page, page_row(page), p, kvh, &tmk, &tmv);
+  };
+  if (tid == 0) {
+    ptx::prefetch_tensormap(&tmk);
+    ptx::prefetch_tensormap(&tmv);
+    for (int i = 0; i < n_pg && i < kNS; ++i) issue(i);
+  }
+
+  const int pos = pos0 + R / G;
+  const int lim = pos < a.n_new ? a.start + pos : -1;   // last key this row sees
+  float m = -INFINITY, l = 0.f;
+  int vexp[NGV];
+  float cap[NGV], sh[NGV];
+#pragma unroll
+  for (int g = 0; g < NGV; ++g) {
+    vexp[g] = INT_MIN;
+    cap[g] = 0.f;
+    sh[g] = 0.f;
+  }
+  const uint16_t* sck = reinterpret_cast<const uint16_t*>(smem + LY::SC_OFF);
+  const uint16_t* scv = sck + 4 * kPage;
+  constexpr uint32_t idS = idesc_f16(128, 64, 0), idO = idesc_f16(128, 64, 1);
+  bool o_live = false;   // some P.V batch has written O
+  int nS = 0, nO = 0;    // S and P.V batches committed so far (one mbarrier phase each)
+  __shared__ float s_vmax[4];
+  __shared__ float s_mx[2][kRows];   // the two halves' score maxima of each row
+
+  for (int i = 0; i < n_pg; ++i) {
+    const int st = i % kNS;
+    // the previous P.V batch is done: its V tile, P' columns and stage are free
+    bool bad = false;
+    if (nO > 0) bad = !ptx::mbar_wait(mO, (nO - 1) & 1, kMaxPolls);
+    bad |= !ptx::mbar_wait(&full[st], (i / kNS) & 1, kMaxPolls);
+    if (__syncthreads_or(bad)) {
+      if (tid == 0) s_fail = 1;
+      break;
+    }
+    tc_fence_after();
+    if (tid == 0 && i > 0 && i - 1 + kNS < n_pg) issue(i - 1 + kNS);   // refill the freed stage
+    unsigned char* sb = smem + LY::ST_OFF + st * SP::STAGE;
+    const int page = stage_page[st];
+    const int key0 = (p_first + i) * kPage;
+    const bool edge = key0 < j0 || key0 + kPage > j1;
+    if (page >= 0) {
+      if constexpr (KI8) convert_side<D>(sb + SP::K_OFF, smem + LY::KH_OFF);
+      if constexpr (VI8) convert_side<D>(sb + SP::V_OFF, smem + LY::VH_OFF);
+      if constexpr (!KI8) if (edge) zero_rows<D>(sb + SP::K_OFF, key0, j0, j1);
+      if constexpr (!VI8) if (edge) zero_rows<D>(sb + SP::V_OFF, key0, j0, j1);
+      uint16_t* sc = reinterpret_cast<uint16_t*>(smem + LY::SC_OFF);
+      for (int e = tid; e < kPage * NG; e += kThreads) {
+        const int row = e / NG, g = e - row * NG;
+        if (KI8) sc[g * kPage + row] = reinterpret_cast<const uint16_t*>(sb + SP::KS_OFF)[e];
+        if (VI8) sc[4 * kPage + g * kPage + row] = reinterpret_cast<const uint16_t*>(sb + SP::VS_OFF)[e];
+      }
+      if constexpr (VI8) {
+        __syncthreads();
+        if (tid < NGV) {   // the largest V scale of group tid among the keys in [j0, j1)
+          float mv = 0.f;
+          for (int k = 0; k < kPage; ++k) {
+            const int key = key0 + k;
+            if (key >= j0 && key < j1) mv = fmaxf(mv, __half2float(__ushort_as_half(scv[tid * kPage + k])));
+          }
+          s_vmax[tid] = mv;
+        }
+      }
+    }
+    ptx::fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (page < 0) continue;   // flagged by the lookup; every thread skips alike
+    tc_fence_after();
+
+    // ---- S_g = Q_g K_g^T into columns [64g, 64g + 64)
+    if (tid == 0) {
+      const uint32_t kt = ptx::smem_u32(KI8 ? smem + LY::KH_OFF : sb + SP::K_OFF);
+      const uint32_t qt0 = ptx::smem_u32(smem + LY::Q_OFF);
+#pragma unroll
+      for (int g = 0; g < NGK; ++g)
+#pragma unroll
+        for (int kk = 0; kk < KSG; ++kk) {
+          const int ks = g * KSG + kk;   // 16-dim k-step: box ks/4, 32-byte step ks%4
+          const uint64_t da = sdesc(qt0 + (ks >> 2) * LY::QBOX + (ks & 3) * 32, 16, 1024);
+          const uint64_t db = sdesc(kt + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024);
+          mma_ss(tbase + g * 64, da, db, idS, kk > 0);
+        }
+      mma_commit(mS);
+    }
+    const bool okS = ptx::mbar_wait(mS, nS & 1, kMaxPolls);
+    ++nS;
+    tc_fence_after();
+
+    // ---- this half-row: scores, softmax, P' per V group (chunks c = 2 half, 2 half + 1)
+    const bool full_page = !edge && key0 + kPage - 1 <= lim;
+    const bool skip = !okS;
+    // all 32 scores first (the reference max must be settled before any P')
+    float sv[2][16];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = 2 * half + cc;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) sv[cc][k] = 0.f;
+#pragma unroll
+      for (int g = 0; g < NGK; ++g) {
+        uint32_t v[16];
+        tmem_ld16(tbase + lane_off + g * 64 + c * 16, v);
+        float f[16];
+        if constexpr (KI8) {
+#pragma unroll
+          for (int k8 = 0; k8 < 2; ++k8) {   // 8 fp16 K scales per 16-byte load
+            const uint4 w = *reinterpret_cast<const uint4*>(sck + g * kPage + c * 16 + 8 * k8);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&ww[q]));
+              f[8 * k8 + 2 * q] = h.x * a.scale_log2;
+              f[8 * k8 + 2 * q + 1] = h.y * a.scale_log2;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) f[k] = a.scale_log2;
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) sv[cc][k] = fmaf(__uint_as_float(v[k]), f[k], sv[cc][k]);
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int key = key0 + c * 16 + k;
+        if (!full_page && !(key >= j0 && key < j1 && key <= lim)) sv[cc][k] = -INFINITY;
+        mx = fmaxf(mx, sv[cc][k]);
+      }
+    }
+    s_mx[half][R] = mx;
+    __syncthreads();
+    mx = fmaxf(s_mx[0][R], s_mx[1][R]);   // both halves take the same steps
+    // move the reference max when exceeded by more than 2^kTau: O and l scale by
+    // 2^(m_old - m_new); tensor-memory accesses are warp-wide, so the warp goes
+    // together and unaffected rows scale by 1
+    const bool need = !skip && mx > m + kTau;
+    float al = 1.f;
+    if (need) {
+      const float mn = fmaxf(m, mx);
+      al = m == -INFINITY ? 1.f : ptx::ex2(m - mn);
+      l *= al;
+      m = mn;
+    }
+    if (__any_sync(0xffffffffu, need && o_live && al != 1.f))
+      tmem_scale(tbase + lane_off + LY::OB + half * (D / 2), D / 2, al);
+    const float base = m == -INFINITY ? 0.f : m;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        sv[cc][k] = ptx::ex2(sv[cc][k] - base);   // now p
+        l += sv[cc][k];                           // this half's share of the row sum
+      }
+    // V range per group: 2^e_g bounds every V scale of the group seen so far
+    // (the same for every row: block-uniform branches)
+#pragma unroll
+    for (int g = 0; g < NGV; ++g) {
+      if constexpr (VI8) {
+        const float mv = s_vmax[g];
+        if (mv > 0.f && mv >= cap[g]) {
+          const int ne = exponent_of(mv) + 1;
+          // the group's columns that lie in this thread's half of O
+          const int c_lo = max(g * (D / NGV), half * (D / 2));
+          const int c_hi = min((g + 1) * (D / NGV), (half + 1) * (D / 2));
+          if (vexp[g] != INT_MIN && o_live && c_hi > c_lo)
+            tmem_scale(tbase + lane_off + LY::OB + c_lo, c_hi - c_lo, pow2f(vexp[g] - ne));
+          vexp[g] = ne;
+          cap[g] = pow2f(ne);
+          sh[g] = pow2f(kPShift - ne);
+        }
+      } else {
+        sh[g] = pow2f(kPShift);
+      }
+    }
+    // P'_g hi | lo for chunk c over the S columns of chunk c (already read)
+#pragma unroll
+    for (int g = 0; g < NGV; ++g)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * half + cc;
+        uint32_t v[16];
+        uint32_t vs[8];   // V scales of the chunk's 16 keys, fp16 pairs
+        if constexpr (VI8) {
+          const uint4 w0 = *reinterpret_cast<const uint4*>(scv + g * kPage + c * 16);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(scv + g * kPage + c * 16 + 8);
+          vs[0] = w0.x; vs[1] = w0.y; vs[2] = w0.z; vs[3] = w0.w;
+          vs[4] = w1.x; vs[5] = w1.y; vs[6] = w1.z; vs[7] = w1.w;
+        }
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2) {
+          float w0 = sv[cc][2 * k2] * sh[g], w1 = sv[cc][2 * k2 + 1] * sh[g];
+          if constexpr (VI8) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&vs[k2]));
+            w0 *= f.x;
+            w1 *= f.y;
+          }
+          const uint32_t h = ptx::pack_f16x2(w0, w1);
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+          v[k2] = h;
+          v[8 + k2] = ptx::pack_f16x2(w0 - f.x, w1 - f.y);
+        }
+        tmem_st16(tbase + lane_off + g * 64 + c * 16, v);
+      }
+    tmem_wait_st();
+    tc_fence_before();
+    if (__syncthreads_or(skip)) {
+      if (tid == 0) s_fail = 1;
+      break;
+    }
+    tc_fence_after();
+
+    // ---- O[:, box b] += P'_hi V_b + P'_lo V_b, chunk by chunk (16 keys each)
+    if (tid == 0) {
+      const uint32_t vt = ptx::smem_u32(VI8 ? smem + LY::VH_OFF : sb + SP::V_OFF);
+#pragma unroll
+      for (int b = 0; b < D / 64; ++b) {
+        const int g = b / BPG;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint64_t dv = sdesc(vt + b * kBoxBytes + c * 2048, 1024, 1024);
+          const uint32_t pa = tbase + g * 64 + c * 16;
+          mma_ts(tbase + LY::OB + b * 64, pa, dv, idO, o_live || c > 0);
+          mma_ts(tbase + LY::OB + b * 64, pa + 8, dv, idO, true);
+        }
+      }
+      mma_commit(mO);
+    }
+    ++nO;
+    o_live = true;
+  }
+
+  // ---- epilogue: the last P.V batch, then this row's O
+  bool fail = s_fail != 0;
+  if (!fail && nO > 0) fail = !ptx::mbar_wait(mO, (nO - 1) & 1, kMaxPolls);
+  tc_fence_after();
+  if (fail && tid == 0) flag_error(p.err, INT8KV_DEVERR_TIMEOUT);
+  s_mx[half][R] = l;   // the row sum is the two halves' sums
+  __syncthreads();
+  l = s_mx[0][R] + s_mx[1][R];
+  const bool wr = pos < a.n_new;
+  const size_t h = (size_t)pos * a.H + (size_t)kvh * G + R % G;
+  const int S = a.n_splits;
+#pragma unroll 1
+  for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 16) {
+    uint32_t v[16];
+    tmem_ld16(tbase + lane_off + LY::OB + c, v);
+    tmem_wait_ld();
+    const int g = c / (D / NGV);
+    float u = pow2f(-kPShift);
+    if constexpr (VI8) u = vexp[g] == INT_MIN ? 0.f : pow2f(vexp[g] - kPShift);
+    if (!o_live) u = 0.f;
+    const float f = S == 1 ? (l > 0.f ? u / l : 0.f) : u;
+    float* dst = S == 1 ? a.out + h * D + c : a.ws.part_o + (h * S + split) * D + c;
+    if (wr) {   // no P.V batch at all: O was never written, the row is 0
+#pragma unroll
+      for (int k = 0; k < 16; k += 4)
+        *reinterpret_cast<float4*>(dst + k) =
+            o_live ? make_float4(__uint_as_float(v[k]) * f, __uint_as_float(v[k + 1]) * f,
+                                 __uint_as_float(v[k + 2]) * f, __uint_as_float(v[k + 3]) * f)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  if (S > 1 && wr && half == 0) a.ws.part_ml[h * S + split] = make_float2(m, l);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),
+                 "r"((uint32_t)LY::TCOLS)
+                 : "memory");
+  }
+}
+
+template <int D, bool KI8, bool VI8, int NG>
+cudaError_t launch_typed(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                         int layer_page0, cudaStream_t stream) {
+  using LY = TLayout<D, KI8, VI8, NG>;
+  auto kern = prefill_tc_kernel<D, KI8, VI8, NG>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured[dev] = true;
+  }
+  const int ppb = kRows / a.G;
+  const dim3 grid((a.n_new + ppb - 1) / ppb, a.pool.Hkv, a.n_splits);
+  kern<<<grid, kThreads, LY::SMEM, stream>>>(a, tmk, tmv, layer_page0);
+  return cudaGetLastError();
+}
+
+template <int D, bool KI8, bool VI8>
+cudaError_t launch_ng(const PrefillArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                      int layer_page0, cudaStream_t stream) {
+  switch (a.pool.ng) {
+    case 1: return launch_typed<D, KI8, VI8, 1>(a, tmk, tmv, layer_page0, stream);
+    case 2: return launch_typed<D, KI8, VI8, 2>(a, tmk, tmv, layer_page0, stream);
+    case 4:
+      if constexpr (D == 256) return launch_typed<D, KI8, VI8, 4>(a, tmk, tmv, layer_page0, stream);
+      return cudaErrorNotSupported;
+    default: return cudaErrorNotSupported;
+  }
+}
+
+}  // namespace
+
+static cudaError_t launch_prefill_tc(const int8kv_pool* pool, int layer, const PrefillArgs& a,
+                                     cudaStream_t stream) {
+  const int lp0 = layer * pool->n_pages;
+  const bool k8 = pool->k_int8, v8 = pool->v_int8;
+  if (pool->head_dim == 256) {
+    if (k8 && v8) return launch_ng<256, true, true>(a, pool->tmap_k, pool->tmap_v, lp0, stream);
+    if (k8) return launch_ng<256, true, false>(a, pool->tmap_k, pool->tmap_v, lp0, stream);
+    return launch_ng<256, false, true>(a, pool->tmap_k, pool->tmap_v, lp0, stream);
+  }
+  if (k8 && v8) return launch_ng<128, true, true>(a, pool->tmap_k, pool->tmap_v, lp0, stream);
+  if (k8) return launch_ng<128, true, false>(a, pool->tmap_k, pool->tmap_v, lp0, stream);
+  return launch_ng<128, false, true>(a, pool->tmap_k, pool->tmap_v, lp0, stream);
+}
+
+bool prefill_supported(const int8kv_pool* pool, int G) {
+  return pool->has_tmaps && pool->page_size == kPage && pool->group_size >= 64 &&
+         (pool->head_dim == 128 || pool->head_dim == 256) && (G == 1 || G == 2 || G == 4 || G == 8);
+}
+
+cudaError_t launch_prefill(const int8kv_pool* pool, int layer, const PrefillArgs& a,
+                           cudaStream_t stream) {
+  const cudaError_t e = launch_prefill_tc(pool, layer, a, stream);
+  if (e != cudaSuccess || a.n_splits == 1) return e;
+  DecodeArgs c{};
+  c.pool = a.pool;
+  c.out = a.out;
+  c.ws = a.ws;
+  c.B = a.n_new;
+  c.H = a.H;
+  c.G = a.G;
+  c.n_splits = a.n_splits;
+  return launch_decode_combine(c, stream);
+}
+
+}  // namespace int8kv
