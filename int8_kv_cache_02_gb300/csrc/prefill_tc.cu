@@ -19,12 +19,12 @@
 //      laid out as 128-byte-swizzled K-major boxes [D/64][64 keys][128 B].
 //   2. Thread 0 issues S_g = Q_g K_g^T per 64-value K scale group g
 //      (M = 128 rows, N = 64 keys, K = 16 per instruction) into tensor memory.
-//   3. Two threads per row (warps w and w + 4 share tensor-memory lanes) each
-//      read half of the row's S_g (32 keys), form s = scale * sum_g s_k * S_g,
-//      mask, and run the online softmax (lazy reference max, base 2; the two
-//      halves' maxima meet in shared memory).  They write P' = p * s_v *
-//      2^(6 - e_g) per V scale group as an fp16 hi + lo pair back into tensor
-//      memory, over the S columns they have consumed.
+//   3. Four threads per row (warps w, w + 4, w + 8, w + 12 share tensor-memory
+//      lanes) each read a quarter of the row's S_g (16 keys), form
+//      s = scale * sum_g s_k * S_g, mask, and run the online softmax (lazy
+//      reference max, base 2; the quarters' maxima meet in shared memory).
+//      They write P' = p * s_v * 2^(6 - e_g) per V scale group as an fp16
+//      hi + lo pair back into tensor memory, over the S columns they have read.
 //   4. Thread 0 issues O += P'_hi V + P'_lo V with P' from tensor memory and V
 //      from shared memory (MN-major: dims contiguous), N = 64 dims per
 //      instruction.  O (128 rows x D fp32) lives in tensor memory throughout;
@@ -53,7 +53,9 @@ using mma::pow2f;
 using mma::exponent_of;
 
 constexpr int kRows = 128;            // query rows per block = tensor-memory lanes
-constexpr int kThreads = 2 * kRows;   // two threads per row: keys and output columns halved
+constexpr int kParts = 4;             // threads per row: each takes 16 of the 64 keys of a page
+constexpr int kThreads = kParts * kRows;   // and D / kParts of the output columns
+constexpr int kChunks = 4 / kParts;   // 16-key chunks per thread
 constexpr int kNS = 2;                // stages of the page ring
 constexpr float kTau = 8.f;           // lazy rescale threshold (log2 units)
 constexpr int kPShift = 6;            // P' < 2^8 * 2^6 in fp16
@@ -68,8 +70,9 @@ struct TLayout {
   static constexpr int ST_OFF = Q_OFF + kRows * D * 2;      // page ring
   static constexpr int KH_OFF = ST_OFF + kNS * SP::STAGE;   // converted K page (int8 K only)
   static constexpr int VH_OFF = KH_OFF + (KI8 ? kPage * D * 2 : 0);   // converted V page
-  static constexpr int SC_OFF = VH_OFF + (VI8 ? kPage * D * 2 : 0);   // scales [K|V][g][64 keys]
-  static constexpr int BAR_OFF = SC_OFF + 2 * 4 * kPage * 2;
+  static constexpr int KSF_OFF = VH_OFF + (VI8 ? kPage * D * 2 : 0);   // fp32 K scales x scale [key][NG]
+  static constexpr int VSF_OFF = KSF_OFF + kPage * 4 * 4;               // fp32 V scales [key][NG]
+  static constexpr int BAR_OFF = VSF_OFF + kPage * 4 * 4;
   static constexpr int SMEM = 1024 + BAR_OFF + 128;
   // tensor memory: S_g / P'_g region, then O
   static constexpr int SREG = (NGK > NGV ? NGK : NGV) * 64;
@@ -183,6 +186,7 @@ __device__ __forceinline__ void codes_to_f16(const uint4 w, uint4& lo, uint4& hi
 template <int D>
 __device__ __forceinline__ void convert_side(const unsigned char* src, unsigned char* dst) {
   constexpr int CPR = D / 16;   // 16-byte code chunks per row
+#pragma unroll 4
   for (int c = threadIdx.x; c < kPage * CPR; c += kThreads) {
     const int g8 = c >> 3;
     const int row = (g8 / CPR) * 8 + (c & 7), cc = g8 % CPR;
@@ -229,7 +233,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
 
   const int qt = blockIdx.x, kvh = blockIdx.y, split = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int R = tid & (kRows - 1), half = tid / kRows;   // row, and which half of it
+  const int R = tid & (kRows - 1), half = tid / kRows;   // row, and which part of it
   const PoolView& p = a.pool;
   const int G = a.G, ppb = kRows / G, pos0 = qt * ppb;
 
@@ -296,13 +300,11 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
     cap[g] = 0.f;
     sh[g] = 0.f;
   }
-  const uint16_t* sck = reinterpret_cast<const uint16_t*>(smem + LY::SC_OFF);
-  const uint16_t* scv = sck + 4 * kPage;
   constexpr uint32_t idS = idesc_f16(128, 64, 0), idO = idesc_f16(128, 64, 1);
   bool o_live = false;   // some P.V batch has written O
   int nS = 0, nO = 0;    // S and P.V batches committed so far (one mbarrier phase each)
   __shared__ float s_vmax[4];
-  __shared__ float s_mx[2][kRows];   // the two halves' score maxima of each row
+  __shared__ float s_mx[kParts][kRows];   // the parts' score maxima (then sums) of each row
 
   for (int i = 0; i < n_pg; ++i) {
     const int st = i % kNS;
@@ -325,21 +327,31 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
       if constexpr (VI8) convert_side<D>(sb + SP::V_OFF, smem + LY::VH_OFF);
       if constexpr (!KI8) if (edge) zero_rows<D>(sb + SP::K_OFF, key0, j0, j1);
       if constexpr (!VI8) if (edge) zero_rows<D>(sb + SP::V_OFF, key0, j0, j1);
-      uint16_t* sc = reinterpret_cast<uint16_t*>(smem + LY::SC_OFF);
-      for (int e = tid; e < kPage * NG; e += kThreads) {
-        const int row = e / NG, g = e - row * NG;
-        if (KI8) sc[g * kPage + row] = reinterpret_cast<const uint16_t*>(sb + SP::KS_OFF)[e];
-        if (VI8) sc[4 * kPage + g * kPage + row] = reinterpret_cast<const uint16_t*>(sb + SP::VS_OFF)[e];
+      // the page's scales as fp32 tables (K scales times the softmax scale)
+      if (tid < kPage * NG) {
+        if constexpr (KI8)
+          reinterpret_cast<float*>(smem + LY::KSF_OFF)[tid] =
+              __half2float(reinterpret_cast<const __half*>(sb + SP::KS_OFF)[tid]) * a.scale_log2;
+        if constexpr (VI8)
+          reinterpret_cast<float*>(smem + LY::VSF_OFF)[tid] =
+              __half2float(reinterpret_cast<const __half*>(sb + SP::VS_OFF)[tid]);
       }
       if constexpr (VI8) {
-        __syncthreads();
-        if (tid < NGV) {   // the largest V scale of group tid among the keys in [j0, j1)
-          float mv = 0.f;
-          for (int k = 0; k < kPage; ++k) {
-            const int key = key0 + k;
-            if (key >= j0 && key < j1) mv = fmaxf(mv, __half2float(__ushort_as_half(scv[tid * kPage + k])));
+        if (warp == 0) {   // the largest V scale of each group among the keys in [j0, j1)
+          const uint16_t* vs = reinterpret_cast<const uint16_t*>(sb + SP::VS_OFF);
+          const int lane = tid & 31;
+#pragma unroll
+          for (int g = 0; g < NGV; ++g) {
+            float mv = 0.f;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {   // keys 2 lane, 2 lane + 1
+              const int k = 2 * lane + e;
+              if (key0 + k >= j0 && key0 + k < j1)
+                mv = fmaxf(mv, __half2float(__ushort_as_half(vs[k * NG + g])));
+            }
+            mv = warp_max(mv);
+            if (lane == 0) s_vmax[g] = mv;
           }
-          s_vmax[tid] = mv;
         }
       }
     }
@@ -364,45 +376,70 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
         }
       mma_commit(mS);
     }
+    // V range per group: 2^e_g bounds every V scale of the group seen so far
+    // (the same for every row: block-uniform branches).  O is stable here (the
+    // last P.V batch is done; the S batch in flight writes other columns).
+#pragma unroll
+    for (int g = 0; g < NGV; ++g) {
+      if constexpr (VI8) {
+        const float mv = s_vmax[g];
+        if (mv > 0.f && mv >= cap[g]) {
+          const int ne = exponent_of(mv) + 1;
+          // the group's columns that lie in this thread's part of O
+          const int c_lo = max(g * (D / NGV), half * (D / kParts));
+          const int c_hi = min((g + 1) * (D / NGV), (half + 1) * (D / kParts));
+          if (vexp[g] != INT_MIN && o_live && c_hi > c_lo)
+            tmem_scale(tbase + lane_off + LY::OB + c_lo, c_hi - c_lo, pow2f(vexp[g] - ne));
+          vexp[g] = ne;
+          cap[g] = pow2f(ne);
+          sh[g] = pow2f(kPShift - ne);
+        }
+      } else {
+        sh[g] = pow2f(kPShift);
+      }
+    }
+    // the V-scale table takes the range shift: P' = p * table[key][g]
+    if constexpr (VI8)
+      if (tid < kPage * NG) reinterpret_cast<float*>(smem + LY::VSF_OFF)[tid] *= sh[tid % NG];
     const bool okS = ptx::mbar_wait(mS, nS & 1, kMaxPolls);
     ++nS;
     tc_fence_after();
 
-    // ---- this half-row: scores, softmax, P' per V group (chunks c = 2 half, 2 half + 1)
+    // ---- this part of the row: scores, softmax, P' per V group (chunks
+    // c = kChunks * half ..)
     const bool full_page = !edge && key0 + kPage - 1 <= lim;
     const bool skip = !okS;
-    // all 32 scores first (the reference max must be settled before any P')
-    float sv[2][16];
+    // all of the part's scores first (the reference max must be settled before any P')
+    float sv[kChunks][16];
     float mx = -INFINITY;
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int c = 2 * half + cc;
+    for (int cc = 0; cc < kChunks; ++cc) {
+      const int c = kChunks * half + cc;
+      uint32_t v[NGK][16];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) sv[cc][k] = 0.f;
+      for (int g = 0; g < NGK; ++g) tmem_ld16(tbase + lane_off + g * 64 + c * 16, v[g]);
+      tmem_wait_ld();
+      const float* ksf = reinterpret_cast<const float*>(smem + LY::KSF_OFF);
 #pragma unroll
-      for (int g = 0; g < NGK; ++g) {
-        uint32_t v[16];
-        tmem_ld16(tbase + lane_off + g * 64 + c * 16, v);
-        float f[16];
+      for (int k = 0; k < 16; ++k) {
+        float acc = 0.f;
         if constexpr (KI8) {
-#pragma unroll
-          for (int k8 = 0; k8 < 2; ++k8) {   // 8 fp16 K scales per 16-byte load
-            const uint4 w = *reinterpret_cast<const uint4*>(sck + g * kPage + c * 16 + 8 * k8);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&ww[q]));
-              f[8 * k8 + 2 * q] = h.x * a.scale_log2;
-              f[8 * k8 + 2 * q + 1] = h.y * a.scale_log2;
-            }
+          float f[NG];
+          if constexpr (NG == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(ksf + (c * 16 + k) * 4);
+            f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+          } else if constexpr (NG == 2) {
+            const float2 x = *reinterpret_cast<const float2*>(ksf + (c * 16 + k) * 2);
+            f[0] = x.x; f[1] = x.y;
+          } else {
+            f[0] = ksf[c * 16 + k];
           }
+#pragma unroll
+          for (int g = 0; g < NG; ++g) acc = fmaf(__uint_as_float(v[g][k]), f[g], acc);
         } else {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) f[k] = a.scale_log2;
+          acc = __uint_as_float(v[0][k]) * a.scale_log2;
         }
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 16; ++k) sv[cc][k] = fmaf(__uint_as_float(v[k]), f[k], sv[cc][k]);
+        sv[cc][k] = acc;
       }
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
@@ -413,7 +450,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
     }
     s_mx[half][R] = mx;
     __syncthreads();
-    mx = fmaxf(s_mx[0][R], s_mx[1][R]);   // both halves take the same steps
+#pragma unroll
+    for (int q = 0; q < kParts; ++q) mx = fmaxf(mx, s_mx[q][R]);   // every part takes the same steps
     // move the reference max when exceeded by more than 2^kTau: O and l scale by
     // 2^(m_old - m_new); tensor-memory accesses are warp-wide, so the warp goes
     // together and unaffected rows scale by 1
@@ -426,57 +464,32 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
       m = mn;
     }
     if (__any_sync(0xffffffffu, need && o_live && al != 1.f))
-      tmem_scale(tbase + lane_off + LY::OB + half * (D / 2), D / 2, al);
+      tmem_scale(tbase + lane_off + LY::OB + half * (D / kParts), D / kParts, al);
     const float base = m == -INFINITY ? 0.f : m;
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc)
+    for (int cc = 0; cc < kChunks; ++cc)
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         sv[cc][k] = ptx::ex2(sv[cc][k] - base);   // now p
-        l += sv[cc][k];                           // this half's share of the row sum
+        l += sv[cc][k];                           // this part's share of the row sum
       }
-    // V range per group: 2^e_g bounds every V scale of the group seen so far
-    // (the same for every row: block-uniform branches)
-#pragma unroll
-    for (int g = 0; g < NGV; ++g) {
-      if constexpr (VI8) {
-        const float mv = s_vmax[g];
-        if (mv > 0.f && mv >= cap[g]) {
-          const int ne = exponent_of(mv) + 1;
-          // the group's columns that lie in this thread's half of O
-          const int c_lo = max(g * (D / NGV), half * (D / 2));
-          const int c_hi = min((g + 1) * (D / NGV), (half + 1) * (D / 2));
-          if (vexp[g] != INT_MIN && o_live && c_hi > c_lo)
-            tmem_scale(tbase + lane_off + LY::OB + c_lo, c_hi - c_lo, pow2f(vexp[g] - ne));
-          vexp[g] = ne;
-          cap[g] = pow2f(ne);
-          sh[g] = pow2f(kPShift - ne);
-        }
-      } else {
-        sh[g] = pow2f(kPShift);
-      }
-    }
     // P'_g hi | lo for chunk c over the S columns of chunk c (already read)
+    const float* vsf = reinterpret_cast<const float*>(smem + LY::VSF_OFF);
 #pragma unroll
     for (int g = 0; g < NGV; ++g)
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * half + cc;
+      for (int cc = 0; cc < kChunks; ++cc) {
+        const int c = kChunks * half + cc;
         uint32_t v[16];
-        uint32_t vs[8];   // V scales of the chunk's 16 keys, fp16 pairs
-        if constexpr (VI8) {
-          const uint4 w0 = *reinterpret_cast<const uint4*>(scv + g * kPage + c * 16);
-          const uint4 w1 = *reinterpret_cast<const uint4*>(scv + g * kPage + c * 16 + 8);
-          vs[0] = w0.x; vs[1] = w0.y; vs[2] = w0.z; vs[3] = w0.w;
-          vs[4] = w1.x; vs[5] = w1.y; vs[6] = w1.z; vs[7] = w1.w;
-        }
 #pragma unroll
         for (int k2 = 0; k2 < 8; ++k2) {
-          float w0 = sv[cc][2 * k2] * sh[g], w1 = sv[cc][2 * k2 + 1] * sh[g];
-          if constexpr (VI8) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&vs[k2]));
-            w0 *= f.x;
-            w1 *= f.y;
+          float w0, w1;
+          if constexpr (VI8) {   // table: V scale times the group's range shift
+            w0 = sv[cc][2 * k2] * vsf[(c * 16 + 2 * k2) * NG + g];
+            w1 = sv[cc][2 * k2 + 1] * vsf[(c * 16 + 2 * k2 + 1) * NG + g];
+          } else {
+            w0 = sv[cc][2 * k2] * sh[g];
+            w1 = sv[cc][2 * k2 + 1] * sh[g];
           }
           const uint32_t h = ptx::pack_f16x2(w0, w1);
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
@@ -518,14 +531,16 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
   if (!fail && nO > 0) fail = !ptx::mbar_wait(mO, (nO - 1) & 1, kMaxPolls);
   tc_fence_after();
   if (fail && tid == 0) flag_error(p.err, INT8KV_DEVERR_TIMEOUT);
-  s_mx[half][R] = l;   // the row sum is the two halves' sums
+  s_mx[half][R] = l;   // the row sum is the parts' sums
   __syncthreads();
-  l = s_mx[0][R] + s_mx[1][R];
+  l = 0.f;
+#pragma unroll
+  for (int q = 0; q < kParts; ++q) l += s_mx[q][R];
   const bool wr = pos < a.n_new;
   const size_t h = (size_t)pos * a.H + (size_t)kvh * G + R % G;
   const int S = a.n_splits;
 #pragma unroll 1
-  for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 16) {
+  for (int c = half * (D / kParts); c < (half + 1) * (D / kParts); c += 16) {
     uint32_t v[16];
     tmem_ld16(tbase + lane_off + LY::OB + c, v);
     tmem_wait_ld();
