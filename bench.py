@@ -40,7 +40,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("INT8-KV decode attn: achieved HBM GB/s (% of ~8 TB/s), μs/step at "
           "8K–128K ctx")
-WORKLOAD = ("decode step (append 1 token + split-K GQA decode + combine, one fused kernel): "
+WORKLOAD = ("decode step (1-token append fused into the split-K GQA decode kernel, then the combine kernel): "
             "batch 1, 16 q heads, "
             "2 kv heads, head_dim 256, fp16 scale per 64 values, ctx 8192, k8v8, outlier K "
             "channels")
@@ -424,7 +424,7 @@ def run_ours(args, rank, world, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": e2e_s / n_e2e * 1e6, "steps": n_e2e},
         "roofline": {"bound": "hbm", "kernel": "decode_mma_kernel (attn_decode_int8: split-K "
-                                               "partials + in-kernel combine)",
+                                               "partials; the combine kernel follows)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": traffic, "algorithmic_bytes": decode_bytes(),
