@@ -191,8 +191,11 @@ int attn_decode_append_int8(const int8kv_pool* pool, int layer, const uint16_t* 
                             int max_pages_per_seq, int window, float softmax_scale, int n_splits,
                             float* out, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Blocks of the prefill-chunk kernel per (128-row query tile, kv head): about one
- * block per SM in total, at least 1, at most the pages of the context.  Returns
+/* Blocks of the prefill-chunk kernel per (128-row query tile, kv head).  The
+ * kernel runs one block per SM at a time, so tiles x kv heads x splits blocks
+ * take ceil(blocks / SMs) waves of ceil(pages / splits) pages; the count with
+ * the shortest such chain (two pages of per-block overhead added per wave) is
+ * returned: at least 1, at most the pages of the context and 256.  Returns
  * >= 1, or NULL_PTR, INVALID_ARG, UNSUPPORTED. */
 int attn_prefill_n_splits(const int8kv_pool* pool, int n_new, int n_heads, int start_pos);
 

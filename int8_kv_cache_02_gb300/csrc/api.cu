@@ -343,15 +343,26 @@ int attn_prefill_n_splits(const int8kv_pool* pool, int n_new, int n_heads, int s
     return INT8KV_ERR_INVALID_ARG;
   const int G = n_heads / pool->n_kv_heads;
   if (G > 8) return INT8KV_ERR_UNSUPPORTED;
-  // one block per SM: (query tiles of 128 rows) x kv heads x splits ~ SM count
+  // One block per SM at a time: (query tiles of 128 rows) x kv heads x splits
+  // blocks run in ceil(blocks / SMs) waves of ceil(pages / splits) pages each.
+  // Take the split count with the shortest such chain, counting two pages of
+  // per-block overhead (the q tile, the epilogue) per wave.
   const long long tiles = (n_new + 128 / G - 1) / (128 / G);
   const long long units = tiles * pool->n_kv_heads;
-  long long n = pool->num_sms / units;
   const int pages = (start_pos + n_new + pool->page_size - 1) / pool->page_size;
-  if (n > pages) n = pages;
-  if (n > kMaxSplits) n = kMaxSplits;
-  if (n < 1) n = 1;
-  return (int)n;
+  const long long sms = pool->num_sms > 0 ? pool->num_sms : 1;
+  const int top = pages < kMaxSplits ? pages : kMaxSplits;
+  long long best = -1;
+  int n = 1;
+  for (int s = 1; s <= top; ++s) {
+    const long long waves = (units * s + sms - 1) / sms;
+    const long long cost = waves * ((pages + s - 1) / s + 2);
+    if (best < 0 || cost < best) {
+      best = cost;
+      n = s;
+    }
+  }
+  return n;
 }
 
 int attn_prefill_workspace_bytes(int n_new, int n_heads, int n_kv_heads, int head_dim,

@@ -46,7 +46,7 @@ def _run(seed, H, Hkv, D, gs, start, n_new, variant, n_splits=0, outliers=True, 
 
 
 @pytest.mark.parametrize("start,n_new", [(0, 1), (0, 70), (100, 17), (1000, 200), (4000, 64)])
-@pytest.mark.parametrize("n_splits", [1, 3, 0])
+@pytest.mark.parametrize("n_splits", [1, 3, 20, 0])
 def test_prefill_matches_oracle_grouped(start, n_new, n_splits):
     out, ref, *_ = _run(10 + start + n_new, 16, 2, 256, 64, start, n_new, 0, n_splits)
     gu.assert_attention_close(out, ref, f"start {start} n_new {n_new} ns {n_splits}")
