@@ -134,11 +134,12 @@ int kv_quant_append(const int8kv_pool* pool, int layer, const uint16_t* k_new,
                     const int32_t* page_table, int max_pages_per_seq, void* stream);
 
 /* Splits the library picks when attn_decode_int8 gets n_splits = 0, for a
- * batch of `batch` sequences of at most max_ctx positions on this pool: as
- * many (sequence, kv head, split) blocks as the decode kernel keeps resident
- * on the pool's device at once (queried once per pool), and at least enough
- * that a split of a max_ctx sequence holds no more than 64 pages; each split at
- * least one page.
+ * batch of `batch` sequences of at most max_ctx positions on this pool.  The
+ * (sequence, kv head, split) blocks run in waves of as many blocks as the
+ * decode kernel keeps resident on the pool's device (queried once per pool);
+ * the count with the shortest chain of waves x (pages per block + 1), plus 2
+ * when the splits need combining, is returned: at least 1, at most the pages
+ * of max_ctx and 256.
  * Returns >= 1, or a negative status (NULL_PTR, INVALID_ARG). */
 int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx);
 

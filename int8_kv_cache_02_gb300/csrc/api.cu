@@ -236,18 +236,26 @@ int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx) {
     }
     mp->resident = n > 0 ? n : 3 * pool->num_sms;
   }
+  // units x splits blocks run in ceil(blocks / resident) waves, each as long as
+  // a block's ceil(pages / splits) pages plus about one page of prologue and
+  // epilogue; more than one split adds the combine (about two pages).  Take the
+  // split count with the shortest chain (the smallest on a tie).
   const long long units = (long long)batch * pool->n_kv_heads;
   const int ps = pool->page_size;
   const int pages = max_ctx > 0 ? (max_ctx + ps - 1) / ps : 1;
-  long long n = (pool->resident + units - 1) / units;
-  // with more units than resident blocks, still cut long sequences so that no
-  // block holds more than 64 pages: ragged batches then balance over the waves
-  const long long by_length = (pages + 63) / 64;
-  if (n < by_length) n = by_length;
-  if (n > pages) n = pages;
-  if (n > kMaxSplits) n = kMaxSplits;
-  if (n < 1) n = 1;
-  return (int)n;
+  const long long resident = pool->resident;
+  const int top = pages < kMaxSplits ? pages : kMaxSplits;
+  long long best = -1;
+  int n = 1;
+  for (int s = 1; s <= top; ++s) {
+    const long long waves = (units * s + resident - 1) / resident;
+    const long long cost = waves * ((pages + s - 1) / s + 1) + (s > 1 ? 2 : 0);
+    if (best < 0 || cost < best) {
+      best = cost;
+      n = s;
+    }
+  }
+  return n;
 }
 
 int attn_decode_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_dim,
