@@ -133,10 +133,32 @@ int kv_quant_append(const int8kv_pool* pool, int layer, const uint16_t* k_new,
                     const uint16_t* v_new, int n_seqs, int n_new, const int32_t* seq_pos,
                     const int32_t* page_table, int max_pages_per_seq, void* stream);
 
+/* Decode kernels, for kv_pool_set_decode_kernel. */
+#define INT8KV_DECODE_AUTO      0  /* the library's choice (the default) */
+#define INT8KV_DECODE_WARP_MMA  1  /* warp-level tensor-core kernel (mma.sync): fused append,
+                                      up to 8 splits combined in the kernel */
+#define INT8KV_DECODE_TCGEN05   2  /* tensor-memory kernel (tcgen05.mma, S and O in tensor
+                                      memory, separate converter and softmax warps); int8 K
+                                      and V only; the combine kernel reduces its splits.
+                                      Slower than WARP_MMA on GB300 at every measured
+                                      size: never picked by AUTO */
+#define INT8KV_DECODE_SIMT      3  /* CUDA-core kernel: any shape the pool takes */
+
+/* Choose the kernel that serves this pool's decode calls (attn_decode_int8,
+ * attn_decode_append_int8, attn_decode_n_splits).  All kernels compute the same
+ * result within the attention tolerance; the choice is for tuning and testing.
+ * WARP_MMA and TCGEN05 need page_size 64, head_dim 128 or 256 and
+ * group_size >= 64 (TCGEN05 also the K8V8 variant); a call whose
+ * n_heads / n_kv_heads exceeds 8 uses SIMT whatever the choice.
+ * Errors: NULL_PTR, INVALID_ARG (unknown kind), UNSUPPORTED (the kernel does not
+ * serve the pool's shape or variant). */
+int kv_pool_set_decode_kernel(int8kv_pool* pool, int kind);
+
 /* Splits the library picks when attn_decode_int8 gets n_splits = 0, for a
  * batch of `batch` sequences of at most max_ctx positions on this pool.  The
  * (sequence, kv head, split) blocks run in waves of as many blocks as the
- * decode kernel keeps resident on the pool's device (queried once per pool);
+ * pool's decode kernel keeps resident on the pool's device (queried once per
+ * pool and kernel);
  * the count with the shortest chain of waves x (pages per block + 1), plus 2
  * when the splits need combining, is returned: at least 1, at most the pages
  * of max_ctx and 256.
@@ -166,9 +188,10 @@ int attn_decode_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head
  *   workspace    device, >= attn_decode_workspace_bytes, 16-byte aligned, any
  *                contents (every partial a call reads, it writes first).  Calls
  *                sharing one workspace must not overlap on the device.
- * Up to 8 splits are combined inside the decode kernel (the splits of a
- * (sequence, kv head) form one thread-block cluster and reduce through
- * distributed shared memory); with more, a combine kernel follows on the stream.
+ * With the warp-level tensor-core kernel, up to 8 splits are combined inside
+ * the decode kernel (the splits of a (sequence, kv head) form one thread-block
+ * cluster and reduce through distributed shared memory); with more, or with the
+ * other kernels, a combine kernel follows on the stream.
  * n_heads must be a multiple of n_kv_heads with n_heads / n_kv_heads <= 8.
  * Errors: NULL_PTR, INVALID_ARG, UNSUPPORTED, WORKSPACE, CAPACITY, CUDA. */
 int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int batch,
@@ -179,10 +202,10 @@ int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int 
 /* One decode step with its append fused: the new token's K and V rows
  *   k_new, v_new  device fp16 [batch][n_kv_heads][head_dim]
  * are quantized (as kv_quant_append does) into position seq_lens[b] - 1 of each
- * sequence, then attn_decode_int8 runs over positions 0 .. seq_lens[b] - 1.  On
- * the tensor-core path the block whose key range holds the new position writes
- * it before streaming its pages, so the whole step is one kernel; otherwise the
- * append kernel runs first on the same stream.  Same arguments, workspace and
+ * sequence, then attn_decode_int8 runs over positions 0 .. seq_lens[b] - 1.  With
+ * the warp-level tensor-core kernel the block whose key range holds the new
+ * position writes it before streaming its pages, so the whole step is one
+ * kernel; otherwise the append kernel runs first on the same stream.  Same arguments, workspace and
  * errors as attn_decode_int8 (a length beyond the page-table row skips the
  * append and is flagged).  Bit-identical to kv_quant_append followed by
  * attn_decode_int8. */

@@ -21,6 +21,7 @@ K8V8, K8V16, K16V8 = 0, 1, 2
 VARIANTS = {"k8v8": K8V8, "k8v16": K8V16, "k16v8": K16V8}
 REGION_K_STORE, REGION_V_STORE, REGION_K_SCALES, REGION_V_SCALES = 0, 1, 2, 3
 DEVERR_PAGE_ID, DEVERR_LENGTH, DEVERR_TIMEOUT = 1, 2, 4
+DECODE_AUTO, DECODE_WARP_MMA, DECODE_TCGEN05, DECODE_SIMT = 0, 1, 2, 3
 
 _c_int, _c_size, _vp, _c_float = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
 _SIGS = {
@@ -43,6 +44,7 @@ _SIGS = {
                                          _c_float, _c_int, _vp, _vp, _c_size, _vp]),
     "attn_decode_int8_noalloc": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _c_int,
                                           _c_int, _c_float, _c_int, _vp, _vp]),
+    "kv_pool_set_decode_kernel": (_c_int, [_vp, _c_int]),
 }
 
 _lib = None
@@ -223,6 +225,11 @@ def attn_prefill_chunk_int8(pool, layer, q, start_pos, page_table, out, workspac
                                          _stream(stream)), "attn_prefill_chunk_int8")
 
 
+def kv_pool_set_decode_kernel(pool, kind):
+    """kind: DECODE_AUTO, DECODE_WARP_MMA, DECODE_TCGEN05 or DECODE_SIMT."""
+    _check(lib().kv_pool_set_decode_kernel(pool.handle, int(kind)), "kv_pool_set_decode_kernel")
+
+
 def kv_pool_read_device_error(pool, stream=None):
     v = ctypes.c_int32(0)
     _check(lib().kv_pool_read_device_error(pool.handle, ctypes.byref(v), _stream(stream)),
@@ -266,6 +273,9 @@ class KVPool:
         if h is not None and _lib is not None:
             _lib.kv_pool_destroy(h)
             self.handle = None
+
+    def set_decode_kernel(self, kind):
+        kv_pool_set_decode_kernel(self, kind)
 
     def decode_workspace(self, batch, n_heads, n_splits):
         n = attn_decode_workspace_bytes(batch, n_heads, self.n_kv_heads, self.head_dim, n_splits)

@@ -187,7 +187,8 @@ int kv_pool_create(int8kv_pool** out, int n_layers, int n_kv_heads, int head_dim
   p->device = dev;
   p->num_sms = sms;
   p->has_tmaps = false;
-  p->resident = 0;
+  p->decode_kernel = INT8KV_DECODE_AUTO;
+  for (int k = 0; k < 4; ++k) p->resident[k] = 0;
   if (page_size == 64 && (head_dim == 128 || head_dim == 256)) {
     const size_t rows = (size_t)n_layers * n_pages * n_kv_heads * page_size;
     if (rows >= (1ull << 31) || !make_store_map(&p->tmap_k, k_store, k8, head_dim, rows) ||
@@ -218,23 +219,39 @@ int kv_quant_append(const int8kv_pool* pool, int layer, const uint16_t* k_new,
   return e == cudaSuccess ? INT8KV_OK : INT8KV_ERR_CUDA;
 }
 
+int kv_pool_set_decode_kernel(int8kv_pool* pool, int kind) {
+  if (!pool) return INT8KV_ERR_NULL_PTR;
+  if (kind < INT8KV_DECODE_AUTO || kind > INT8KV_DECODE_SIMT) return INT8KV_ERR_INVALID_ARG;
+  const PoolView v = layer_view(pool, 0);
+  if (kind == INT8KV_DECODE_WARP_MMA && !(pool->has_tmaps && decode_mma_supported(v, 1)))
+    return INT8KV_ERR_UNSUPPORTED;
+  if (kind == INT8KV_DECODE_TCGEN05 &&
+      !(pool->has_tmaps && decode_tc_supported(v, pool->k_int8, pool->v_int8, 1)))
+    return INT8KV_ERR_UNSUPPORTED;
+  pool->decode_kernel = kind;
+  return INT8KV_OK;
+}
+
 int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx) {
   if (!pool) return INT8KV_ERR_NULL_PTR;
   if (batch <= 0 || max_ctx < 0) return INT8KV_ERR_INVALID_ARG;
-  if (pool->resident == 0) {
-    // Blocks the decode kernel keeps resident at once (three per SM for the
-    // tensor-core kernel's shapes); the CUDA-core kernel is taken as three per SM.
+  const int kind = decode_kernel_for(pool, 1);
+  if (pool->resident[kind] == 0) {
+    // Blocks the pool's decode kernel keeps resident at once (queried once);
+    // the CUDA-core kernel is taken as three per SM.
     int8kv_pool* mp = const_cast<int8kv_pool*>(pool);
     int n = 0;
-    if (pool->has_tmaps && pool->group_size >= 64) {
+    if (kind != INT8KV_DECODE_SIMT) {
       int prev = -1;
       if (cudaGetDevice(&prev) == cudaSuccess && prev != pool->device)
         cudaSetDevice(pool->device);
-      n = decode_mma_resident_blocks(pool->head_dim, pool->k_int8, pool->v_int8,
-                                     pool->n_groups);
+      n = kind == INT8KV_DECODE_TCGEN05
+              ? decode_tc_resident_blocks(pool->head_dim, pool->n_groups)
+              : decode_mma_resident_blocks(pool->head_dim, pool->k_int8, pool->v_int8,
+                                           pool->n_groups);
       if (prev >= 0 && prev != pool->device) cudaSetDevice(prev);
     }
-    mp->resident = n > 0 ? n : 3 * pool->num_sms;
+    mp->resident[kind] = n > 0 ? n : 3 * pool->num_sms;
   }
   // units x splits blocks run in ceil(blocks / resident) waves, each as long as
   // a block's ceil(pages / splits) pages plus about one page of prologue and
@@ -243,7 +260,7 @@ int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx) {
   const long long units = (long long)batch * pool->n_kv_heads;
   const int ps = pool->page_size;
   const int pages = max_ctx > 0 ? (max_ctx + ps - 1) / ps : 1;
-  const long long resident = pool->resident;
+  const long long resident = pool->resident[kind];
   const int top = pages < kMaxSplits ? pages : kMaxSplits;
   long long best = -1;
   int n = 1;
@@ -439,29 +456,51 @@ int kv_pool_read_device_error(const int8kv_pool* pool, int32_t* out, void* strea
 
 namespace int8kv {
 
+int decode_kernel_for(const int8kv_pool* pool, int G) {
+  const PoolView v = layer_view(pool, 0);
+  const bool mma_ok = pool->has_tmaps && decode_mma_supported(v, G);
+  const bool tc_ok = pool->has_tmaps && decode_tc_supported(v, pool->k_int8, pool->v_int8, G);
+  switch (pool->decode_kernel) {
+    case INT8KV_DECODE_WARP_MMA:
+      if (mma_ok) return INT8KV_DECODE_WARP_MMA;
+      break;
+    case INT8KV_DECODE_TCGEN05:
+      if (tc_ok) return INT8KV_DECODE_TCGEN05;
+      break;
+    case INT8KV_DECODE_SIMT:
+      return INT8KV_DECODE_SIMT;
+    default:
+      break;
+  }
+  if (mma_ok) return INT8KV_DECODE_WARP_MMA;
+  return INT8KV_DECODE_SIMT;
+}
+
 cudaError_t launch_decode(const int8kv_pool* pool, int layer, const DecodeArgs& a_in,
                           cudaStream_t stream) {
   bool k8, v8;
   variant_int8(pool->variant, &k8, &v8);
   DecodeArgs a = a_in;
-  if (a.k_new && !(pool->has_tmaps && decode_mma_supported(a.pool, a.G))) {
-    // the CUDA-core kernel has no fused append: append first, at seq_lens[b] - 1
+  const int kind = decode_kernel_for(pool, a.G);
+  if (a.k_new && kind != INT8KV_DECODE_WARP_MMA) {
+    // only the warp-level kernel fuses the append: append first, at seq_lens[b] - 1
     const cudaError_t e0 = launch_quant_append(a.pool, a.k_new, a.v_new, a.B, 1, a.seq_lens,
                                                a.page_table, a.max_pages, k8, v8, stream, -1);
     if (e0 != cudaSuccess) return e0;
     a.k_new = a.v_new = nullptr;
   }
-  // The tensor-core kernel combines up to 8 splits itself (one cluster); more
-  // splits, and the CUDA-core kernel's, go through the combine kernel.
-  if (pool->has_tmaps && decode_mma_supported(a.pool, a.G)) {
-    const cudaError_t e = launch_decode_mma(a, k8, v8, pool->tmap_k, pool->tmap_v,
-                                            layer * pool->n_pages, stream);
+  cudaError_t e;
+  if (kind == INT8KV_DECODE_WARP_MMA) {
+    e = launch_decode_mma(a, k8, v8, pool->tmap_k, pool->tmap_v, layer * pool->n_pages, stream);
     // up to 8 splits are combined inside the kernel (one cluster)
     if (e != cudaSuccess || a.n_splits <= 8) return e;
-    return launch_decode_combine(a, stream);
+  } else if (kind == INT8KV_DECODE_TCGEN05) {
+    e = launch_decode_tc(a, pool->tmap_k, pool->tmap_v, layer * pool->n_pages, stream);
+    if (e != cudaSuccess || a.n_splits == 1) return e;
+  } else {
+    e = launch_decode_simt(a, k8, v8, stream);
+    if (e != cudaSuccess || a.n_splits == 1) return e;
   }
-  const cudaError_t e = launch_decode_simt(a, k8, v8, stream);
-  if (e != cudaSuccess || a.n_splits == 1) return e;
   return launch_decode_combine(a, stream);
 }
 

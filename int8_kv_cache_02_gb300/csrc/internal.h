@@ -21,7 +21,8 @@ struct int8kv_pool {
   int device;        // CUDA device the pool was created on
   int num_sms;       // its SM count (split heuristic)
   bool has_tmaps;    // TMA descriptors below are valid (shapes the tensor-core decode serves)
-  int resident;      // blocks of its decode kernel resident at once (0 = not yet queried)
+  int decode_kernel; // INT8KV_DECODE_*: the kernel its decode calls use (AUTO = the library's choice)
+  int resident[4];   // per INT8KV_DECODE_* kernel: blocks resident at once (0 = not yet queried)
   CUtensorMap tmap_k;              // K store as [rows][head_dim], 64-row x 128-byte swizzled boxes
   CUtensorMap tmap_v;              // V store, same
 };
@@ -95,8 +96,13 @@ cudaError_t launch_quant_append(const PoolView& pool, const uint16_t* k_new, con
                                 const int32_t* page_table, int max_pages, bool k_int8,
                                 bool v_int8, cudaStream_t stream, int pos_offset = 0);
 
-// Partial kernel (tensor-core when the shape allows, else CUDA-core) and, with
-// n_splits > 1, the combine.  cudaErrorNotSupported when no kernel fits.
+// The decode kernel (INT8KV_DECODE_WARP_MMA, _TCGEN05 or _SIMT) that serves a
+// call with G query heads per kv head on this pool.
+int decode_kernel_for(const int8kv_pool* pool, int G);
+
+// Partial kernel (the one decode_kernel_for picks) and, with n_splits > 1 where
+// that kernel does not combine itself, the combine.  cudaErrorNotSupported when
+// no kernel fits.
 cudaError_t launch_decode(const int8kv_pool* pool, int layer, const DecodeArgs& a,
                           cudaStream_t stream);
 

@@ -42,6 +42,7 @@
 #include "decode_common.cuh"
 #include "mma_common.cuh"
 #include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace int8kv {
 namespace {
@@ -82,74 +83,18 @@ struct TLayout {
 };
 
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int b_mn) {
-  // kind::f16: D f32 (bits 4-5 = 1), A and B f16, A K-major, B K- or MN-major,
-  // N >> 3 at bit 17, M >> 4 at bit 24
-  return (1u << 4) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+  return tc::idesc_f16(M, N, 0, b_mn);   // A K-major
 }
-
-// Shared-memory matrix descriptor: 128-byte swizzle, rows of 128 B in groups of
-// 8 (stride 1024 B), start and offsets in 16-byte units.
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, bool acc) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.u32 p, %4, 0; "
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
-      "l"(a), "l"(b), "r"(id), "r"((uint32_t)acc)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id,
-                                       bool acc) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.u32 p, %4, 0; "
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d),
-      "r"(a_tmem), "l"(b), "r"(id), "r"((uint32_t)acc)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          ptx::smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// 16 consecutive 32-bit columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t ta, uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15}, [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-        "=r"(v[14]), "=r"(v[15])
-      : "r"(ta));
-}
-__device__ __forceinline__ void tmem_st16(uint32_t ta, const uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16};" ::"r"(ta),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
+using tc::sdesc;
+using tc::mma_ss;
+using tc::mma_ts;
+using tc::mma_commit;
+__device__ __forceinline__ void tc_fence_before() { tc::fence_before(); }
+__device__ __forceinline__ void tc_fence_after() { tc::fence_after(); }
+__device__ __forceinline__ void tmem_ld16(uint32_t ta, uint32_t (&v)[16]) { tc::ld16(ta, v); }
+__device__ __forceinline__ void tmem_st16(uint32_t ta, const uint32_t (&v)[16]) { tc::st16(ta, v); }
+__device__ __forceinline__ void tmem_wait_ld() { tc::wait_ld(); }
+__device__ __forceinline__ void tmem_wait_st() { tc::wait_st(); }
 
 // Multiply this lane's columns [c0, c0 + n) of tensor memory by f.
 __device__ __forceinline__ void tmem_scale(uint32_t ta, int n, float f) {

@@ -54,6 +54,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// True in exactly one active lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Shared-memory counter add with acquire-release ordering at block scope;
 // returns the old value.
 __device__ __forceinline__ int atom_add_acq_rel_shared(int* addr, int v) {
