@@ -111,8 +111,8 @@ template <int D, bool KI8, bool VI8>
 __device__ __forceinline__ void issue_page(unsigned char* smem, uint64_t* full, int* stage_page,
                                            int st, int page, int row, const PoolView& p, int kvh,
                                            const CUtensorMap* tmk, const CUtensorMap* tmv) {
-  mma::issue_page<D, KI8, VI8>(smem + st * Layout<D, KI8, VI8>::STAGE, &full[st], &stage_page[st],
-                               page, row, p, kvh, tmk, tmv);
+  mma::issue_page<D, KI8, VI8, true>(smem + st * Layout<D, KI8, VI8>::STAGE, &full[st],
+                                     &stage_page[st], page, row, p, kvh, tmk, tmv);
 }
 
 template <int NG>

@@ -278,7 +278,7 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     }
     auto issue = [&](int i) {
       const int st = i % NS, page = page_of(i);
-      mma::issue_page<D, true, true>(smem + LY::RAW_OFF + st * SP::STAGE, &full[st],
+      mma::issue_page<D, true, true, true>(smem + LY::RAW_OFF + st * SP::STAGE, &full[st],
                                      &stage_page[st], page,
                                      ((layer_page0 + page) * p.Hkv + kvh) * kPage, p, kvh,
                                      &tmk, &tmv);

@@ -59,8 +59,10 @@ __device__ __forceinline__ int exponent_of(float x) {   // floor(log2 x), x > 0 
 }
 
 // Issue the copies of one page (or, for a page id flagged invalid, complete the
-// stage's barrier with no bytes) into stage `st`.
-template <int D, bool KI8, bool VI8>
+// stage's barrier with no bytes) into stage `st`.  kStream: the page is read
+// once (decode), so its L2 lines go first; otherwise (prefill: every query tile
+// of the kv head reads it) the default policy keeps it for the other blocks.
+template <int D, bool KI8, bool VI8, bool kStream = false>
 __device__ __forceinline__ void issue_page(unsigned char* stage, uint64_t* full_bar, int* stage_page,
                                            int page, int row, const PoolView& p, int kvh,
                                            const CUtensorMap* tmk, const CUtensorMap* tmv) {
@@ -76,15 +78,27 @@ __device__ __forceinline__ void issue_page(unsigned char* stage, uint64_t* full_
   ptx::mbar_arrive_expect_tx(full_bar, tx);
   constexpr int KX = KI8 ? 128 : 64;   // box width in elements
   constexpr int VX = VI8 ? 128 : 64;
-#pragma unroll
-  for (int bx = 0; bx < SP::KBOXES; ++bx)
-    ptx::tma_load_2d(stage + SP::K_OFF + bx * kBoxBytes, tmk, bx * KX, row, full_bar);
-#pragma unroll
-  for (int bx = 0; bx < SP::VBOXES; ++bx)
-    ptx::tma_load_2d(stage + SP::V_OFF + bx * kBoxBytes, tmv, bx * VX, row, full_bar);
   const size_t srow = ((size_t)page * p.Hkv + kvh) * kPage * ng;
-  if (KI8) ptx::bulk_load(stage + SP::KS_OFF, p.ks + srow, kPage * ng * 2, full_bar);
-  if (VI8) ptx::bulk_load(stage + SP::VS_OFF, p.vs + srow, kPage * ng * 2, full_bar);
+  if constexpr (kStream) {
+    const uint64_t pol = ptx::policy_evict_first();
+#pragma unroll
+    for (int bx = 0; bx < SP::KBOXES; ++bx)
+      ptx::tma_load_2d_hint(stage + SP::K_OFF + bx * kBoxBytes, tmk, bx * KX, row, full_bar, pol);
+#pragma unroll
+    for (int bx = 0; bx < SP::VBOXES; ++bx)
+      ptx::tma_load_2d_hint(stage + SP::V_OFF + bx * kBoxBytes, tmv, bx * VX, row, full_bar, pol);
+    if (KI8) ptx::bulk_load_hint(stage + SP::KS_OFF, p.ks + srow, kPage * ng * 2, full_bar, pol);
+    if (VI8) ptx::bulk_load_hint(stage + SP::VS_OFF, p.vs + srow, kPage * ng * 2, full_bar, pol);
+  } else {
+#pragma unroll
+    for (int bx = 0; bx < SP::KBOXES; ++bx)
+      ptx::tma_load_2d(stage + SP::K_OFF + bx * kBoxBytes, tmk, bx * KX, row, full_bar);
+#pragma unroll
+    for (int bx = 0; bx < SP::VBOXES; ++bx)
+      ptx::tma_load_2d(stage + SP::V_OFF + bx * kBoxBytes, tmv, bx * VX, row, full_bar);
+    if (KI8) ptx::bulk_load(stage + SP::KS_OFF, p.ks + srow, kPage * ng * 2, full_bar);
+    if (VI8) ptx::bulk_load(stage + SP::VS_OFF, p.vs + srow, kPage * ng * 2, full_bar);
+  }
 }
 
 }  // namespace mma
