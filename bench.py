@@ -486,7 +486,7 @@ def run_prefill(n_iter=20):
     return {"us_per_step": ms * 1e3, "TFLOPs": PREFILL_FLOPS / (ms * 1e-3) / 1e12,
             "algorithmic_flops": PREFILL_FLOPS, "kv_bytes": kv_bytes, "n_splits": ns,
             "note": "append of the 256-token chunk + causal attention; the 33,024-position "
-                    "cache (34 MB) is L2-resident; bound by the tensor pipe"}
+                    "cache (34 MB) is L2-resident; paced by the CUDA-core work between the two MMA batches of a page"}
 
 
 def run_batched(n_iter=20):

@@ -111,33 +111,47 @@ __device__ __forceinline__ void tmem_scale(uint32_t ta, int n, float f) {
 
 __device__ __forceinline__ int swz(int row, int c) { return row * 128 + ((c ^ (row & 7)) << 4); }
 
-// 16 int8 codes -> 16 exact fp16 values in natural order.
+// 16 int8 codes -> 16 exact fp16 values, two per operation: bytes 0 and 2 of a
+// word, then 1 and 3, so inside each group of four dims, positions 1 and 2 hold
+// dims 2 and 1 (the Q tile is stored in the same order, and O's columns are
+// read back through it).
 __device__ __forceinline__ void codes_to_f16(const uint4 w, uint4& lo, uint4& hi) {
-  const uint32_t in[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u,
-                          w.w ^ 0x80808080u};
-  uint32_t o[8];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    o[2 * k] = mma::sub1152(ptx::prmt(in[k], 0x64646464u, 0x4140));
-    o[2 * k + 1] = mma::sub1152(ptx::prmt(in[k], 0x64646464u, 0x4342));
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
+  using mma::lop_i8pair;
+  using mma::sub1152;
+  lo = make_uint4(sub1152(lop_i8pair(w.x)), sub1152(lop_i8pair(w.x >> 8)),
+                  sub1152(lop_i8pair(w.y)), sub1152(lop_i8pair(w.y >> 8)));
+  hi = make_uint4(sub1152(lop_i8pair(w.z)), sub1152(lop_i8pair(w.z >> 8)),
+                  sub1152(lop_i8pair(w.w)), sub1152(lop_i8pair(w.w >> 8)));
+}
+
+// Dims of 8 consecutive fp16 values (one 16-byte chunk) in that order.
+__device__ __forceinline__ uint4 pair_order(const uint4 x) {
+  return make_uint4(ptx::prmt(x.x, x.y, 0x5410), ptx::prmt(x.x, x.y, 0x7632),
+                    ptx::prmt(x.z, x.w, 0x5410), ptx::prmt(x.z, x.w, 0x7632));
 }
 
 // int8 rows of one side (K or V) of a staged page -> fp16 boxes [D/64][64][128 B].
 // Eight consecutive threads take one code chunk of eight consecutive rows, so
-// loads and stores hit eight different swizzled positions.
+// loads and stores hit eight different swizzled positions; every thread's
+// loads are in flight before its first conversion.
 template <int D>
 __device__ __forceinline__ void convert_side(const unsigned char* src, unsigned char* dst) {
-  constexpr int CPR = D / 16;   // 16-byte code chunks per row
-#pragma unroll 4
-  for (int c = threadIdx.x; c < kPage * CPR; c += kThreads) {
-    const int g8 = c >> 3;
+  constexpr int CPR = D / 16;                       // 16-byte code chunks per row
+  constexpr int PER = kPage * CPR / kThreads;       // chunks per thread
+  static_assert(PER * kThreads == kPage * CPR, "whole chunks per thread");
+  uint4 w[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int c = threadIdx.x + k * kThreads, g8 = c >> 3;
     const int row = (g8 / CPR) * 8 + (c & 7), cc = g8 % CPR;
-    const uint4 w = *reinterpret_cast<const uint4*>(src + (cc >> 3) * kBoxBytes + swz(row, cc & 7));
+    w[k] = *reinterpret_cast<const uint4*>(src + (cc >> 3) * kBoxBytes + swz(row, cc & 7));
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int c = threadIdx.x + k * kThreads, g8 = c >> 3;
+    const int row = (g8 / CPR) * 8 + (c & 7), cc = g8 % CPR;
     uint4 lo, hi;
-    codes_to_f16(w, lo, hi);
+    codes_to_f16(w[k], lo, hi);
     unsigned char* box = dst + (cc >> 2) * kBoxBytes;
     const int c16 = (cc & 3) * 2;
     *reinterpret_cast<uint4*>(box + swz(row, c16)) = lo;
@@ -209,8 +223,10 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
     const int row = c / (D / 8), ch = c - row * (D / 8);
     const int pos = pos0 + row / G;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (pos < a.n_new)
+    if (pos < a.n_new) {
       v = ptx::ldg128(a.q + ((size_t)pos * a.H + (size_t)kvh * G + row % G) * D + ch * 8);
+      if constexpr (KI8) v = pair_order(v);   // the order of the converted K tiles
+    }
     *reinterpret_cast<uint4*>(smem + LY::Q_OFF + (ch >> 3) * LY::QBOX + swz(row, ch & 7)) = v;
   }
   ptx::fence_proxy_async();   // generic writes of the Q tile before the tensor-core reads
@@ -306,20 +322,23 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
     if (page < 0) continue;   // flagged by the lookup; every thread skips alike
     tc_fence_after();
 
-    // ---- S_g = Q_g K_g^T into columns [64g, 64g + 64)
-    if (tid == 0) {
-      const uint32_t kt = ptx::smem_u32(KI8 ? smem + LY::KH_OFF : sb + SP::K_OFF);
-      const uint32_t qt0 = ptx::smem_u32(smem + LY::Q_OFF);
+    // ---- S_g = Q_g K_g^T into columns [64g, 64g + 64).  Warp 0 runs this
+    // (descriptors warp-uniform); one elected lane issues.
+    if (warp == 0) {
+      const uint64_t da0 = sdesc(ptx::smem_u32(smem + LY::Q_OFF), 16, 1024);
+      const uint64_t db0 = sdesc(ptx::smem_u32(KI8 ? smem + LY::KH_OFF : sb + SP::K_OFF), 16, 1024);
+      if (ptx::elect_one()) {
 #pragma unroll
-      for (int g = 0; g < NGK; ++g)
+        for (int g = 0; g < NGK; ++g)
 #pragma unroll
-        for (int kk = 0; kk < KSG; ++kk) {
-          const int ks = g * KSG + kk;   // 16-dim k-step: box ks/4, 32-byte step ks%4
-          const uint64_t da = sdesc(qt0 + (ks >> 2) * LY::QBOX + (ks & 3) * 32, 16, 1024);
-          const uint64_t db = sdesc(kt + (ks >> 2) * kBoxBytes + (ks & 3) * 32, 16, 1024);
-          mma_ss(tbase + g * 64, da, db, idS, kk > 0);
-        }
-      mma_commit(mS);
+          for (int kk = 0; kk < KSG; ++kk) {
+            const int ks = g * KSG + kk;   // 16-dim k-step: box ks/4, 32-byte step ks%4
+            mma_ss(tbase + g * 64, da0 + (((ks >> 2) * LY::QBOX + (ks & 3) * 32) >> 4),
+                   db0 + (((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4), idS, kk > 0);
+          }
+        mma_commit(mS);
+      }
+      __syncwarp();
     }
     // V range per group: 2^e_g bounds every V scale of the group seen so far
     // (the same for every row: block-uniform branches).  O is stable here (the
@@ -452,20 +471,23 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
     tc_fence_after();
 
     // ---- O[:, box b] += P'_hi V_b + P'_lo V_b, chunk by chunk (16 keys each)
-    if (tid == 0) {
-      const uint32_t vt = ptx::smem_u32(VI8 ? smem + LY::VH_OFF : sb + SP::V_OFF);
+    if (warp == 0) {
+      const uint64_t dv0 = sdesc(ptx::smem_u32(VI8 ? smem + LY::VH_OFF : sb + SP::V_OFF), 1024, 1024);
+      if (ptx::elect_one()) {
 #pragma unroll
-      for (int b = 0; b < D / 64; ++b) {
-        const int g = b / BPG;
+        for (int b = 0; b < D / 64; ++b) {
+          const int g = b / BPG;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint64_t dv = sdesc(vt + b * kBoxBytes + c * 2048, 1024, 1024);
-          const uint32_t pa = tbase + g * 64 + c * 16;
-          mma_ts(tbase + LY::OB + b * 64, pa, dv, idO, o_live || c > 0);
-          mma_ts(tbase + LY::OB + b * 64, pa + 8, dv, idO, true);
+          for (int c = 0; c < 4; ++c) {
+            const uint64_t dv = dv0 + ((b * kBoxBytes + c * 2048) >> 4);
+            const uint32_t pa = tbase + g * 64 + c * 16;
+            mma_ts(tbase + LY::OB + b * 64, pa, dv, idO, o_live || c > 0);
+            mma_ts(tbase + LY::OB + b * 64, pa + 8, dv, idO, true);
+          }
         }
+        mma_commit(mO);
       }
-      mma_commit(mO);
+      __syncwarp();
     }
     ++nO;
     o_live = true;
@@ -496,11 +518,13 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
     const float f = S == 1 ? (l > 0.f ? u / l : 0.f) : u;
     float* dst = S == 1 ? a.out + h * D + c : a.ws.part_o + (h * S + split) * D + c;
     if (wr) {   // no P.V batch at all: O was never written, the row is 0
+      // int8 V: columns 4j + 1 and 4j + 2 hold dims 4j + 2 and 4j + 1
+      constexpr int X1 = VI8 ? 2 : 1, X2 = VI8 ? 1 : 2;
 #pragma unroll
       for (int k = 0; k < 16; k += 4)
         *reinterpret_cast<float4*>(dst + k) =
-            o_live ? make_float4(__uint_as_float(v[k]) * f, __uint_as_float(v[k + 1]) * f,
-                                 __uint_as_float(v[k + 2]) * f, __uint_as_float(v[k + 3]) * f)
+            o_live ? make_float4(__uint_as_float(v[k]) * f, __uint_as_float(v[k + X1]) * f,
+                                 __uint_as_float(v[k + X2]) * f, __uint_as_float(v[k + 3]) * f)
                    : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
