@@ -265,14 +265,17 @@ def traffic_from_profiles(kernel_src_sha):
     return val if sha == kernel_src_sha and val is not None else None
 
 
+DECODE_SOURCES = ("common.cuh", "decode_combine.cu", "decode_common.cuh", "decode_mma.cu",
+                  "internal.h", "mma_common.cuh", "ptx.cuh", "quant_row.cuh")
+
+
 def decode_source_sha():
-    """Hash of the sources the decode kernels are built from."""
+    """Hash of the sources the timed decode step's kernels (the warp-level
+    tensor-core decode kernel and the combine) are built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "int8_kv_cache_02_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
-        if n.startswith("decode") or n in ("common.cuh", "internal.h", "ptx.cuh",
-                                           "mma_common.cuh", "quant_row.cuh"):
-            h.update(open(os.path.join(csrc, n), "rb").read())
+    for n in DECODE_SOURCES:
+        h.update(open(os.path.join(csrc, n), "rb").read())
     return h.hexdigest()[:16]
 
 
