@@ -137,11 +137,11 @@ int kv_quant_append(const int8kv_pool* pool, int layer, const uint16_t* k_new,
 #define INT8KV_DECODE_AUTO      0  /* the library's choice (the default) */
 #define INT8KV_DECODE_WARP_MMA  1  /* warp-level tensor-core kernel (mma.sync): fused append,
                                       up to 8 splits combined in the kernel */
-#define INT8KV_DECODE_TCGEN05   2  /* tensor-memory kernel (tcgen05.mma, S and O in tensor
-                                      memory, separate converter and softmax warps); int8 K
-                                      and V only; the combine kernel reduces its splits.
-                                      Slower than WARP_MMA on GB300 at every measured
-                                      size: never picked by AUTO */
+#define INT8KV_DECODE_TCGEN05   2  /* tensor-memory kernel (tcgen05.mma; K, S and O in
+                                      tensor memory; converter, softmax and producer
+                                      warps); int8 K and V only; the combine kernel reduces
+                                      its splits.  Slower than WARP_MMA on GB300 at every
+                                      measured size: never picked by AUTO */
 #define INT8KV_DECODE_SIMT      3  /* CUDA-core kernel: any shape the pool takes */
 
 /* Choose the kernel that serves this pool's decode calls (attn_decode_int8,

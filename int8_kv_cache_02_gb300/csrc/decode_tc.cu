@@ -19,28 +19,32 @@
 // all the MMAs, and the CUDA cores are left with turning codes into fp16, the
 // softmax and P', in separate warps working on different pages.
 //
-// Measured on GB300 (128K positions, k8v8): 45-47 us against 34.4 us for the
-// mma.sync kernel, so the library does not pick it by itself.  The tensor core
-// reads its operands from shared memory, so every page crosses shared memory
-// several times -- TMA in (33 KB), int8 codes out (32 KB), fp16 tiles in (64 KB)
-// and out again to the tensor core (64 KB): ~200 KB per page, which at 128 B per
-// clock takes longer than the page's share of HBM time.  Feeding K and V from
-// tensor memory instead (V stored transposed within a page) would remove the
-// fp16 round trip.
+// Measured on GB300 (128K positions, k8v8): 41.9 us against 33.8 us for the
+// mma.sync kernel, so the library does not pick it by itself.  K reaches the
+// tensor core from tensor memory (the converters build mma-style fragments and
+// store them with tcgen05.st.16x256b), V through an fp16 tile in shared memory.
+// Per page the converters need ~2,000 clocks and the softmax ~1,500 (both chains
+// of dependent latencies, one page at a time per role), against ~1,560 clocks of
+// HBM time per page at the measured peak.
 //
-// Roles (416 threads, one block per SM at head_dim 256):
+// Roles (448 threads, one block per SM at head_dim 256):
 //   warps 0-3  softmax.  Warp w owns tokens 16w .. 16w + 15 of every page.
-//   warps 4-11 converters.  int8 K and V rows of a staged page become fp16
-//              tiles Kc, Vc (128-byte-swizzled boxes [D/64][64 tokens][128 B]),
-//              the scales become fp32 tables, and the page's largest V scale
-//              per group is noted.
+//   warps 4-11 converters.  int8 K rows of a staged page become the fp16 A
+//              operand of q.K^T in tensor memory (Ka), V rows an fp16 tile Vc in
+//              shared memory (128-byte-swizzled boxes [D/64][64 tokens][128 B]),
+//              the scales fp32 tables; the page's largest V scale per group is
+//              noted.
 //              The staged page is released as soon as its codes are in
 //              registers, so its stage refills while they are converted.
-//   warp 12    producer.  An elected lane issues the TMA copies of the page
-//              ring (three stages) and every MMA.
-// Per page i (buffers b = i % 2 of Vc, the tables, P' and S; one Kc):
-//   producer   S_g[b] = sum over the group's 64-dim boxes of Kc q^T: M = 64
-//              tokens, N = 16 (the G <= 8 heads, zero-padded), K = 16.
+//   warp 12    producer of S: an elected lane issues the TMA copies of the
+//              page ring (four stages) and q.K^T.
+//   warp 13    producer of O: an elected lane issues P.V.
+// Per page i (buffers b = i % 2 of Ka, Vc, the tables, P' and S):
+//   converters K rows -> Ka[b] in tensor memory and the scale tables ("K ready"),
+//              then V rows -> the fp16 tile Vc[b] in shared memory ("V ready").
+//   producer   S_g[b] = sum over the group's 64-dim boxes of Ka q^T: M = 64
+//              tokens, N = 16 (the G <= 8 heads, zero-padded), K = 16, A read
+//              from tensor memory.
 //   softmax    s = sum_g table_k * S_g (tensor memory, mma-fragment layout),
 //              masks, per-head page maxima shared by the four warps, the lazy
 //              rescale (O in tensor memory, read and rewritten per warp quarter),
@@ -54,9 +58,10 @@
 // device error bit on expiry.
 //
 // Codes are turned into fp16 two at a time -- bytes 0 and 2 of a word, then 1
-// and 3 -- so inside each group of four dims, tile positions 1 and 2 hold dims
-// 2 and 1.  q is laid out in the same order (q.k is unchanged), and the rows of
-// O (dims) are read back through it.
+// and 3.  In Vc, positions 1 and 2 of every four dims swap, and the rows of O
+// (dims) are read back through that order.  In Ka, K index 16e + 4u + x of a
+// 64-dim box holds dim 16u + 4e + (0, 2, 1, 3)[x] (see KFrag); q is laid out in
+// the same K order, so q.k is unchanged.
 
 #include <climits>
 
@@ -83,8 +88,9 @@ using mma::sub1152;
 constexpr int kSoftWarps = 4;
 constexpr int kConvWarps = 8;
 constexpr int kConv0 = kSoftWarps * 32;                  // first converter thread
-constexpr int kProd = (kSoftWarps + kConvWarps) * 32;    // the producer thread
-constexpr int kThreads = kProd + 32;
+constexpr int kProdK = kSoftWarps + kConvWarps;          // warp: copies and q.K
+constexpr int kProdV = kProdK + 1;                       // warp: P.V
+constexpr int kThreads = (kProdV + 1) * 32;
 constexpr float kTau = 8.f;         // lazy rescale: the reference max moves when exceeded by > 2^8
 constexpr int kPShift = 6;          // P' < 2^8 * 2^6 in fp16
 constexpr int kPagesCached = 256;   // page ids of a block's range kept in shared memory
@@ -94,25 +100,31 @@ struct DLayout {
   using SP = mma::StagedPage<D, true, true>;
   static constexpr int NBOX = D / 64;                 // 64-dim boxes
   static constexpr int BPG = NBOX / NG;               // boxes per scale group
-  static constexpr int NS = 3;                        // stages of the raw page ring
-  static constexpr int CBYTES = kPage * D * 2;        // one converted side of a page
+  static constexpr int CBYTES = kPage * D * 2;        // one converted V page
   static constexpr int PBG = 2048;                    // P' of one V group: [hi | lo][64][16 B]
   static constexpr int QBOX = 16 * 128;               // one 64-dim box of q: 16 rows x 128 B
+  static constexpr int OTHER = 2 * CBYTES + 2 * NG * PBG + NBOX * QBOX + 4 * kPage * NG * 4;
+  static constexpr int NS_FIT = (224 * 1024 - OTHER) / SP::STAGE;
+  static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;   // stages of the raw page ring
   static constexpr int RAW_OFF = 0;
-  static constexpr int KC_OFF = RAW_OFF + NS * SP::STAGE;
-  static constexpr int VC_OFF = KC_OFF + CBYTES;      // one Kc, two Vc
+  static constexpr int VC_OFF = RAW_OFF + NS * SP::STAGE;   // two Vc
   static constexpr int PB_OFF = VC_OFF + 2 * CBYTES;
   static constexpr int QB_OFF = PB_OFF + 2 * NG * PBG;
   static constexpr int KSF_OFF = QB_OFF + NBOX * QBOX;       // fp32 [2][64][NG]
   static constexpr int VSF_OFF = KSF_OFF + 2 * kPage * NG * 4;
   static constexpr int BAR_OFF = VSF_OFF + 2 * kPage * NG * 4;
   static constexpr int SMEM = 1024 + BAR_OFF + 256;
-  // tensor memory: S[2] (NG groups x 16 columns each), then O (NBOX boxes x 16)
+  // tensor memory: Ka[2] (the K tile of a page as the A operand: 64 token rows,
+  // D/2 columns of dim pairs), S[2] (NG groups x 16 columns), O (NBOX boxes x 16)
+  static constexpr int KA_COLS = D / 2;
+  static constexpr int S_COL = 2 * KA_COLS;
   static constexpr int S_COLS = NG * 16;
-  static constexpr int O_COL = 2 * S_COLS;
+  static constexpr int O_COL = S_COL + 2 * S_COLS;
   static constexpr int NEED = O_COL + NBOX * 16;
-  static constexpr int TCOLS = NEED <= 32 ? 32 : NEED <= 64 ? 64 : NEED <= 128 ? 128 : 256;
-  static_assert(QB_OFF % 1024 == 0 && KC_OFF % 1024 == 0, "swizzled tiles start on 1 KB");
+  static constexpr int TCOLS = NEED <= 64 ? 64 : NEED <= 128 ? 128 : NEED <= 256 ? 256 : 512;
+  static_assert(NS >= 2, "at least two raw stages");
+  static_assert(NEED <= 512, "tensor memory holds Ka, S and O");
+  static_assert(QB_OFF % 1024 == 0 && VC_OFF % 1024 == 0, "swizzled tiles start on 1 KB");
   static_assert(SMEM <= 232448, "one block fits the shared memory of an SM");
 };
 
@@ -170,6 +182,47 @@ struct SideChunks {
   }
 };
 
+// K rows of a staged page -> the Ka tile in tensor memory: the A operand of
+// q.K^T, 64 token rows in the M = 64 layout (row m in lane 32 (m / 16) + m % 16),
+// column c holding K indices 2c and 2c + 1.  Converter warp (quarter qd, half h)
+// takes tokens 16 qd .. 16 qd + 15 and the 64-dim boxes of its half; thread t
+// holds tokens 16 qd + t/4 and + 8 and, per box, the 16-byte chunk u = t % 4
+// (dims 16u .. 16u + 15) of both rows.  Word e of the chunk becomes columns 2u and
+// 2u + 1 of the box's 8-column block e (tcgen05.st.16x256b, the mma.sync
+// accumulator layout): K index 16e + 4u + x holds dim 16u + 4e + (0, 2, 1, 3)[x].
+template <int D>
+struct KFrag {
+  static constexpr int BOXES = D / 64 / 2;   // boxes per half
+  uint4 ra[BOXES], rb[BOXES];
+
+  __device__ __forceinline__ void load(const unsigned char* src, int qd, int h, int lane) {
+    const int rowA = 16 * qd + (lane >> 2), rowB = rowA + 8, u = lane & 3;
+#pragma unroll
+    for (int j = 0; j < BOXES; ++j) {
+      const int cc = 4 * (h * BOXES + j) + u;   // 16-byte chunk of a 128-byte row box
+      ra[j] = *reinterpret_cast<const uint4*>(src + (cc >> 3) * kBoxBytes + swz(rowA, cc & 7));
+      rb[j] = *reinterpret_cast<const uint4*>(src + (cc >> 3) * kBoxBytes + swz(rowB, cc & 7));
+    }
+  }
+  // ta: tensor-memory address of this warp's lanes at the Ka buffer's column 0
+  __device__ __forceinline__ void store(uint32_t ta, int h) const {
+#pragma unroll
+    for (int j = 0; j < BOXES; ++j) {
+      const uint32_t wa[4] = {ra[j].x, ra[j].y, ra[j].z, ra[j].w};
+      const uint32_t wb[4] = {rb[j].x, rb[j].y, rb[j].z, rb[j].w};
+      uint32_t v[16];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[4 * e + 0] = sub1152(lop_i8pair(wa[e]));
+        v[4 * e + 1] = sub1152(lop_i8pair(wa[e] >> 8));
+        v[4 * e + 2] = sub1152(lop_i8pair(wb[e]));
+        v[4 * e + 3] = sub1152(lop_i8pair(wb[e] >> 8));
+      }
+      tc::st_frag_x4(ta + (h * BOXES + j) * 32, v);
+    }
+  }
+};
+
 template <int NG>
 __device__ __forceinline__ void load_f32(const float* p, float (&x)[NG]) {
   if constexpr (NG == 4) {
@@ -198,8 +251,9 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);   // [NS] page landed
-  uint64_t* conv = full + NS;     // [2] page converted
-  uint64_t* sfull = conv + 2;     // [2] S ready
+  uint64_t* convk = full + NS;    // [2] Ka tile and scale tables written
+  uint64_t* convv = convk + 2;    // [2] Vc tile written
+  uint64_t* sfull = convv + 2;    // [2] S ready
   uint64_t* pfull = sfull + 2;    // [2] P' written
   uint64_t* ofull = pfull + 2;    // [2] P.V done
   uint64_t* empty = ofull + 2;    // [NS] staged page read into registers
@@ -223,7 +277,8 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       ptx::mbar_init(&empty[s], kConvWarps);
     }
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(&conv[s], kConvWarps);
+      ptx::mbar_init(&convk[s], kConvWarps);
+      ptx::mbar_init(&convv[s], kConvWarps);
       ptx::mbar_init(&sfull[s], 1);
       ptx::mbar_init(&pfull[s], kSoftWarps);
       ptx::mbar_init(&ofull[s], 1);
@@ -241,16 +296,28 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   const bool row_cached = a.max_pages <= kPagesCached;
   if (row_cached)
     for (int i = tid; i < a.max_pages; i += kThreads) s_pages[i] = ptx::ldg32(ptrow + i);
-  // q of the kv head's G heads -> 16 K-major rows (rows >= G zero), dims in tile order
+  // q of the kv head's G heads -> 16 K-major rows (rows >= G zero), in the K order
+  // of the Ka tile (see the converters): within a 64-dim box, K index 16e + 4u + x
+  // holds dim 16u + 4e + (0, 2, 1, 3)[x]
   for (int c = tid; c < 16 * (D / 8); c += kThreads) {
-    const int row = c / (D / 8), ch = c - row * (D / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
+    const int row = c / (D / 8), ch = c - row * (D / 8);   // 8 K indices 8ch .. 8ch + 7
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
     if (row < G) {
-      const uint4 x = ptx::ldg128(a.q + ((size_t)b * a.H + (size_t)kvh * G + row) * D + ch * 8);
-      v = make_uint4(ptx::prmt(x.x, x.y, 0x5410), ptx::prmt(x.x, x.y, 0x7632),
-                     ptx::prmt(x.z, x.w, 0x5410), ptx::prmt(x.z, x.w, 0x7632));
+      const uint16_t* qh = a.q + ((size_t)b * a.H + (size_t)kvh * G + row) * D + (ch >> 3) * 64;
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2) {
+        uint16_t hv[2];
+#pragma unroll
+        for (int z = 0; z < 2; ++z) {
+          const int kk = (ch & 7) * 8 + 2 * k2 + z;   // K index within the box
+          const int e = kk >> 4, u = (kk >> 2) & 3, x = kk & 3;
+          hv[z] = __ldg(qh + 16 * u + 4 * e + ((x == 1) ? 2 : (x == 2) ? 1 : x));
+        }
+        w[k2] = (uint32_t)hv[0] | ((uint32_t)hv[1] << 16);
+      }
     }
-    *reinterpret_cast<uint4*>(smem + LY::QB_OFF + (ch >> 3) * LY::QBOX + swz(row, ch & 7)) = v;
+    *reinterpret_cast<uint4*>(smem + LY::QB_OFF + (ch >> 3) * LY::QBOX + swz(row, ch & 7)) =
+        make_uint4(w[0], w[1], w[2], w[3]);
   }
   const int L = clamp_length(L_raw, a.max_pages, p);
   const int lo_pos = a.window > 0 ? max(0, L - a.window) : 0;
@@ -268,40 +335,59 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                       : lookup_page(ptrow, p_first + i, a.max_pages, p);
   };
 
-  if (warp == kSoftWarps + kConvWarps) {
-    // ------------------------------------------------------------- producer
-    // The whole warp runs the loop (its waits and the descriptors stay
-    // warp-uniform); one elected lane issues each copy and MMA batch.
-    if (lane == 0) {
-      ptx::prefetch_tensormap(&tmk);
-      ptx::prefetch_tensormap(&tmv);
-    }
-    auto issue = [&](int i) {
-      const int st = i % NS, page = page_of(i);
-      mma::issue_page<D, true, true, true>(smem + LY::RAW_OFF + st * SP::STAGE, &full[st],
-                                     &stage_page[st], page,
-                                     ((layer_page0 + page) * p.Hkv + kvh) * kPage, p, kvh,
-                                     &tmk, &tmv);
-    };
-    if (ptx::elect_one())
-      for (int i = 0; i < NS && i < n_pg; ++i) issue(i);
-    __syncwarp();
-    constexpr uint32_t idS = tc::idesc_f16(64, 16, 0, 0);   // A = Kc (K-major), B = q
+  if (warp == kProdK || warp == kProdV) {
+    // ----------------------------------------------------------- producers
+    // Each warp runs its loop whole (waits and descriptors stay warp-uniform);
+    // one elected lane issues each copy and MMA batch.  Warp kProdK: the page
+    // ring and S = Ka q^T; warp kProdV: O += Vc^T P'.  Their MMAs use disjoint
+    // operands, and each commit tracks its own warp's MMAs.
+    constexpr uint32_t idS = tc::idesc_f16(64, 16, 0, 0);   // A = Ka (tensor memory), B = q
     constexpr uint32_t idO = tc::idesc_f16(64, 16, 1, 1);   // A = Vc^T (MN-major), B = P'
-    const uint64_t dk = tc::sdesc(ptx::smem_u32(smem + LY::KC_OFF), 16, 1024);
-    const uint64_t dq = tc::sdesc(ptx::smem_u32(smem + LY::QB_OFF), 16, 1024);
-    const uint64_t dv = tc::sdesc(ptx::smem_u32(smem + LY::VC_OFF), 1024, 1024);
-    const uint64_t dp = tc::sdesc(ptx::smem_u32(smem + LY::PB_OFF), 128, 1024, tc::kSwizzleNone);
     bool ok = true;
-    for (int i = 0; i <= n_pg; ++i) {
-      if (i + NS < n_pg) {   // page i's codes are in registers: its stage takes page i + NS
-        ok = ok && ptx::mbar_wait(&empty[i % NS], (i / NS) & 1, kMaxPolls);
-        if (ptx::elect_one()) issue(i + NS);
+    if (warp == kProdK) {
+      if (lane == 0) {
+        ptx::prefetch_tensormap(&tmk);
+        ptx::prefetch_tensormap(&tmv);
+      }
+      auto issue = [&](int i) {
+        const int st = i % NS, page = page_of(i);
+        mma::issue_page<D, true, true, true>(smem + LY::RAW_OFF + st * SP::STAGE, &full[st],
+                                             &stage_page[st], page,
+                                             ((layer_page0 + page) * p.Hkv + kvh) * kPage, p,
+                                             kvh, &tmk, &tmv);
+      };
+      if (ptx::elect_one())
+        for (int i = 0; i < NS && i < n_pg; ++i) issue(i);
+      __syncwarp();
+      const uint64_t dq = tc::sdesc(ptx::smem_u32(smem + LY::QB_OFF), 16, 1024);
+      for (int i = 0; i < n_pg; ++i) {
+        const int bb = i & 1;
+        if (i + NS < n_pg) {   // page i's codes are in registers: its stage takes page i + NS
+          ok = ok && ptx::mbar_wait(&empty[i % NS], (i / NS) & 1, kMaxPolls);
+          if (ptx::elect_one()) issue(i + NS);
+          __syncwarp();
+        }
+        ok = ok && ptx::mbar_wait(&convk[bb], (i >> 1) & 1, kMaxPolls);
+        tc::fence_after();
+        if (ptx::elect_one()) {
+#pragma unroll
+          for (int x = 0; x < NBOX; ++x)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc::mma_ts(tbase + LY::S_COL + bb * LY::S_COLS + (x / BPG) * 16,
+                         tbase + bb * LY::KA_COLS + x * 32 + ks * 8,
+                         dq + ((x * LY::QBOX + 32 * ks) >> 4), idS, (x % BPG) != 0 || ks != 0);
+          tc::mma_commit(&sfull[bb]);
+        }
         __syncwarp();
       }
-      if (i >= 1) {     // O += V^T P' of page i - 1, as soon as its P' is written
-        const int j = i - 1, bj = j & 1;
-        ok = ok && ptx::mbar_wait(&pfull[bj], (j >> 1) & 1, kMaxPolls);
+    } else {
+      const uint64_t dv = tc::sdesc(ptx::smem_u32(smem + LY::VC_OFF), 1024, 1024);
+      const uint64_t dp = tc::sdesc(ptx::smem_u32(smem + LY::PB_OFF), 128, 1024, tc::kSwizzleNone);
+      for (int i = 0; i < n_pg; ++i) {
+        const int bb = i & 1;
+        ok = ok && ptx::mbar_wait(&convv[bb], (i >> 1) & 1, kMaxPolls);
+        ok = ok && ptx::mbar_wait(&pfull[bb], (i >> 1) & 1, kMaxPolls);
         tc::fence_after();
         if (ptx::elect_one()) {
 #pragma unroll
@@ -309,26 +395,10 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
               tc::mma_ss(tbase + LY::O_COL + x * 16,
-                         dv + ((bj * LY::CBYTES + x * kBoxBytes + 2048 * ks) >> 4),
-                         dp + (((bj * NG + x / BPG) * LY::PBG + 256 * ks) >> 4), idO,
-                         j != 0 || ks != 0);
-          tc::mma_commit(&ofull[bj]);
-        }
-        __syncwarp();
-      }
-      if (i < n_pg) {   // S[b] of page i, once it is converted
-        const int bb = i & 1;
-        ok = ok && ptx::mbar_wait(&conv[bb], (i >> 1) & 1, kMaxPolls);
-        tc::fence_after();
-        if (ptx::elect_one()) {
-#pragma unroll
-          for (int x = 0; x < NBOX; ++x)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc::mma_ss(tbase + bb * LY::S_COLS + (x / BPG) * 16,
-                         dk + ((x * kBoxBytes + 32 * ks) >> 4),
-                         dq + ((x * LY::QBOX + 32 * ks) >> 4), idS, (x % BPG) != 0 || ks != 0);
-          tc::mma_commit(&sfull[bb]);
+                         dv + ((bb * LY::CBYTES + x * kBoxBytes + 2048 * ks) >> 4),
+                         dp + (((bb * NG + x / BPG) * LY::PBG + 256 * ks) >> 4), idO,
+                         i != 0 || ks != 0);
+          tc::mma_commit(&ofull[bb]);
         }
         __syncwarp();
       }
@@ -342,8 +412,9 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       const int st = i % NS, bb = i & 1;
       ok = ok && ptx::mbar_wait(&full[st], (i / NS) & 1, kMaxPolls);
       const unsigned char* sb = smem + LY::RAW_OFF + st * SP::STAGE;
-      SideChunks<D> kw, vw;
-      kw.load(sb + SP::K_OFF, ct);
+      KFrag<D> kf;
+      SideChunks<D> vw;
+      kf.load(sb + SP::K_OFF, warp & 3, (warp - kSoftWarps) >> 2, lane);
       vw.load(sb + SP::V_OFF, ct);
       const bool page_ok = stage_page[st] >= 0;
       float kx[NG], vx[NG];   // token ct's scales (warps 4 and 5)
@@ -358,8 +429,13 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&empty[st]);   // every read of the stage is done
-      // the tables, s_valid and Vc[b] were read last by the page i - 2
-      if (i >= 2) ok = ok && ptx::mbar_wait(&ofull[bb], ((i - 2) >> 1) & 1, kMaxPolls);
+      // ---- K side (all that q.K^T and the softmax of page i need): the tables and
+      // s_valid[b] were read last by the softmax of page i - 2, Ka[b] by its q.K
+      if (i >= 2) {
+        ok = ok && ptx::mbar_wait(&pfull[bb], ((i - 2) >> 1) & 1, kMaxPolls);
+        ok = ok && ptx::mbar_wait(&sfull[bb], ((i - 2) >> 1) & 1, kMaxPolls);
+      }
+      tc::fence_after();
       if (ct < kPage) {
         const int pos = (p_first + i) * kPage + ct;
         const bool valid = page_ok && pos >= j0 && pos < j1;
@@ -382,13 +458,19 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
         }
       }
       if (ct == 0) s_valid[bb] = page_ok ? 1 : 0;
-      vw.store(smem + LY::VC_OFF + bb * LY::CBYTES, ct);
-      // Kc was read last by the q.K of page i - 1
-      if (i >= 1) ok = ok && ptx::mbar_wait(&sfull[(i - 1) & 1], ((i - 1) >> 1) & 1, kMaxPolls);
-      kw.store(smem + LY::KC_OFF, ct);
-      ptx::fence_proxy_async();   // the tiles (generic stores) are read by the tensor core
+      kf.store(tbase + ((uint32_t)((warp & 3) * 32) << 16) + bb * LY::KA_COLS,
+               (warp - kSoftWarps) >> 2);
+      tc::wait_st();
+      tc::fence_before();   // the Ka stores precede the MMA that reads them
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&conv[bb]);
+      if (lane == 0) ptx::mbar_arrive(&convk[bb]);
+      // ---- V side (only the P.V of page i needs it): Vc[b] was read last by the
+      // P.V of page i - 2
+      if (i >= 2) ok = ok && ptx::mbar_wait(&ofull[bb], ((i - 2) >> 1) & 1, kMaxPolls);
+      vw.store(smem + LY::VC_OFF + bb * LY::CBYTES, ct);
+      ptx::fence_proxy_async();   // the V tile (generic stores) is read by the tensor core
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&convv[bb]);
     }
     if (!ok) flag_error(p.err, INT8KV_DEVERR_TIMEOUT);
   } else {
@@ -409,12 +491,13 @@ decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     bool ok = true;
     for (int i = 0; i < n_pg; ++i) {
       const int bb = i & 1;
-      ok = ok && ptx::mbar_wait(&conv[bb], (i >> 1) & 1, kMaxPolls);
+      ok = ok && ptx::mbar_wait(&convk[bb], (i >> 1) & 1, kMaxPolls);
       ok = ok && ptx::mbar_wait(&sfull[bb], (i >> 1) & 1, kMaxPolls);
       tc::fence_after();
       float sg[NG][4];
 #pragma unroll
-      for (int g = 0; g < NG; ++g) tc::ld_frag(tbase + lane_off + bb * LY::S_COLS + g * 16, sg[g]);
+      for (int g = 0; g < NG; ++g)
+        tc::ld_frag(tbase + lane_off + LY::S_COL + bb * LY::S_COLS + g * 16, sg[g]);
       tc::wait_ld();
       const int t0 = warp * 16 + r, t1 = t0 + 8;             // tokens of the page
       const int pos0 = (p_first + i) * kPage + t0, pos1 = pos0 + 8;

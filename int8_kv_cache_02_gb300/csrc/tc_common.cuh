@@ -107,6 +107,18 @@ __device__ __forceinline__ void ld_frag(uint32_t ta, float (&f)[4]) {
   f[2] = __uint_as_float(v[2]);
   f[3] = __uint_as_float(v[3]);
 }
+// Four 16 x 8 blocks at columns ta, ta + 8, ta + 16, ta + 24 (first 16 lanes of
+// the warp's quarter), in the mma.sync accumulator layout: v[4i .. 4i + 3] is block
+// i's (row t/4, column 2(t%4)), (row t/4, column 2(t%4)+1), and the same for row
+// t/4 + 8.
+__device__ __forceinline__ void st_frag_x4(uint32_t ta, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(ta),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
 __device__ __forceinline__ void wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
