@@ -10,7 +10,11 @@
 //     Column n of D is column n of the allocation in both cases.
 //   - tcgen05.ld.16x256b gives a warp the 16 x 8 block of its first 16 lanes
 //     in the register layout of an mma.sync m16n8 accumulator: thread t holds
-//     rows t/4 and t/4 + 8, columns 2(t%4) and 2(t%4) + 1.
+//     rows t/4 and t/4 + 8, columns 2(t%4) and 2(t%4) + 1; tcgen05.st.16x256b
+//     writes the same block from the same registers.
+//   - An A operand read from tensor memory (kind::f16) sits in the rows of the
+//     M layout above, column c holding K elements 2c and 2c + 1; one 16-element
+//     K step is 8 columns.
 //   - 128-byte swizzle, K-major: rows of 128 B in groups of 8 (SBO = 1024 B),
 //     +32 B per 16-element K step; MN-major: 64 MN-elements per 128-byte row,
 //     +2048 B per 16 K-rows.  No swizzle, MN-major: 8 x 16-byte core matrices,
