@@ -270,14 +270,16 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
     if (!vB) s[2] = s[3] = -INFINITY;
   }
 
-  // ---- online softmax (base 2) per head column, lazy reference max
+  // ---- online softmax (base 2) per head column, lazy reference max: a lane's
+  // own scores decide whether the tile moves it; the column maxima are formed
+  // only then (rarely)
   float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-  }
   if (__any_sync(0xffffffffu, mx0 > m0 + kTau || mx1 > m1 + kTau)) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
     const float al0 = mn0 == -INFINITY ? 1.f : ptx::ex2(m0 - mn0);
     const float al1 = mn1 == -INFINITY ? 1.f : ptx::ex2(m1 - mn1);
