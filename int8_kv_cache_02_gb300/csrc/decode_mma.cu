@@ -71,6 +71,7 @@ constexpr int kThreads = kConsumerWarps * 32;
 constexpr float kTau = 8.f;                // lazy rescale: the running max moves when exceeded by > 2^8
 constexpr int kPShift = 6;                 // P' fed to the MMA as P' * 2^(6 - e) < 2^8 * 2^6 = 2^14
 constexpr int kPagesCached = 256;          // page ids of a block's range kept in shared memory
+constexpr float kCap0 = 1.17549435e-38f;   // smallest normal float: below every nonzero fp16 scale
 using mma::kPage;
 using mma::kBoxBytes;
 using mma::kMaxPolls;
@@ -318,7 +319,7 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
         va[g] = vA ? va[g] : 0.f;
         vb[g] = vB ? vb[g] : 0.f;
       }
-      need |= (va[g] > 0.f && va[g] >= cap[g]) || (vb[g] > 0.f && vb[g] >= cap[g]);
+      need |= fmaxf(va[g], vb[g]) >= cap[g];   // cap > 0: a zero scale never moves it
     }
     if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -326,7 +327,7 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
         float mx = fmaxf(va[g], vb[g]);
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        if (mx > 0.f && mx >= cap[g]) {
+        if (mx >= cap[g]) {
           const int ne = exponent_of(mx) + 1;
           if (vexp[g] != INT_MIN) {
             const float f = pow2f(vexp[g] - ne);
@@ -618,11 +619,11 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   float o[MTILES][4];
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int vexp[NG];      // per V group: 2^vexp > every V scale this warp has seen
-  float cap[NG], sh[NG];   // 2^vexp and 2^(kPShift - vexp), 0 before the first scale
+  float cap[NG], sh[NG];   // 2^vexp and 2^(kPShift - vexp); kCap0 and 0 before the first scale
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     vexp[g] = INT_MIN;
-    cap[g] = 0.f;
+    cap[g] = kCap0;
     sh[g] = 0.f;
   }
 #pragma unroll
