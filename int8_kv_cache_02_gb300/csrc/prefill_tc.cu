@@ -269,34 +269,36 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
 
   for (int i = 0; i < n_pg; ++i) {
     const int st = i % kNS;
+    bool bad = !ptx::mbar_wait(&full[st], (i / kNS) & 1, kMaxPolls);
+    unsigned char* sb = smem + LY::ST_OFF + st * SP::STAGE;
+    const int page = stage_page[st];
+    const int key0 = (p_first + i) * kPage;
+    const bool edge = key0 < j0 || key0 + kPage > j1;
+    // K side first: the K tile and table were last read by the previous page's
+    // q.K and softmax, both done, so this overlaps the previous P.V batch
+    if (!bad && page >= 0) {
+      if constexpr (KI8) convert_side<D>(sb + SP::K_OFF, smem + LY::KH_OFF);
+      if constexpr (!KI8) if (edge) zero_rows<D>(sb + SP::K_OFF, key0, j0, j1);
+      if constexpr (KI8)   // K scales times the softmax scale
+        if (tid < kPage * NG)
+          reinterpret_cast<float*>(smem + LY::KSF_OFF)[tid] =
+              __half2float(reinterpret_cast<const __half*>(sb + SP::KS_OFF)[tid]) * a.scale_log2;
+    }
     // the previous P.V batch is done: its V tile, P' columns and stage are free
-    bool bad = false;
-    if (nO > 0) bad = !ptx::mbar_wait(mO, (nO - 1) & 1, kMaxPolls);
-    bad |= !ptx::mbar_wait(&full[st], (i / kNS) & 1, kMaxPolls);
+    if (nO > 0 && !bad) bad = !ptx::mbar_wait(mO, (nO - 1) & 1, kMaxPolls);
     if (__syncthreads_or(bad)) {
       if (tid == 0) s_fail = 1;
       break;
     }
     tc_fence_after();
     if (tid == 0 && i > 0 && i - 1 + kNS < n_pg) issue(i - 1 + kNS);   // refill the freed stage
-    unsigned char* sb = smem + LY::ST_OFF + st * SP::STAGE;
-    const int page = stage_page[st];
-    const int key0 = (p_first + i) * kPage;
-    const bool edge = key0 < j0 || key0 + kPage > j1;
     if (page >= 0) {
-      if constexpr (KI8) convert_side<D>(sb + SP::K_OFF, smem + LY::KH_OFF);
       if constexpr (VI8) convert_side<D>(sb + SP::V_OFF, smem + LY::VH_OFF);
-      if constexpr (!KI8) if (edge) zero_rows<D>(sb + SP::K_OFF, key0, j0, j1);
       if constexpr (!VI8) if (edge) zero_rows<D>(sb + SP::V_OFF, key0, j0, j1);
-      // the page's scales as fp32 tables (K scales times the softmax scale)
-      if (tid < kPage * NG) {
-        if constexpr (KI8)
-          reinterpret_cast<float*>(smem + LY::KSF_OFF)[tid] =
-              __half2float(reinterpret_cast<const __half*>(sb + SP::KS_OFF)[tid]) * a.scale_log2;
-        if constexpr (VI8)
+      if constexpr (VI8)   // V scales
+        if (tid < kPage * NG)
           reinterpret_cast<float*>(smem + LY::VSF_OFF)[tid] =
               __half2float(reinterpret_cast<const __half*>(sb + SP::VS_OFF)[tid]);
-      }
       if constexpr (VI8) {
         if (warp == 0) {   // the largest V scale of each group among the keys in [j0, j1)
           const uint16_t* vs = reinterpret_cast<const uint16_t*>(sb + SP::VS_OFF);
