@@ -19,7 +19,7 @@
 // all the MMAs, and the CUDA cores are left with turning codes into fp16, the
 // softmax and P', in separate warps working on different pages.
 //
-// Measured on GB300 (128K positions, k8v8): 41.9 us against 33.8 us for the
+// Measured on GB300 (128K positions, k8v8): 41.9 us against 32.3 us for the
 // mma.sync kernel, so the library does not pick it by itself.  K reaches the
 // tensor core from tensor memory (the converters build mma-style fragments and
 // store them with tcgen05.st.16x256b), V through an fp16 tile in shared memory.

@@ -445,3 +445,28 @@ def test_many_splits_on_a_grid_larger_than_the_gpu():
     from int8_kv_cache_02_gb300 import binding
     assert binding.kv_pool_read_device_error(dev) == 0
     gu.assert_attention_close(out, _oracle(orc, 0, q, lens, pt), "combine kernel")
+
+
+@pytest.mark.parametrize("D,gs,variant", [(256, 64, 0), (128, 128, 0), (256, 128, 1), (128, 64, 2)])
+def test_every_decode_kernel_matches_the_oracle(D, gs, variant):
+    """kv_pool_set_decode_kernel: each kernel that serves the pool gives the oracle's
+    result; AUTO is the warp-level tensor-core kernel, bit for bit."""
+    from int8_kv_cache_02_gb300 import binding
+    lens = [700, 129, 64]
+    q, pt, dev, orc = _setup(600 + D + gs + variant, 3, 16, 2, D, gs, lens, variant, outliers=True)
+    ref = _oracle(orc, 0, q, lens, pt)
+    kinds = [binding.DECODE_WARP_MMA, binding.DECODE_SIMT]
+    if variant == binding.K8V8:
+        kinds.append(binding.DECODE_TCGEN05)
+    outs = {}
+    for kind in kinds:
+        dev.set_decode_kernel(kind)
+        for ns in (1, 5):
+            out = _decode(dev, 0, q, lens, pt, n_splits=ns)
+            gu.assert_attention_close(out, ref, f"kind {kind} ns {ns}")
+            outs[(kind, ns)] = out
+    dev.set_decode_kernel(binding.DECODE_AUTO)
+    for ns in (1, 5):
+        assert np.array_equal(_decode(dev, 0, q, lens, pt, n_splits=ns),
+                              outs[(binding.DECODE_WARP_MMA, ns)])
+    assert binding.kv_pool_read_device_error(dev) == 0
