@@ -322,13 +322,20 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
       need |= fmaxf(va[g], vb[g]) >= cap[g];   // cap > 0: a zero scale never moves it
     }
     if (__any_sync(0xffffffffu, need)) {
+      // the scales depend on the lane's rows only (lanes 4r .. 4r + 3 agree):
+      // the three upper xor levels give the warp's maximum, the groups' chains
+      // interleaved
+      float mx[NG];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) mx[g] = fmaxf(va[g], vb[g]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+        for (int g = 0; g < NG; ++g) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], off));
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
-        float mx = fmaxf(va[g], vb[g]);
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        if (mx >= cap[g]) {
-          const int ne = exponent_of(mx) + 1;
+        if (mx[g] >= cap[g]) {
+          const int ne = exponent_of(mx[g]) + 1;
           if (vexp[g] != INT_MIN) {
             const float f = pow2f(vexp[g] - ne);
 #pragma unroll
