@@ -711,32 +711,32 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     h1[pos(dy)] = o[j][3] * u;
   }
   __syncthreads();
-  if (threadIdx.x < 8) {   // per-head merge weights of the four warps
-    const int g = threadIdx.x;
-    float M = -INFINITY;
+  // Per-head merge weights of the four warps: f_w = 2^(m_w - M), M the block
+  // max, L = sum_w l_w f_w.
+  auto merge_weights = [&](int g, float (&f)[kConsumerWarps], float& M, float& Ls) {
+    M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w][g]);
-    float Ls = 0.f;
+    Ls = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      const float f = M == -INFINITY ? 0.f : ptx::ex2(s_m[w][g] - M);
-      s_f[w][g] = f;
-      Ls = fmaf(s_l[w][g], f, Ls);
+      f[w] = M == -INFINITY ? 0.f : ptx::ex2(s_m[w][g] - M);
+      Ls = fmaf(s_l[w][g], f[w], Ls);
     }
-    s_inv[g] = Ls;
-    s_m[0][g] = M;   // warp 0's entry is no longer needed: keep the block max there
-  }
-  __syncthreads();
+  };
 
   // ---- this block's partial (M, L, O~) of its split
   if (a.n_splits > kMaxCluster) {
     // many splits: the partial goes to the workspace and the combine kernel
     // (launched next, as a programmatic dependent) reduces the splits.
-    // Thread: 4 consecutive dims (one 16-byte store) of heads g0, g0 + stride, ...
+    // Thread: 4 consecutive dims (one 16-byte store) of heads g0, g0 + stride,
+    // ..., each head's weights formed by the thread itself.
     constexpr int TPH = D / 4;                    // threads per head row
     constexpr int HSTEP = kThreads / TPH;         // heads handled in parallel
     const int d = (threadIdx.x % TPH) * 4;
     for (int g = threadIdx.x / TPH; g < G; g += HSTEP) {
+      float f[kConsumerWarps], M, Ls;
+      merge_weights(g, f, M, Ls);
       float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
@@ -746,18 +746,27 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
           x = make_float4(row[pos(d)], row[pos(d) + 1], row[pos(d) + 2], row[pos(d) + 3]);
         else
           x = *reinterpret_cast<const float4*>(row + d);
-        const float f = s_f[w][g];
-        O.x = fmaf(x.x, f, O.x);
-        O.y = fmaf(x.y, f, O.y);
-        O.z = fmaf(x.z, f, O.z);
-        O.w = fmaf(x.w, f, O.w);
+        O.x = fmaf(x.x, f[w], O.x);
+        O.y = fmaf(x.y, f[w], O.y);
+        O.z = fmaf(x.z, f[w], O.z);
+        O.w = fmaf(x.w, f[w], O.w);
       }
       const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
       *reinterpret_cast<float4*>(a.ws.part_o + (h * a.n_splits + split) * D + d) = O;
-      if (d == 0) a.ws.part_ml[h * a.n_splits + split] = make_float2(s_m[0][g], s_inv[g]);
+      if (d == 0) a.ws.part_ml[h * a.n_splits + split] = make_float2(M, Ls);
     }
     return;
   }
+  if (threadIdx.x < 8) {
+    const int g = threadIdx.x;
+    float f[kConsumerWarps], M, Ls;
+    merge_weights(g, f, M, Ls);
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) s_f[w][g] = f[w];
+    s_inv[g] = Ls;
+    s_m[0][g] = M;   // warp 0's entry is no longer needed: keep the block max there
+  }
+  __syncthreads();
   float* cta_o = s_o + kConsumerWarps * 8 * DP;   // [8][D]
   for (int e = threadIdx.x; e < G * D; e += kThreads) {
     const int g = e / D, d = e - g * D;
