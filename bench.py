@@ -466,7 +466,9 @@ def run_ours(args, rank, world, local):
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": traffic, "algorithmic_bytes": decode_bytes(),
                      "us_per_launch": dec_s * 1e6, "kernel_src_sha": src_sha},
-        "gpu_launches": K,
+        # per step: the fused append + decode kernel, and the combine kernel when
+        # there are more than 8 splits (up to 8 combine inside the decode kernel)
+        "gpu_launches": K * (2 if st.n_splits > 8 else 1),
         "clocks": clocks,
         "cpu_baseline": cpu,
         "extra": extra,
