@@ -470,3 +470,19 @@ def test_every_decode_kernel_matches_the_oracle(D, gs, variant):
         assert np.array_equal(_decode(dev, 0, q, lens, pt, n_splits=ns),
                               outs[(binding.DECODE_WARP_MMA, ns)])
     assert binding.kv_pool_read_device_error(dev) == 0
+
+
+@pytest.mark.parametrize("row_len,n_splits", [(313, 1), (2500, 1), (2500, 4), (2048, 3)])
+def test_page_table_rows_read_with_the_length_or_per_page(row_len, n_splits):
+    """Page-table rows longer than the 256 entries a block reads whole with the length:
+    the block's page ids are read page by page, and a block whose range holds more than
+    256 pages reads the rest of them from memory when it refills.  Entries past the
+    sequence's pages are never used."""
+    from int8_kv_cache_02_gb300 import binding
+    L = 20000   # 313 pages
+    q, pt, dev, orc = _setup(1300 + row_len + n_splits, 1, 16, 2, 256, 64, [L], 0, outliers=True)
+    wide = torch.zeros((1, row_len), dtype=torch.int32)
+    wide[:, :pt.shape[1]] = pt
+    out = _decode(dev, 0, q, [L], wide, n_splits=n_splits)
+    assert binding.kv_pool_read_device_error(dev) == 0
+    gu.assert_attention_close(out, _oracle(orc, 0, q, [L], pt), f"row {row_len} ns {n_splits}")
