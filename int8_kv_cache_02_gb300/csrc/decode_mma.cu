@@ -99,6 +99,11 @@ struct Layout : mma::StagedPage<D, KI8, VI8> {
   static constexpr int BARS = NS * SP::STAGE;
   static constexpr int SMEM = 1024 + BARS + 2 * NS * 8 + NS * 4 + 64;   // stages, barriers, page ids
   static_assert(MERGE <= NS * SP::STAGE, "merge buffer must fit in the stages");
+  // Request pages 1 .. NS-1 only once page 0 has landed (see the kernel).  Only
+  // where the tile arithmetic paces the kernel (int8 K and V at head_dim 256):
+  // there the smaller first burst lets every block start computing sooner; the
+  // byte-bound variants lose more from the shallower start than they gain.
+  static constexpr bool DEFER = D == 256 && KI8 && VI8;
 };
 
 // Codes at byte k of W0 and W1 -> exact f16x2 (lo = W0's, hi = W1's).
@@ -534,12 +539,17 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   if (app_k) nk.fetch(a.k_new + ((size_t)b * p.Hkv + kvh) * D, lane);
   if (app_v) nv.fetch(a.v_new + ((size_t)b * p.Hkv + kvh) * D, lane);
 
-  // Thread 0 fills the ring with the first NS pages; afterwards the last warp
-  // to release a stage refills it with page i + NS.  When the row is not held
-  // whole, the ids of the block's first pages go to shared memory meanwhile;
-  // no barrier is needed before the refills read them: every warp writes its
-  // share before it first releases a stage (a release the refilling warp
-  // acquires), and the consumers learn of a stage's page through its mbarrier.
+  // Thread 0 requests the block's first NS pages; with LY::DEFER, the first
+  // page alone, and pages 1 .. NS-1 once it has landed: every block of the
+  // grid starts at once, so a first burst of NS pages per block makes every
+  // block's first page land late.  (A block that appends requests all NS at
+  // once: its append warps may wait on any of them before the page loop.)
+  // Afterwards the last warp to release a stage refills it with page i + NS.
+  // When the row is not held whole, the ids of the block's first pages go to
+  // shared memory meanwhile; no barrier is needed before the refills read
+  // them: every warp writes its share before it first releases a stage (a
+  // release the refilling warp acquires), and the consumers learn of a
+  // stage's page through its mbarrier.
   auto page_row = [&](int page) { return ((layer_page0 + page) * p.Hkv + kvh) * kPage; };
   if (row_cached) __syncthreads();
   auto page_direct = [&](int i) {   // page i of the block's range, from the row or from memory
@@ -553,9 +563,14 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       first[i] = i < n_pg ? page_direct(i) : -1;
 #pragma unroll
     for (int i = 0; i < LY::NS; ++i)
-      if (i < n_pg)
-        issue_page<D, KI8, VI8>(smem, full, stage_page, i, first[i], page_row(first[i]), p, kvh,
-                                &tmk, &tmv);
+      if (i < n_pg) {
+        if (i == 0 || appends || !LY::DEFER)
+          issue_page<D, KI8, VI8>(smem, full, stage_page, i, first[i], page_row(first[i]), p, kvh,
+                                  &tmk, &tmv);
+        else
+          stage_page[i] = first[i];   // kept for the request after page 0 lands; no consumer
+                                      // reads it before that request's mbarrier completes
+      }
   }
   if (!row_cached)
     for (int i = threadIdx.x; i < n_pg && i < kPagesCached; i += kThreads)
@@ -642,6 +657,15 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       if (!ptx::mbar_wait(&full[st], (i / LY::NS) & 1, kMaxPolls)) {
         flag_error(p.err, INT8KV_DEVERR_TIMEOUT);
         break;
+      }
+      if (LY::DEFER && i == 0 && !appends && threadIdx.x == 0) {   // the rest of the first NS pages
+#pragma unroll
+        for (int k = 1; k < LY::NS; ++k)
+          if (k < n_pg) {
+            const int pg = stage_page[k];
+            issue_page<D, KI8, VI8>(smem, full, stage_page, k, pg, page_row(pg), p, kvh, &tmk,
+                                    &tmv);
+          }
       }
       const int page = stage_page[st];
       const int tile0 = (p_first + i) * kPage + warp * 16;   // position of the tile's token 0
