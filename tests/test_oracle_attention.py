@@ -154,3 +154,18 @@ def test_combine_skips_empty_splits_and_matches_two_key_closed_form():
     v0, v1 = np.array([4.0, 0.0]), np.array([0.0, 8.0])
     parts = [(0.0, 1.0, v0), (-math.inf, 0.0, np.zeros(2)), (math.log(3), 1.0, v1)]
     assert np.allclose(oatt.combine(parts), [1.0, 6.0], rtol=0, atol=1e-15)
+
+
+def test_default_scale_is_inverse_sqrt_head_dim():
+    """head_dim 4, two keys: q.k = 0 and 2, so with the default scale 1/sqrt(4) the
+    scores are 0 and 1 and the weights are 1 - sigmoid(1) and sigmoid(1), where
+    sigmoid(1) = 0.7310585786300049 (the logistic function at 1)."""
+    kh = np.zeros((2, 1, 4))
+    kh[1, 0, 0] = 2.0
+    vh = np.zeros((2, 1, 4))
+    vh[0, 0, 0] = 1.0
+    vh[1, 0, 1] = 1.0
+    q = np.array([[1, 0, 0, 0]], np.float16)
+    o = oatt.decode(q, kh, vh, 2)
+    sig1 = 0.7310585786300049
+    assert np.allclose(o[0], [1.0 - sig1, sig1, 0.0, 0.0], rtol=0, atol=1e-15)

@@ -1,8 +1,10 @@
-"""The quantization pins catch plausible mistakes planted in the oracle (CPU only).
+"""The oracle's pins catch plausible mistakes planted in the oracle (CPU only).
 
-Each case swaps one numpy routine the oracle's quantizer uses for a wrong one
-(round-half-away instead of half-even, truncated scale, asymmetric clamp) and
-checks that the exhaustive brute-force pins of test_oracle_quant now fail.
+Quantization: each case swaps one numpy routine the oracle's quantizer uses for
+a wrong one (round-half-away instead of half-even, truncated scale, asymmetric
+clamp) and checks that the exhaustive brute-force pins of test_oracle_quant
+now fail.  Attention: each case replaces one oracle function with a copy that
+carries one mistake and checks that a pin of test_oracle_attention fails.
 """
 
 import numpy as np
@@ -65,3 +67,112 @@ def test_truncated_scale_is_caught(monkeypatch):
 
     monkeypatch.setattr(q, "group_scales", truncated)
     assert not _scale_pin_holds()
+
+
+# --------------------------------------------------------------------------------------
+# Attention: each case plants one plausible mistake in the oracle's attention (a
+# dropped term, a wrong sign or index, a transposed operand, a bound off by one)
+# and checks that one of the pins of test_oracle_attention now fails.
+
+import functools  # noqa: E402
+import math  # noqa: E402
+
+import oracle.attention as oatt  # noqa: E402
+from tests import test_oracle_attention as pins  # noqa: E402
+
+
+def _decode_mutant(q16, khat, vhat, length, window=0, scale=None, *, interleaved=False,
+                   lo_shift=0, normalise=True, k_is_v=False, sign=1.0, drop_scale=False):
+    """The oracle's decode with one knob turned."""
+    q = np.asarray(q16, np.float16).astype(np.float64)
+    H, D = q.shape
+    Hkv = khat.shape[1]
+    G = H // Hkv
+    sc = (1.0 if drop_scale else 1.0 / math.sqrt(D)) if scale is None else float(scale)
+    lo = max(0, length - window + lo_shift) if window > 0 else 0
+    keys = vhat if k_is_v else khat
+    out = np.zeros((H, D), np.float64)
+    for h in range(H):
+        kvh = h % Hkv if interleaved else h // G
+        z = sign * sc * (keys[lo:length, kvh, :] @ q[h])
+        if z.shape[0] == 0:
+            continue
+        p = np.exp(z - np.max(z))
+        o = p @ vhat[lo:length, kvh, :]
+        out[h] = o / np.sum(p) if normalise else o
+    return out
+
+
+def _fails(pin, *args):
+    try:
+        pin(*args)
+    except AssertionError:
+        return True
+    return False
+
+
+@pytest.mark.parametrize("knob,pin", [
+    (dict(), None),                                        # the unmutated copy passes them all
+    (dict(drop_scale=True), pins.test_default_scale_is_inverse_sqrt_head_dim),
+    (dict(interleaved=True), pins.test_context_one_returns_dequantized_v_row_and_gqa_mapping),
+    (dict(lo_shift=1), pins.test_window_keeps_exactly_the_last_w_positions),
+    (dict(lo_shift=-1), pins.test_window_keeps_exactly_the_last_w_positions),
+    (dict(normalise=False), pins.test_identical_keys_return_mean_of_v),
+    (dict(k_is_v=True), pins.test_dominant_key_selects_its_value),
+    (dict(sign=-1.0), pins.test_dominant_key_selects_its_value),
+])
+def test_decode_mistakes_are_caught(monkeypatch, knob, pin):
+    monkeypatch.setattr(oatt, "decode", functools.partial(_decode_mutant, **knob))
+    if pin is None:
+        for p in (pins.test_default_scale_is_inverse_sqrt_head_dim,
+                  pins.test_context_one_returns_dequantized_v_row_and_gqa_mapping,
+                  pins.test_window_keeps_exactly_the_last_w_positions,
+                  pins.test_identical_keys_return_mean_of_v,
+                  pins.test_dominant_key_selects_its_value,
+                  pins.test_golden_two_keys_hand_computed):
+            p()
+    else:
+        assert _fails(pin)
+
+
+def test_combine_without_rescale_is_caught(monkeypatch):
+    def combine_no_rescale(partials):
+        live = [(m, l, o) for (m, l, o) in partials if l > 0.0]
+        M = max(m for m, _, _ in live)
+        Lsum = sum(l * math.exp(m - M) for m, l, _ in live)
+        return sum(o for _, _, o in live) / Lsum          # o~_s not brought to the common max
+    monkeypatch.setattr(oatt, "combine", combine_no_rescale)
+    assert _fails(pins.test_combine_skips_empty_splits_and_matches_two_key_closed_form)
+    assert _fails(pins.test_split_equals_single_pass, 4, 300, 0)
+
+
+def test_split_bounds_rounding_down_is_caught(monkeypatch):
+    def floor_bounds(lo, hi, n_splits, page_size):
+        if hi <= lo:
+            return [(lo, lo)] * n_splits
+        p0 = lo // page_size
+        per = ((hi - 1) // page_size + 1 - p0) // n_splits * page_size   # floor: drops the tail
+        return [(max(lo, p0 * page_size + s * per), max(max(lo, p0 * page_size + s * per),
+                                                          min(hi, p0 * page_size + (s + 1) * per)))
+                for s in range(n_splits)]
+    monkeypatch.setattr(oatt, "split_bounds", floor_bounds)
+    assert _fails(pins.test_split_bounds_cover_the_range_once)
+
+
+def test_prefill_without_the_current_position_is_caught(monkeypatch):
+    def prefill_short(q16, khat, vhat, start, scale=None):
+        q = np.asarray(q16, np.float16).astype(np.float64)
+        n_new, H, D = q.shape
+        G = H // khat.shape[1]
+        sc = 1.0 / math.sqrt(D) if scale is None else float(scale)
+        out = np.zeros((n_new, H, D), np.float64)
+        for kvh in range(khat.shape[1]):
+            heads = slice(kvh * G, (kvh + 1) * G)
+            for i in range(n_new):
+                n_vis = start + i                               # the query's own key left out
+                z = sc * (q[i, heads, :] @ khat[:n_vis, kvh, :].T)
+                p = np.exp(z - np.max(z, axis=1, keepdims=True))
+                out[i, heads, :] = (p @ vhat[:n_vis, kvh, :]) / np.sum(p, axis=1, keepdims=True)
+        return out
+    monkeypatch.setattr(oatt, "prefill_chunk", prefill_short)
+    assert _fails(pins.test_prefill_row_equals_decode_at_its_length_and_is_causal)
