@@ -215,6 +215,32 @@ int attn_decode_append_int8(const int8kv_pool* pool, int layer, const uint16_t* 
                             int max_pages_per_seq, int window, float softmax_scale, int n_splits,
                             float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Decode of a window of q_len queries per sequence, causal within the window:
+ * the verify windows of speculative decoding (Strata pull request #2698, "What
+ * it does", third bullet: the MTP block and its verify windows go through the
+ * same dequantizing decode kernels).  Query i of sequence b sits at position
+ * seq_lens[b] - q_len + i and attends keys 0 .. seq_lens[b] - q_len + i of the
+ * pool: append the window's K/V with kv_quant_append first.
+ *   q            device fp16 [batch][q_len][n_heads][head_dim]
+ *   out          device fp32 [batch][q_len][n_heads][head_dim]; a query at a
+ *                negative position gets a zero row
+ *   q_len        1 .. 64 (1 is attn_decode_int8 without a window)
+ *   workspace    >= attn_decode_workspace_bytes(batch * q_len, n_heads, ...,
+ *                n_splits), 16-byte aligned, any contents
+ *   n_splits     0 -> attn_decode_n_splits(pool, batch * ceil(q_len * G / 8),
+ *                longest context of the page table); else as attn_decode_int8
+ * The (query, head) pairs of a kv head take the 8 columns of the tensor-core
+ * products, eight per block: q_len * G <= 8 reads each page once per split,
+ * more reads it once per group of eight pairs.  Served by the warp-level
+ * tensor-core kernel only (page_size 64, head_dim 128/256, group_size >= 64, a
+ * multiple of 64); other pools return UNSUPPORTED.  No sliding window.
+ * Errors: NULL_PTR, INVALID_ARG, UNSUPPORTED, WORKSPACE, ALIGNMENT, CUDA. */
+int attn_decode_multi_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int batch,
+                           int q_len, int n_heads, const int32_t* seq_lens,
+                           const int32_t* page_table, int max_pages_per_seq, float softmax_scale,
+                           int n_splits, float* out, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
 /* Blocks of the prefill-chunk kernel per (128-row query tile, kv head).  The
  * kernel runs one block per SM at a time, so tiles x kv heads x splits blocks
  * take ceil(blocks / SMs) waves of ceil(pages / splits) pages; the count with

@@ -8,6 +8,7 @@ raises if it has not been built (``int8_kv_cache_02_gb300.build.build()``).
 
 from .binding import (K8V8, K8V16, K16V8, VARIANTS, Int8KVError, KVPool,  # noqa: F401
                       attn_decode_append_int8, attn_decode_int8, attn_decode_int8_noalloc,
+                      attn_decode_multi_int8,
                       attn_decode_n_splits,
                       attn_decode_workspace_bytes, attn_prefill_chunk_int8, attn_prefill_n_splits,
                       attn_prefill_workspace_bytes,

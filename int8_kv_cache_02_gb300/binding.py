@@ -38,6 +38,8 @@ _SIGS = {
     "attn_decode_append_int8": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp,
                                          _c_int, _c_int, _c_float, _c_int, _vp, _vp, _c_size,
                                          _vp]),
+    "attn_decode_multi_int8": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _c_int, _vp, _vp,
+                                        _c_int, _c_float, _c_int, _vp, _vp, _c_size, _vp]),
     "attn_prefill_n_splits": (_c_int, [_vp, _c_int, _c_int, _c_int]),
     "attn_prefill_workspace_bytes": (_c_int, [_c_int] * 5 + [ctypes.POINTER(_c_size)]),
     "attn_prefill_chunk_int8": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _c_int, _vp, _c_int,
@@ -196,6 +198,24 @@ def attn_decode_append_int8(pool, layer, q, k_new, v_new, seq_lens, page_table, 
                                          page_table.shape[1], window, float(softmax_scale),
                                          n_splits, _dev(out, torch.float32, "out"), ws, nbytes,
                                          _stream(stream)), "attn_decode_append_int8")
+
+
+def attn_decode_multi_int8(pool, layer, q, seq_lens, page_table, out, workspace=None,
+                           softmax_scale=0.0, n_splits=0, stream=None):
+    """Decode of a window of queries per sequence, causal within the window.
+
+    q: fp16 [B][q_len][H][D]; query i of sequence b sits at position
+    seq_lens[b] - q_len + i.  out: fp32 [B][q_len][H][D].  The workspace is sized
+    by attn_decode_workspace_bytes(B * q_len, H, ...)."""
+    B, Q, H = q.shape[0], q.shape[1], q.shape[2]
+    ws = _dev(workspace, torch.uint8, "workspace") if workspace is not None else None
+    nbytes = workspace.numel() if workspace is not None else 0
+    _check(lib().attn_decode_multi_int8(pool.handle, layer, _dev(q, torch.float16, "q"), B, Q, H,
+                                        _dev(seq_lens, torch.int32, "seq_lens"),
+                                        _dev(page_table, torch.int32, "page_table"),
+                                        page_table.shape[1], float(softmax_scale), n_splits,
+                                        _dev(out, torch.float32, "out"), ws, nbytes,
+                                        _stream(stream)), "attn_decode_multi_int8")
 
 
 def attn_prefill_n_splits(pool, n_new, n_heads, start_pos):

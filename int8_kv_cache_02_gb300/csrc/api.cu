@@ -287,8 +287,8 @@ int attn_decode_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head
 }
 
 static int decode_entry(const int8kv_pool* pool, int layer, const uint16_t* q,
-                        const uint16_t* k_new, const uint16_t* v_new, int batch, int n_heads,
-                        const int32_t* seq_lens, const int32_t* page_table,
+                        const uint16_t* k_new, const uint16_t* v_new, int batch, int q_len,
+                        int n_heads, const int32_t* seq_lens, const int32_t* page_table,
                         int max_pages_per_seq, int window, float softmax_scale, int n_splits,
                         float* out, void* workspace, size_t workspace_bytes, void* stream);
 
@@ -296,8 +296,18 @@ int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int 
                      int n_heads, const int32_t* seq_lens, const int32_t* page_table,
                      int max_pages_per_seq, int window, float softmax_scale, int n_splits,
                      float* out, void* workspace, size_t workspace_bytes, void* stream) {
-  return decode_entry(pool, layer, q, nullptr, nullptr, batch, n_heads, seq_lens, page_table,
-                      max_pages_per_seq, window, softmax_scale, n_splits, out, workspace,
+  return decode_entry(pool, layer, q, nullptr, nullptr, batch, 1, n_heads, seq_lens,
+                      page_table, max_pages_per_seq, window, softmax_scale, n_splits, out,
+                      workspace, workspace_bytes, stream);
+}
+
+int attn_decode_multi_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int batch,
+                           int q_len, int n_heads, const int32_t* seq_lens,
+                           const int32_t* page_table, int max_pages_per_seq, float softmax_scale,
+                           int n_splits, float* out, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  return decode_entry(pool, layer, q, nullptr, nullptr, batch, q_len, n_heads, seq_lens,
+                      page_table, max_pages_per_seq, 0, softmax_scale, n_splits, out, workspace,
                       workspace_bytes, stream);
 }
 
@@ -308,36 +318,42 @@ int attn_decode_append_int8(const int8kv_pool* pool, int layer, const uint16_t* 
                             float* out, void* workspace, size_t workspace_bytes, void* stream) {
   if (batch > 0 && (!k_new || !v_new)) return INT8KV_ERR_NULL_PTR;
   if (!aligned16(k_new) || !aligned16(v_new)) return INT8KV_ERR_ALIGNMENT;
-  return decode_entry(pool, layer, q, k_new, v_new, batch, n_heads, seq_lens, page_table,
+  return decode_entry(pool, layer, q, k_new, v_new, batch, 1, n_heads, seq_lens, page_table,
                       max_pages_per_seq, window, softmax_scale, n_splits, out, workspace,
                       workspace_bytes, stream);
 }
 
 static int decode_entry(const int8kv_pool* pool, int layer, const uint16_t* q,
-                        const uint16_t* k_new, const uint16_t* v_new, int batch, int n_heads,
-                        const int32_t* seq_lens, const int32_t* page_table,
+                        const uint16_t* k_new, const uint16_t* v_new, int batch, int q_len,
+                        int n_heads, const int32_t* seq_lens, const int32_t* page_table,
                         int max_pages_per_seq, int window, float softmax_scale, int n_splits,
                         float* out, void* workspace, size_t workspace_bytes, void* stream) {
   if (!pool) return INT8KV_ERR_NULL_PTR;
   if (layer < 0 || layer >= pool->n_layers || batch < 0 || n_heads <= 0 ||
       max_pages_per_seq <= 0 || window < 0 || n_splits < 0 || n_splits > kMaxSplits ||
-      !std::isfinite(softmax_scale))
+      q_len < 1 || q_len > kMaxQueryWindow || !std::isfinite(softmax_scale))
     return INT8KV_ERR_INVALID_ARG;
   if (n_heads % pool->n_kv_heads != 0) return INT8KV_ERR_INVALID_ARG;
   const int G = n_heads / pool->n_kv_heads;
   if (G > 8) return INT8KV_ERR_UNSUPPORTED;
+  // a query window runs on the warp-level tensor-core kernel only
+  if (q_len > 1 && decode_kernel_for(pool, G) != INT8KV_DECODE_WARP_MMA)
+    return INT8KV_ERR_UNSUPPORTED;
   if (batch == 0) return INT8KV_OK;
   if (!q || !seq_lens || !page_table || !out) return INT8KV_ERR_NULL_PTR;
   if (!aligned16(q) || !aligned16(out)) return INT8KV_ERR_ALIGNMENT;
+  const int n_cg = (q_len * G + 7) / 8;   // blocks per (sequence, kv head) sharing the columns
   if (n_splits == 0) {
     int ctx = max_pages_per_seq * pool->page_size;
     if (window > 0 && window + pool->page_size < ctx) ctx = window + pool->page_size;
-    n_splits = attn_decode_n_splits(pool, batch, ctx);
+    n_splits = attn_decode_n_splits(pool, batch * n_cg, ctx);
     if (n_splits < 0) return n_splits;
   }
   DecodeArgs a;
-  const size_t need = decode_workspace_layout(batch, n_heads, pool->n_kv_heads, pool->head_dim,
-                                              n_splits, &a.ws, workspace);
+  a.q_len = q_len;
+  a.n_cg = n_cg;
+  const size_t need = decode_workspace_layout(batch * q_len, n_heads, pool->n_kv_heads,
+                                              pool->head_dim, n_splits, &a.ws, workspace);
   if (need > 0) {
     if (!workspace || workspace_bytes < need) return INT8KV_ERR_WORKSPACE;
     if (!aligned16(workspace)) return INT8KV_ERR_ALIGNMENT;
@@ -501,7 +517,9 @@ cudaError_t launch_decode(const int8kv_pool* pool, int layer, const DecodeArgs& 
     e = launch_decode_simt(a, k8, v8, stream);
     if (e != cudaSuccess || a.n_splits == 1) return e;
   }
-  return launch_decode_combine(a, stream);
+  DecodeArgs c = a;   // the combine's rows: [B][q_len][H]
+  c.B = a.B * a.q_len;
+  return launch_decode_combine(c, stream);
 }
 
 }  // namespace int8kv

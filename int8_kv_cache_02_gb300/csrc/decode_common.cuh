@@ -9,6 +9,7 @@
 namespace int8kv {
 
 constexpr int kMaxSplits = 256;
+constexpr int kMaxQueryWindow = 64;   // queries per sequence of one attn_decode_multi_int8 call
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

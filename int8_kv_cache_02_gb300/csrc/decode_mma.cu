@@ -82,6 +82,15 @@ using mma::exponent_of;
 
 __device__ __forceinline__ int rho(int r) { return (0x37156240u >> (4 * r)) & 0xF; }
 
+// The block's column group (grid y = kv head + Hkv * column group), read from
+// the special register at each use so that it holds no register across the
+// page loop.
+__device__ __forceinline__ int column_group(int Hkv) {
+  int y;
+  asm volatile("mov.u32 %0, %%ctaid.y;" : "=r"(y));
+  return y / Hkv;
+}
+
 template <int D, bool KI8, bool VI8>
 struct Layout : mma::StagedPage<D, KI8, VI8> {
   using SP = mma::StagedPage<D, KI8, VI8>;
@@ -203,7 +212,7 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
                                             int j0, int j1, const uint32_t (&qf)[D / 16][2],
                                             float scale_log2, float (&o)[D / 16][4], float& m0,
                                             float& m1, float& l0, float& l1, float (&cap)[NG],
-                                            float (&sh)[NG], int (&vexp)[NG]) {
+                                            float (&sh)[NG], int (&vexp)[NG], int lim0, int lim1) {
   using LY = Layout<D, KI8, VI8>;
   constexpr int MACROS = D / 64, MTILES = D / 16;
   constexpr int NGV = VI8 ? NG : 1;
@@ -271,9 +280,12 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
 #pragma unroll
     for (int k = 0; k < 4; ++k) s[k] *= scale_log2;
   }
-  if constexpr (!FULL) {
-    if (!vA) s[0] = s[1] = -INFINITY;
-    if (!vB) s[2] = s[3] = -INFINITY;
+  if constexpr (!FULL) {   // outside [j0, j1), or after the column's query position
+    const int pA = tile0 + rowA, pB = tile0 + rowB;
+    if (!vA || pA > lim0) s[0] = -INFINITY;
+    if (!vA || pA > lim1) s[1] = -INFINITY;
+    if (!vB || pB > lim0) s[2] = -INFINITY;
+    if (!vB || pB > lim1) s[3] = -INFINITY;
   }
 
   // ---- online softmax (base 2) per head column, lazy reference max: a lane's
@@ -438,7 +450,10 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
   }
 }
 
-template <int D, bool KI8, bool VI8, int NG>
+// WIN: a window of q_len queries per sequence (attn_decode_multi_int8); without
+// it the kernel serves one query per sequence and none of the window's column
+// arithmetic is compiled in.
+template <int D, bool KI8, bool VI8, int NG, bool WIN>
 __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 3)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, int layer_page0) {
@@ -454,14 +469,24 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   __shared__ float s_f[kConsumerWarps][8], s_inv[8];
   __shared__ float s_cm[8][8], s_cl[8][8], s_cL[8];
   __shared__ int s_rel[4];                // per stage: release tickets (the last warp refills)
+  __shared__ int s_q0[kConsumerWarps];   // WIN: L - q_len, the first query's position
   // page ids: the sequence's whole page-table row when it has at most
   // kPagesCached entries, else the entries of the block's first pages
   __shared__ int s_pages[kPagesCached];
 
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const PoolView& p = a.pool;
+  const int split = blockIdx.x, kvh = blockIdx.y % p.Hkv, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G;
+  // B operand column c <-> (query, head) pair colg * 8 + c of the kv head's
+  // q_len * G (colg: the block's column group); with one query (decode) column
+  // c is head c.  Live columns: c < ncol().
+  auto ncol = [&]() { return WIN ? min(8, a.q_len * G - column_group(p.Hkv) * 8) : G; };
+  auto col_row = [&](int c) -> size_t {   // the column's row of q and out: [B][q_len][H]
+    if constexpr (!WIN) return (size_t)b * a.H + (size_t)kvh * G + c;
+    const int f = column_group(p.Hkv) * 8 + c;
+    return ((size_t)b * a.q_len + f / G) * a.H + (size_t)kvh * G + f % G;
+  };
   constexpr int gs = D / NG;   // width of a scale group (>= 64)
 
   if (threadIdx.x == 0) {
@@ -501,8 +526,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   constexpr int QV = D / 64 * 2;   // 16-byte pieces of q a lane holds
   uint4 qraw[QV];
   {
-    const bool live = r < G;
-    const uint16_t* qh = a.q + ((size_t)b * a.H + (size_t)kvh * G + (live ? r : 0)) * D;
+    const bool live = r < ncol();
+    const uint16_t* qh = a.q + col_row(live ? r : 0) * D;
 #pragma unroll
     for (int v = 0; v < QV; ++v) {
       // int8 K: dims 64mc + 16t + 8h (v = 2mc + h); fp16 K: dims 16ks + 2t (+8), see below
@@ -521,6 +546,13 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   }
   const int L = clamp_length(L_raw, a.max_pages, p);
   const int lo_pos = a.window > 0 ? max(0, L - a.window) : 0;
+  // Query i of a window sits at L - q_len + i and sees keys up to it.  The
+  // first query's position is kept in shared memory (one copy per warp, read
+  // only by the warp), so that the page loop holds no register for it.
+  if constexpr (WIN) {
+    if (lane == 0) s_q0[warp] = L - a.q_len;
+    __syncwarp();
+  }
   int j0, j1;
   split_range(lo_pos, L, split, a.n_splits, kPage, &j0, &j1);
   const int p_first = j0 / kPage;
@@ -671,12 +703,22 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       const int tile0 = (p_first + i) * kPage + warp * 16;   // position of the tile's token 0
       if (page >= 0 && tile0 < j1 && tile0 + 16 > j0) {
         const unsigned char* sb = smem + st * LY::STAGE;
-        if (tile0 >= j0 && tile0 + 16 <= j1)
+        // a tile that ends by the first query's position needs no per-column test
+        if (tile0 >= j0 && tile0 + 16 <= j1 && (!WIN || tile0 + 16 <= s_q0[warp] + 1)) {
           decode_tile<D, KI8, VI8, NG, true>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
-                                             m0, m1, l0, l1, cap, sh, vexp);
-        else
+                                             m0, m1, l0, l1, cap, sh, vexp, 0, 0);
+        } else if constexpr (!WIN) {
           decode_tile<D, KI8, VI8, NG, false>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
-                                              m0, m1, l0, l1, cap, sh, vexp);
+                                              m0, m1, l0, l1, cap, sh, vexp, INT_MAX, INT_MAX);
+        } else {
+          // causal limits of the lane's columns 2t, 2t + 1 (a dead column: L - 1)
+          const int q0 = s_q0[warp], c0 = 2 * (lane & 3), nc = ncol();
+          auto lim = [&](int c) {
+            return c < nc ? q0 + (column_group(p.Hkv) * 8 + c) / G : q0 + a.q_len - 1;
+          };
+          decode_tile<D, KI8, VI8, NG, false>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
+                                              m0, m1, l0, l1, cap, sh, vexp, lim(c0), lim(c0 + 1));
+        }
       }
       __syncwarp();   // every lane of this warp is done reading stage st
       if (lane == 0) {
@@ -758,7 +800,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     constexpr int TPH = D / 4;                    // threads per head row
     constexpr int HSTEP = kThreads / TPH;         // heads handled in parallel
     const int d = (threadIdx.x % TPH) * 4;
-    for (int g = threadIdx.x / TPH; g < G; g += HSTEP) {
+    const int nc = ncol();
+    for (int g = threadIdx.x / TPH; g < nc; g += HSTEP) {   // g: the column
       float f[kConsumerWarps], M, Ls;
       merge_weights(g, f, M, Ls);
       float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -775,7 +818,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
         O.z = fmaf(x.z, f[w], O.z);
         O.w = fmaf(x.w, f[w], O.w);
       }
-      const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
+      const size_t h = col_row(g);
       *reinterpret_cast<float4*>(a.ws.part_o + (h * a.n_splits + split) * D + d) = O;
       if (d == 0) a.ws.part_ml[h * a.n_splits + split] = make_float2(M, Ls);
     }
@@ -792,7 +835,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   }
   __syncthreads();
   float* cta_o = s_o + kConsumerWarps * 8 * DP;   // [8][D]
-  for (int e = threadIdx.x; e < G * D; e += kThreads) {
+  const int nc = ncol();
+  for (int e = threadIdx.x; e < nc * D; e += kThreads) {
     const int g = e / D, d = e - g * D;
     float O = 0.f;
 #pragma unroll
@@ -827,7 +871,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   }
   __syncthreads();
   const int slice = (D + CS - 1) / CS, d0 = rank * slice;   // CS need not divide D
-  for (int e = threadIdx.x; e < G * slice; e += kThreads) {
+  for (int e = threadIdx.x; e < nc * slice; e += kThreads) {
     const int g = e / slice, d = d0 + (e - g * slice);
     if (d >= D) continue;
     float v[kMaxCluster];
@@ -838,18 +882,18 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
 #pragma unroll
     for (int j = 0; j < kMaxCluster; ++j)
       if (j < CS) O = fmaf(s_cm[j][g], v[j], O);
-    const size_t h = (size_t)b * a.H + (size_t)kvh * G + g;
+    const size_t h = col_row(g);
     const float Ls = s_cL[g];
     a.out[h * D + d] = Ls > 0.f ? O / Ls : 0.f;
   }
   cluster.sync();   // no block leaves while others read its shared memory
 }
 
-template <int D, bool KI8, bool VI8, int NG>
+template <int D, bool KI8, bool VI8, int NG, bool WIN>
 cudaError_t launch_typed(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                          int layer_page0, cudaStream_t stream) {
   using LY = Layout<D, KI8, VI8>;
-  auto kern = decode_mma_kernel<D, KI8, VI8, NG>;
+  auto kern = decode_mma_kernel<D, KI8, VI8, NG, WIN>;
   static bool configured[64] = {};   // per device: the attribute belongs to the device's function
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -860,7 +904,7 @@ cudaError_t launch_typed(const DecodeArgs& a, const CUtensorMap& tmk, const CUte
     if (dev < 64) configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_splits, a.pool.Hkv, a.B);
+  cfg.gridDim = dim3(a.n_splits, a.pool.Hkv * a.n_cg, a.B);   // y: kv head + Hkv * column group
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = LY::SMEM;
   cfg.stream = stream;
@@ -885,35 +929,43 @@ bool decode_mma_supported(const PoolView& p, int G) {
   return G <= 8 && p.ps == kPage && (p.D == 128 || p.D == 256) && p.gs >= 64 && p.gs % 64 == 0;
 }
 
-template <int D, bool KI8, bool VI8>
+template <int D, bool KI8, bool VI8, bool WIN>
 cudaError_t launch_ng(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                       int layer_page0, cudaStream_t stream) {
   switch (a.pool.ng) {
-    case 1: return launch_typed<D, KI8, VI8, 1>(a, tmk, tmv, layer_page0, stream);
-    case 2: return launch_typed<D, KI8, VI8, 2>(a, tmk, tmv, layer_page0, stream);
+    case 1: return launch_typed<D, KI8, VI8, 1, WIN>(a, tmk, tmv, layer_page0, stream);
+    case 2: return launch_typed<D, KI8, VI8, 2, WIN>(a, tmk, tmv, layer_page0, stream);
     case 4:
-      if constexpr (D == 256) return launch_typed<D, KI8, VI8, 4>(a, tmk, tmv, layer_page0, stream);
+      if constexpr (D == 256)
+        return launch_typed<D, KI8, VI8, 4, WIN>(a, tmk, tmv, layer_page0, stream);
       return cudaErrorNotSupported;
     default: return cudaErrorNotSupported;
   }
 }
 
+template <int D, bool KI8, bool VI8>
+cudaError_t launch_win(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                       int layer_page0, cudaStream_t stream) {
+  return a.q_len > 1 ? launch_ng<D, KI8, VI8, true>(a, tmk, tmv, layer_page0, stream)
+                     : launch_ng<D, KI8, VI8, false>(a, tmk, tmv, layer_page0, stream);
+}
+
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool k8, bool v8, const CUtensorMap& tmk,
                               const CUtensorMap& tmv, int layer_page0, cudaStream_t stream) {
   if (a.pool.D == 256) {
-    if (k8 && v8) return launch_ng<256, true, true>(a, tmk, tmv, layer_page0, stream);
-    if (k8) return launch_ng<256, true, false>(a, tmk, tmv, layer_page0, stream);
-    return launch_ng<256, false, true>(a, tmk, tmv, layer_page0, stream);
+    if (k8 && v8) return launch_win<256, true, true>(a, tmk, tmv, layer_page0, stream);
+    if (k8) return launch_win<256, true, false>(a, tmk, tmv, layer_page0, stream);
+    return launch_win<256, false, true>(a, tmk, tmv, layer_page0, stream);
   }
-  if (k8 && v8) return launch_ng<128, true, true>(a, tmk, tmv, layer_page0, stream);
-  if (k8) return launch_ng<128, true, false>(a, tmk, tmv, layer_page0, stream);
-  return launch_ng<128, false, true>(a, tmk, tmv, layer_page0, stream);
+  if (k8 && v8) return launch_win<128, true, true>(a, tmk, tmv, layer_page0, stream);
+  if (k8) return launch_win<128, true, false>(a, tmk, tmv, layer_page0, stream);
+  return launch_win<128, false, true>(a, tmk, tmv, layer_page0, stream);
 }
 
 template <int D, bool KI8, bool VI8, int NG>
 int resident_typed() {
   using LY = Layout<D, KI8, VI8>;
-  auto kern = decode_mma_kernel<D, KI8, VI8, NG>;
+  auto kern = decode_mma_kernel<D, KI8, VI8, NG, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM) !=
       cudaSuccess)
     return 0;

@@ -78,6 +78,12 @@ struct DecodeArgs {
   DecodeWorkspace ws;
   int B, H, G, max_pages, window, n_splits;
   float scale_log2;         // softmax_scale * log2(e)
+  // Queries per sequence (1: decode; > 1: a verify window, query i at position
+  // seq_lens[b] - q_len + i, q and out [B][q_len][H][D]) and the blocks per
+  // (sequence, kv head) that share its q_len * G (query, head) columns, eight
+  // each (grid y = kv head + Hkv * column group).  Only the warp-level
+  // tensor-core kernel serves q_len > 1.
+  int q_len = 1, n_cg = 1;
 };
 
 struct PrefillArgs {

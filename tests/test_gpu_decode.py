@@ -486,3 +486,59 @@ def test_page_table_rows_read_with_the_length_or_per_page(row_len, n_splits):
     out = _decode(dev, 0, q, [L], wide, n_splits=n_splits)
     assert binding.kv_pool_read_device_error(dev) == 0
     gu.assert_attention_close(out, _oracle(orc, 0, q, [L], pt), f"row {row_len} ns {n_splits}")
+
+
+# --------------------------------------------------------------------------------------
+# Query windows (attn_decode_multi_int8): q_len queries per sequence, causal within the
+# window; the oracle is decode at each query's own length (a pinned prefill row).
+
+@pytest.mark.parametrize("D,gs,variant,H,Hkv,q_len,n_splits", [
+    (256, 64, 0, 16, 2, 1, 0),     # q_len 1: attn_decode_int8, bit for bit
+    (256, 64, 0, 16, 2, 2, 0),     # G 8 x 2 queries: two column groups
+    (256, 64, 0, 8, 2, 2, 4),      # G 4 x 2 queries: the 8 columns of one block
+    (128, 128, 1, 8, 4, 4, 13),    # G 2 x 4 queries; fp16 V; the combine kernel
+    (256, 64, 2, 16, 4, 3, 1),     # G 4 x 3 = 12 columns: groups of 8 and 4; fp16 K; one split
+    (128, 64, 0, 32, 8, 4, 5),     # G 4 x 4: two column groups; a cluster of 5 splits
+])
+def test_query_window_matches_the_oracle(D, gs, variant, H, Hkv, q_len, n_splits):
+    from int8_kv_cache_02_gb300 import binding
+    lens = [700, 129, 3]           # the last: fewer positions than queries
+    B = len(lens)
+    q0, pt, dev, orc = _setup(1400 + D + q_len + variant, B, H, Hkv, D, gs, lens, variant,
+                              outliers=True)
+    g = torch.Generator().manual_seed(1450 + q_len)
+    q = inputs.normal_f16((B, q_len, H, D), g)
+    ns = n_splits or binding.attn_decode_n_splits(dev, B * (-(-q_len * (H // Hkv) // 8)),
+                                                  pt.shape[1] * 64)
+    ws = dev.decode_workspace(B * q_len, H, ns)
+    out = torch.full((B, q_len, H, D), float("nan"), dtype=torch.float32, device="cuda")
+    binding.attn_decode_multi_int8(dev, 0, q.cuda(), torch.tensor(lens, dtype=torch.int32,
+                                                                   device="cuda"),
+                                   pt.cuda(), out, ws, n_splits=ns)
+    torch.cuda.synchronize()
+    assert binding.kv_pool_read_device_error(dev) == 0
+    got = out.cpu().numpy()
+    ref = np.zeros((B, q_len, H, D))
+    for b, L in enumerate(lens):
+        kh, vh = orc.gather(0, pt[b].numpy(), L)
+        for i in range(q_len):
+            pos = L - q_len + i
+            if pos >= 0:
+                ref[b, i] = oatt.decode(q[b, i].numpy(), kh, vh, pos + 1)
+    gu.assert_attention_close(got.reshape(B * q_len, H, D), ref.reshape(B * q_len, H, D),
+                              f"window {q_len}")
+    if q_len == 1:
+        single = _decode(dev, 0, q[:, 0], lens, pt, n_splits=ns)
+        assert np.array_equal(got[:, 0], single)
+
+
+def test_query_window_needs_the_tensor_core_kernel():
+    from int8_kv_cache_02_gb300 import binding
+    q0, pt, dev, orc = _setup(1490, 1, 8, 2, 64, 64, [100], 0)     # head_dim 64: CUDA-core kernel
+    q = torch.zeros((1, 2, 8, 64), dtype=torch.float16, device="cuda")
+    out = torch.zeros((1, 2, 8, 64), dtype=torch.float32, device="cuda")
+    with pytest.raises(binding.Int8KVError) as e:
+        binding.attn_decode_multi_int8(dev, 0, q, torch.tensor([100], dtype=torch.int32,
+                                                                device="cuda"),
+                                       pt.cuda(), out, dev.decode_workspace(2, 8, 4), n_splits=4)
+    assert e.value.status == -6
