@@ -85,6 +85,8 @@ def test_decode_and_append_reject_null_pool(L):
     assert L.attn_decode_int8(None, 0, None, 1, 8, None, None, 1, 0, ctypes.c_float(0), 0, None,
                               None, 0, None) == -2
     assert L.kv_quant_append(None, 0, None, None, 1, 1, None, None, 1, None) == -2
+    assert L.attn_decode_multi_int8(None, 0, None, 1, 2, 8, None, None, 1, ctypes.c_float(0), 0,
+                                    None, None, 0, None) == -2
 
 
 def test_workspace_bytes(L):
