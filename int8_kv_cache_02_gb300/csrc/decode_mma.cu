@@ -47,6 +47,12 @@
 //          +1 (row r+8).  V fp16: ldmatrix.trans, dims d0 + r and d0 + 8 + r.
 // RHO = (0,4,2,6,5,1,7,3) makes both the q.K^T and P.V loads conflict free and
 // lines the transposed fragment up with the P.V slots.
+//
+// Query windows (WIN, attn_decode_multi_int8; Strata pull request #2698, "What
+// it does": the verify windows of speculative decoding go through the decode
+// kernels): the 8 columns are (query, head) pairs instead of heads, query i of
+// a window of q_len at position L - q_len + i; a tile after the window's first
+// position masks each column's keys beyond its query.
 
 #include <climits>
 
