@@ -22,6 +22,9 @@
  *  3. attn_prefill_chunk_int8: causal attention of a chunk of new queries over
  *     the same int8 cache (Strata #2698: the prompt chunk dequantizes on the
  *     fly; genie-ai-runtime v1.3.1: a fused query-tiled kernel for chunks).
+ *  4. attn_decode_multi_int8: decode of a window of queries per sequence,
+ *     causal within the window (Strata #2698 "What it does": the verify
+ *     windows of speculative decoding go through the decode kernels).
  *
  * Store variants (Strata #2698 "What it does": k8v8, and one-store variants):
  *     INT8KV_K8V8  K and V int8 with scales
