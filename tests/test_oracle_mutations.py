@@ -176,3 +176,48 @@ def test_prefill_without_the_current_position_is_caught(monkeypatch):
         return out
     monkeypatch.setattr(oatt, "prefill_chunk", prefill_short)
     assert _fails(pins.test_prefill_row_equals_decode_at_its_length_and_is_causal)
+
+
+# ---- pool image: a layout mistake planted in the oracle's save must fail a pin
+def _image_pins_hold():
+    from tests import test_oracle_image as t
+    try:
+        t.test_image_matches_the_hand_assembled_bytes()
+        t.test_sections_are_position_major_with_their_scales()
+    except AssertionError:
+        return False
+    return True
+
+
+def test_image_pins_hold_unmutated():
+    assert _image_pins_hold()
+
+
+def test_head_major_image_is_caught(monkeypatch):
+    import oracle.image as im
+    real_rows = im._rows
+
+    def swapped_save(pool, lengths, page_table):
+        parts = []
+        for b, L in enumerate(int(x) for x in lengths):
+            pages, slots = real_rows(pool, page_table[b], L)
+            for layer in range(pool.n_layers):
+                for _, region, nbytes in im._sections(pool, L):
+                    rows = np.ascontiguousarray(region[layer, pages, :, slots, :].swapaxes(0, 1))
+                    raw = rows.tobytes()
+                    parts.append(raw + bytes(im._pad16(nbytes) - nbytes))
+        payload = b"".join(parts)
+        lens = np.asarray(lengths, "<i4").tobytes()
+        head = im.HEADER.pack(im.MAGIC, im.VERSION, pool.variant, pool.n_layers, pool.n_kv_heads,
+                              pool.head_dim, pool.gs, len(lengths), len(payload), 0)
+        return head + lens + bytes(im._pad16(len(lens)) - len(lens)) + payload
+
+    monkeypatch.setattr(im, "save", swapped_save)
+    assert not _image_pins_hold()
+
+
+def test_image_without_scales_is_caught(monkeypatch):
+    import oracle.image as im
+    real = im._sections
+    monkeypatch.setattr(im, "_sections", lambda pool, L: real(pool, L)[:2])
+    assert not _image_pins_hold()
