@@ -61,8 +61,11 @@ def decode(q16, khat, vhat, length, window=0, scale=None):
     out = np.zeros((H, D), np.float64)
     for h in range(H):
         kvh = h // G
-        z = sc * (khat[lo:length, kvh, :] @ q[h])
-        out[h] = _softmax_weighted(z, vhat[lo:length, kvh, :])
+        if h % G == 0:   # the visible keys and values of this kv head, as rows
+            kh = np.ascontiguousarray(khat[lo:length, kvh, :])
+            vh = np.ascontiguousarray(vhat[lo:length, kvh, :])
+        z = sc * (kh @ q[h])
+        out[h] = _softmax_weighted(z, vh)
     return out
 
 
