@@ -76,6 +76,11 @@ extern "C" {
 #define INT8KV_ERR_UNSUPPORTED   -6  /* a shape the kernels are not built for (see each call) */
 #define INT8KV_ERR_CUDA          -7  /* a CUDA runtime call or launch failed */
 #define INT8KV_ERR_WORKSPACE     -8  /* workspace NULL or smaller than the *_workspace_bytes query */
+#define INT8KV_ERR_FORMAT        -9  /* a pool image that is not format 3, or that was saved from a
+                                        pool of another variant or shape */
+
+/* Format version of the images kv_pool_save writes and kv_pool_load reads. */
+#define INT8KV_IMAGE_VERSION      3
 
 /* Bits of the device error word. */
 #define INT8KV_DEVERR_PAGE_ID     1  /* page-table entry outside [0, n_pages) */
@@ -104,7 +109,13 @@ int int8kv_pool_region_bytes(int n_layers, int n_kv_heads, int head_dim, int gro
                              int page_size, int n_pages, int variant, int region,
                              size_t* out_bytes);
 
-/* Create a pool descriptor over caller-allocated device regions.
+/* Create a pool descriptor over caller-allocated device regions: codes in one
+ * region, their fp16 scales in a separate one (genie-ai-runtime release
+ * v0.1.0-alpha.12, "Path I series" I1: a separate scales region beside the
+ * int8 pool; Strata #2698 "What it does": K and V stores that can each be int8
+ * or fp16; genie-ai-runtime v1.2.1, "Bugs fixed", first item: the position
+ * stride of a cached slot comes from the cache's own layout, never from the
+ * query's head_dim).
  *   head_dim    64, 128 or 256
  *   group_size  values per scale: head_dim (one scale per (position, kv head))
  *               or 16/32/64/128 dividing head_dim (64 = Strata's grouping)
@@ -139,41 +150,46 @@ int kv_quant_append(const int8kv_pool* pool, int layer, const uint16_t* k_new,
 /* Decode kernels, for kv_pool_set_decode_kernel. */
 #define INT8KV_DECODE_AUTO      0  /* the library's choice (the default) */
 #define INT8KV_DECODE_WARP_MMA  1  /* warp-level tensor-core kernel (mma.sync): fused append,
-                                      up to 8 splits combined in the kernel */
-#define INT8KV_DECODE_TCGEN05   2  /* tensor-memory kernel (tcgen05.mma; K, S and O in
-                                      tensor memory; converter, softmax and producer
-                                      warps); int8 K and V only; the combine kernel reduces
-                                      its splits.  Slower than WARP_MMA on GB300 at every
-                                      measured size: never picked by AUTO */
-#define INT8KV_DECODE_SIMT      3  /* CUDA-core kernel: any shape the pool takes */
+                                      splits combined inside the kernel */
+#define INT8KV_DECODE_SIMT      3  /* CUDA-core kernel: any shape the pool takes; a combine
+                                      kernel reduces its splits */
 
 /* Choose the kernel that serves this pool's decode calls (attn_decode_int8,
- * attn_decode_append_int8, attn_decode_n_splits).  All kernels compute the same
+ * attn_decode_append_int8, attn_decode_n_splits).  Both kernels compute the same
  * result within the attention tolerance; the choice is for tuning and testing.
- * WARP_MMA and TCGEN05 need page_size 64, head_dim 128 or 256 and
- * group_size >= 64 (TCGEN05 also the K8V8 variant); a call whose
- * n_heads / n_kv_heads exceeds 8 uses SIMT whatever the choice.
+ * WARP_MMA needs page_size 64, head_dim 128 or 256 and group_size >= 64; a call
+ * whose n_heads / n_kv_heads exceeds 8 uses SIMT whatever the choice.  The
+ * split-K scheme both follow is genie-ai-runtime v1.3.0, "split-K decode
+ * attention" (a partial per split, combined per head).
  * Errors: NULL_PTR, INVALID_ARG (unknown kind), UNSUPPORTED (the kernel does not
- * serve the pool's shape or variant). */
+ * serve the pool's shape). */
 int kv_pool_set_decode_kernel(int8kv_pool* pool, int kind);
 
 /* Splits the library picks when attn_decode_int8 gets n_splits = 0, for a
- * batch of `batch` sequences of at most max_ctx positions on this pool.  The
- * (sequence, kv head, split) blocks run in waves of as many blocks as the
- * pool's decode kernel keeps resident on the pool's device (queried once per
- * pool and kernel);
- * the count with the shortest chain of waves x (pages per block + 1), plus 2
- * when the splits need combining, is returned: at least 1, at most the pages
- * of max_ctx and 256.
+ * batch of `batch` sequences of at most max_ctx positions on this pool
+ * (genie-ai-runtime v1.3.0, "split-K decode attention": the key range of each
+ * head is cut into n_splits pieces so that short batches fill the GPU; there
+ * the count was fixed, here it is sized to the GPU).  The (sequence, kv head,
+ * split) blocks run in waves of as many blocks as the pool's decode kernel
+ * keeps resident on the pool's device (queried once per pool and kernel); the
+ * count with the shortest chain of waves x (pages per block + 1), plus 2 when
+ * the splits need combining, is returned: at least 1, at most the pages of
+ * max_ctx and 256.
  * Returns >= 1, or a negative status (NULL_PTR, INVALID_ARG). */
 int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx);
 
-/* Workspace bytes attn_decode_int8 needs for this shape (0 when n_splits == 1).
- * Errors: INVALID_ARG. */
+/* Workspace bytes attn_decode_int8 needs for this shape (0 when n_splits == 1):
+ * the split partials of genie-ai-runtime v1.3.0 "split-K decode attention"
+ * ((m, l, o) per split and head).  Errors: INVALID_ARG. */
 int attn_decode_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_dim,
                                 int n_splits, size_t* out_bytes);
 
-/* Split-K GQA decode attention over the int8 cache of one layer.
+/* Split-K GQA decode attention over the int8 cache of one layer
+ * (genie-ai-runtime v1.3.0, "split-K decode attention" and its "Details": a
+ * partial per split with its own running max and sum, combined per head; the
+ * split ranges come from the length in device memory; optional sliding
+ * window), dequantizing each cached row with its own scale as it is loaded
+ * (release v0.1.0-alpha.12, "Path I series" I3; Strata #2698 "What it does").
  *   q            device fp16 [batch][n_heads][head_dim]
  *   seq_lens     device int32 [batch]: keys 0..L-1 of sequence b are attended
  *                (read on the device, so a captured graph can be replayed as
@@ -188,13 +204,13 @@ int attn_decode_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head
  *                [s*P/n_splits, (s+1)*P/n_splits) (integer division: the
  *                counts differ by at most one), clipped to [lo, L)
  *   out          device fp32 [batch][n_heads][head_dim]
- *   workspace    device, >= attn_decode_workspace_bytes, 16-byte aligned, any
+ * *   workspace    device, >= attn_decode_workspace_bytes, 16-byte aligned, any
  *                contents (every partial a call reads, it writes first).  Calls
  *                sharing one workspace must not overlap on the device.
  * With the warp-level tensor-core kernel, up to 8 splits are combined inside
  * the decode kernel (the splits of a (sequence, kv head) form one thread-block
  * cluster and reduce through distributed shared memory); with more, or with the
- * other kernels, a combine kernel follows on the stream.
+ * CUDA-core kernel, a combine kernel follows on the stream.
  * n_heads must be a multiple of n_kv_heads with n_heads / n_kv_heads <= 8.
  * Errors: NULL_PTR, INVALID_ARG, UNSUPPORTED, WORKSPACE, CAPACITY, CUDA. */
 int attn_decode_int8(const int8kv_pool* pool, int layer, const uint16_t* q, int batch,
@@ -252,7 +268,9 @@ int attn_decode_multi_int8(const int8kv_pool* pool, int layer, const uint16_t* q
  * >= 1, or NULL_PTR, INVALID_ARG, UNSUPPORTED. */
 int attn_prefill_n_splits(const int8kv_pool* pool, int n_new, int n_heads, int start_pos);
 
-/* Workspace bytes attn_prefill_chunk_int8 needs (0 when n_splits == 1). */
+/* Workspace bytes attn_prefill_chunk_int8 needs (0 when n_splits == 1): the
+ * split partials of the chunk's (query, head) rows, combined per row as in
+ * genie-ai-runtime v1.3.0 "split-K decode attention". */
 int attn_prefill_workspace_bytes(int n_new, int n_heads, int n_kv_heads, int head_dim,
                                  int n_splits, size_t* out_bytes);
 
@@ -290,15 +308,86 @@ int attn_prefill_chunk_int8(const int8kv_pool* pool, int layer, const uint16_t* 
  *   - Every call on a device shares the one scratch and leaves its contents
  *     there; nothing in it has to start at zero.  Calls that overlap on the GPU
  *     (other streams, other host threads) race on the scratch: serialise them.
- *   - A shape whose workspace (attn_decode_workspace_bytes) exceeds 4 MiB is
- *     rejected with INT8KV_ERR_CAPACITY; lower n_splits or the batch.
+ *   - n_splits = 0 takes the count attn_decode_int8 would pick (same window and
+ *     batch); when that count's workspace would exceed the scratch, the best
+ *     count among those whose workspace fits is taken instead.
+ *   - An explicit n_splits whose workspace (attn_decode_workspace_bytes)
+ *     exceeds 4 MiB is rejected with INT8KV_ERR_CAPACITY; lower n_splits or
+ *     the batch.
  * The source pages have no counterpart of this call.
+ * The cached scratch address assumes the device's primary context lives as
+ * long as the process.
  * Errors: those of attn_decode_int8, and CAPACITY, INVALID_ARG (pool not on the
  * current device), CUDA. */
 int attn_decode_int8_noalloc(const int8kv_pool* pool, int layer, const uint16_t* q, int batch,
                              int n_heads, const int32_t* seq_lens, const int32_t* page_table,
                              int max_pages_per_seq, int window, float softmax_scale,
                              int n_splits, float* out, void* stream);
+
+/* ---- saved pool images ------------------------------------------------
+ * The used positions 0 .. L_b - 1 of each sequence, every layer, with the int8
+ * codes AND their scales (genie-ai-runtime release v0.1.0-alpha.12, "Path F
+ * (#45) interop guard": the persistent-KV format v2 carried the int8 bytes
+ * without the scales attention needs when the cache is hydrated again, so int8
+ * saves had to be skipped; format v3 (#67) persists the scales region.
+ * Release v0.1.0-alpha.11, "--int8-kv triage": save/load must persist the
+ * scales, or refuse caches whose int8 setting differs.  The alpha.10 Path F
+ * table, F3b: a save packs only the used tokens).  Layout (little-endian,
+ * every section 16-byte aligned and zero-padded):
+ *   header, 48 bytes: "I8KV", u32 version (3), u32 variant, u32 n_layers,
+ *     u32 n_kv_heads, u32 head_dim, u32 group_size, u32 n_seqs,
+ *     u64 payload bytes, u64 0
+ *   lengths: int32 [n_seqs], padded to 16 bytes
+ *   payload: per sequence, per layer: K store [L][n_kv_heads][head_dim], V
+ *     store [L][n_kv_heads][head_dim] (int8 codes or fp16 values), then the
+ *     scales [L][n_kv_heads][head_dim / group_size] fp16 of each int8 store.
+ * The payload is position-major: an image does not depend on the page size or
+ * the physical pages of the pool it came from, and loads into any pool of the
+ * same variant, n_layers, n_kv_heads, head_dim and group_size. */
+
+/* Bytes of the image of n_seqs sequences of these lengths (host int32
+ * [n_seqs]).  Errors: NULL_PTR, INVALID_ARG (a negative length). */
+int kv_pool_image_bytes(const int8kv_pool* pool, int n_seqs, const int32_t* seq_lens,
+                        size_t* out_bytes);
+
+/* Save the image of positions 0 .. seq_lens[b] - 1 of every layer of each
+ * sequence into `image` (host memory, >= kv_pool_image_bytes).
+ *   seq_lens    host int32 [n_seqs]
+ *   page_table  device int32 [n_seqs][max_pages_per_seq] of the pool
+ *   staging     device, 16-byte aligned, >= kv_pool_image_bytes: the image is
+ *               assembled there by a gather kernel and copied to `image`
+ * Waits for `stream` before returning (the image is complete).  Page-table
+ * entries outside the pool are flagged in the device error word and their rows
+ * left zero.  Errors: NULL_PTR, INVALID_ARG, ALIGNMENT, CAPACITY (image or
+ * staging too small, a length beyond its page-table row), CUDA. */
+int kv_pool_save(const int8kv_pool* pool, int n_seqs, const int32_t* seq_lens,
+                 const int32_t* page_table, int max_pages_per_seq, void* staging,
+                 size_t staging_bytes, void* image, size_t image_bytes, void* stream);
+
+/* Load an image (host memory) into the pool through page_table (device int32
+ * [n_seqs][max_pages_per_seq]; the pages may differ from those it was saved
+ * from, and so may the page size) and write the sequences' lengths to
+ * seq_lens (host int32 [n_seqs]).  staging: device, 16-byte aligned, >= the
+ * image's bytes.  Waits for `stream` before returning.  An image of another
+ * format version (such as one without scales), variant, n_layers, n_kv_heads,
+ * head_dim, group_size or sequence count is refused with INT8KV_ERR_FORMAT and
+ * nothing is written.  Errors: NULL_PTR, INVALID_ARG, ALIGNMENT, FORMAT,
+ * CAPACITY (staging too small, a length beyond its page-table row), CUDA. */
+int kv_pool_load(const int8kv_pool* pool, const void* image, size_t image_bytes, int n_seqs,
+                 const int32_t* page_table, int max_pages_per_seq, void* staging,
+                 size_t staging_bytes, int32_t* seq_lens, void* stream);
+
+/* Diagnostic for the device-side timeout report (genie-ai-runtime release
+ * v0.1.0-alpha.11, "--int8-kv triage": a path that fell back silently ended in
+ * a hang; here every wait on an asynchronous copy is bounded and its expiry is
+ * reported instead).  With max_polls > 0, the pool's later decode calls on the
+ * warp-level tensor-core kernel issue no page copies at all and arm each stage
+ * barrier for 16 bytes that never arrive, so every wait gives up after
+ * max_polls polls, sets INT8KV_DEVERR_TIMEOUT in the device error word and the
+ * call completes (its output is not meaningful).  No copy is in flight when a
+ * block gives up.  0 restores normal operation.  Errors: NULL_PTR, UNSUPPORTED
+ * (the pool's decode calls do not run on the warp-level kernel). */
+int kv_pool_test_expire_waits(int8kv_pool* pool, uint32_t max_polls);
 
 /* Copy the pool's device error word into *out (host) and clear it.  Blocks
  * until `stream` has finished.  Errors: NULL_PTR (no word given), CUDA. */

@@ -21,7 +21,8 @@ K8V8, K8V16, K16V8 = 0, 1, 2
 VARIANTS = {"k8v8": K8V8, "k8v16": K8V16, "k16v8": K16V8}
 REGION_K_STORE, REGION_V_STORE, REGION_K_SCALES, REGION_V_SCALES = 0, 1, 2, 3
 DEVERR_PAGE_ID, DEVERR_LENGTH, DEVERR_TIMEOUT = 1, 2, 4
-DECODE_AUTO, DECODE_WARP_MMA, DECODE_TCGEN05, DECODE_SIMT = 0, 1, 2, 3
+ERR_FORMAT = -9
+DECODE_AUTO, DECODE_WARP_MMA, DECODE_SIMT = 0, 1, 3
 
 _c_int, _c_size, _vp, _c_float = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
 _SIGS = {
@@ -47,6 +48,10 @@ _SIGS = {
     "attn_decode_int8_noalloc": (_c_int, [_vp, _c_int, _vp, _c_int, _c_int, _vp, _vp, _c_int,
                                           _c_int, _c_float, _c_int, _vp, _vp]),
     "kv_pool_set_decode_kernel": (_c_int, [_vp, _c_int]),
+    "kv_pool_image_bytes": (_c_int, [_vp, _c_int, _vp, ctypes.POINTER(_c_size)]),
+    "kv_pool_test_expire_waits": (_c_int, [_vp, ctypes.c_uint32]),
+    "kv_pool_save": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _vp, _c_size, _vp, _c_size, _vp]),
+    "kv_pool_load": (_c_int, [_vp, _vp, _c_size, _c_int, _vp, _c_int, _vp, _c_size, _vp, _vp]),
 }
 
 _lib = None
@@ -159,7 +164,7 @@ def attn_decode_workspace_bytes(batch, n_heads, n_kv_heads, head_dim, n_splits):
 def attn_decode_int8(pool, layer, q, seq_lens, page_table, out, workspace=None, window=0,
                      softmax_scale=0.0, n_splits=0, stream=None):
     """q fp16 [B][H][D]; seq_lens int32 [B]; page_table int32 [B][max_pages];
-    out fp32 [B][H][D]; workspace uint8 tensor (zero-filled once) or None."""
+    out fp32 [B][H][D]; workspace uint8 tensor (any contents) or None."""
     B, H = q.shape[0], q.shape[1]
     ws = _dev(workspace, torch.uint8, "workspace") if workspace is not None else None
     nbytes = workspace.numel() if workspace is not None else 0
@@ -246,8 +251,63 @@ def attn_prefill_chunk_int8(pool, layer, q, start_pos, page_table, out, workspac
 
 
 def kv_pool_set_decode_kernel(pool, kind):
-    """kind: DECODE_AUTO, DECODE_WARP_MMA, DECODE_TCGEN05 or DECODE_SIMT."""
+    """kind: DECODE_AUTO, DECODE_WARP_MMA or DECODE_SIMT."""
     _check(lib().kv_pool_set_decode_kernel(pool.handle, int(kind)), "kv_pool_set_decode_kernel")
+
+
+def _host_lens(seq_lens):
+    lens = torch.as_tensor(seq_lens, dtype=torch.int32).cpu().contiguous()
+    return lens, ctypes.c_void_p(lens.data_ptr())
+
+
+def kv_pool_image_bytes(pool, seq_lens):
+    """Bytes of the saved image of sequences of these lengths (a host sequence)."""
+    lens, lp = _host_lens(seq_lens)
+    out = _c_size(0)
+    _check(lib().kv_pool_image_bytes(pool.handle, lens.numel(), lp, ctypes.byref(out)),
+           "kv_pool_image_bytes")
+    return out.value
+
+
+def kv_pool_save(pool, seq_lens, page_table, staging=None, stream=None):
+    """The saved image (bytes) of positions 0..L_b-1 of every layer of each sequence.
+    seq_lens: host lengths; page_table: int32 [n_seqs][max_pages] on the device;
+    staging: a device uint8 tensor of at least the image's bytes (allocated here
+    when None)."""
+    lens, lp = _host_lens(seq_lens)
+    n = kv_pool_image_bytes(pool, lens)
+    if staging is None:
+        staging = torch.empty(max(n, 16), dtype=torch.uint8, device=page_table.device)
+    host = torch.empty(max(n, 1), dtype=torch.uint8)
+    _check(lib().kv_pool_save(pool.handle, lens.numel(), lp,
+                              _dev(page_table, torch.int32, "page_table"), page_table.shape[1],
+                              _dev(staging, torch.uint8, "staging"), staging.numel(),
+                              ctypes.c_void_p(host.data_ptr()), host.numel(), _stream(stream)),
+           "kv_pool_save")
+    return bytes(host[:n].numpy())
+
+
+def kv_pool_load(pool, image, page_table, staging=None, stream=None):
+    """Load a saved image into the pool through page_table (int32 [n_seqs][max_pages]
+    on the device); returns the sequences' lengths."""
+    n_seqs = page_table.shape[0]
+    buf = torch.frombuffer(bytearray(image), dtype=torch.uint8) if len(image) else \
+        torch.zeros(1, dtype=torch.uint8)
+    if staging is None:
+        staging = torch.empty(max(len(image), 16), dtype=torch.uint8, device=page_table.device)
+    lens = torch.zeros(max(n_seqs, 1), dtype=torch.int32)
+    _check(lib().kv_pool_load(pool.handle, ctypes.c_void_p(buf.data_ptr()), len(image), n_seqs,
+                              _dev(page_table, torch.int32, "page_table"), page_table.shape[1],
+                              _dev(staging, torch.uint8, "staging"), staging.numel(),
+                              ctypes.c_void_p(lens.data_ptr()), _stream(stream)), "kv_pool_load")
+    return lens[:n_seqs].tolist()
+
+
+def kv_pool_test_expire_waits(pool, max_polls):
+    """Diagnostic: later decode calls arm their copy waits so that they expire after
+    max_polls polls and report INT8KV_DEVERR_TIMEOUT (0 switches it off)."""
+    _check(lib().kv_pool_test_expire_waits(pool.handle, int(max_polls)),
+           "kv_pool_test_expire_waits")
 
 
 def kv_pool_read_device_error(pool, stream=None):

@@ -107,6 +107,60 @@ size_t decode_workspace_layout(int B, int H, int Hkv, int D, int n_splits, Decod
   return o_bytes + ml_bytes;
 }
 
+// Blocks of the pool's decode kernel resident at once on its device (queried
+// once per pool and kernel).  The CUDA-core kernel is taken as three per SM.
+static void query_residency(const int8kv_pool* pool, int kind) {
+  int8kv_pool* mp = const_cast<int8kv_pool*>(pool);
+  if (pool->resident[kind] != 0) return;
+  int n = 0;
+  if (kind == INT8KV_DECODE_WARP_MMA) {
+    int prev = -1;
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != pool->device) cudaSetDevice(pool->device);
+    n = decode_mma_resident_blocks(pool->head_dim, pool->k_int8, pool->v_int8, pool->n_groups);
+    if (prev >= 0 && prev != pool->device) cudaSetDevice(prev);
+  }
+  mp->resident[kind] = n > 0 ? n : 3 * pool->num_sms;
+}
+
+int decode_splits_heuristic(const int8kv_pool* pool, long long units, int max_ctx, int max_splits) {
+  const int kind = decode_kernel_for(pool, 1);
+  query_residency(pool, kind);
+  // units x splits blocks run in ceil(blocks / resident) waves, each as long as
+  // a block's ceil(pages / splits) pages plus about one page of prologue and
+  // epilogue; more than one split adds the combine (about two pages).  Take the
+  // split count with the shortest chain (the smallest on a tie).
+  const int ps = pool->page_size;
+  const int pages = max_ctx > 0 ? (max_ctx + ps - 1) / ps : 1;
+  int top = pages < kMaxSplits ? pages : kMaxSplits;
+  if (max_splits < top) top = max_splits;
+  const long long resident = pool->resident[kind];
+  long long best = -1;
+  int n = 1;
+  for (int s = 1; s <= top; ++s) {
+    const long long waves = (units * s + resident - 1) / resident;
+    const long long cost = waves * ((pages + s - 1) / s + 1) + (s > 1 ? 2 : 0);
+    if (best < 0 || cost < best) {
+      best = cost;
+      n = s;
+    }
+  }
+  return n;
+}
+
+int decode_auto_splits(const int8kv_pool* pool, int batch, int q_len, int G, int max_pages,
+                       int window, size_t max_workspace) {
+  const int n_cg = (q_len * G + 7) / 8;   // blocks per (sequence, kv head) sharing the columns
+  int ctx = max_pages * pool->page_size;
+  if (window > 0 && window + pool->page_size < ctx) ctx = window + pool->page_size;
+  int top = kMaxSplits;
+  if (max_workspace > 0)
+    while (top > 1 && decode_workspace_layout(batch * q_len, G * pool->n_kv_heads,
+                                              pool->n_kv_heads, pool->head_dim, top, nullptr,
+                                              nullptr) > max_workspace)
+      --top;
+  return decode_splits_heuristic(pool, (long long)batch * n_cg * pool->n_kv_heads, ctx, top);
+}
+
 }  // namespace int8kv
 
 extern "C" {
@@ -122,6 +176,7 @@ const char* int8kv_status_string(int status) {
     case INT8KV_ERR_UNSUPPORTED: return "shape not supported by the kernels";
     case INT8KV_ERR_CUDA: return "CUDA runtime error";
     case INT8KV_ERR_WORKSPACE: return "workspace missing or too small";
+    case INT8KV_ERR_FORMAT: return "pool image of another format version, variant or shape";
     default: return "unknown status";
   }
 }
@@ -189,6 +244,7 @@ int kv_pool_create(int8kv_pool** out, int n_layers, int n_kv_heads, int head_dim
   p->has_tmaps = false;
   p->decode_kernel = INT8KV_DECODE_AUTO;
   for (int k = 0; k < 4; ++k) p->resident[k] = 0;
+  p->expire_polls = 0;
   if (page_size == 64 && (head_dim == 128 || head_dim == 256)) {
     const size_t rows = (size_t)n_layers * n_pages * n_kv_heads * page_size;
     if (rows >= (1ull << 31) || !make_store_map(&p->tmap_k, k_store, k8, head_dim, rows) ||
@@ -221,12 +277,10 @@ int kv_quant_append(const int8kv_pool* pool, int layer, const uint16_t* k_new,
 
 int kv_pool_set_decode_kernel(int8kv_pool* pool, int kind) {
   if (!pool) return INT8KV_ERR_NULL_PTR;
-  if (kind < INT8KV_DECODE_AUTO || kind > INT8KV_DECODE_SIMT) return INT8KV_ERR_INVALID_ARG;
+  if (kind != INT8KV_DECODE_AUTO && kind != INT8KV_DECODE_WARP_MMA && kind != INT8KV_DECODE_SIMT)
+    return INT8KV_ERR_INVALID_ARG;
   const PoolView v = layer_view(pool, 0);
   if (kind == INT8KV_DECODE_WARP_MMA && !(pool->has_tmaps && decode_mma_supported(v, 1)))
-    return INT8KV_ERR_UNSUPPORTED;
-  if (kind == INT8KV_DECODE_TCGEN05 &&
-      !(pool->has_tmaps && decode_tc_supported(v, pool->k_int8, pool->v_int8, 1)))
     return INT8KV_ERR_UNSUPPORTED;
   pool->decode_kernel = kind;
   return INT8KV_OK;
@@ -235,44 +289,7 @@ int kv_pool_set_decode_kernel(int8kv_pool* pool, int kind) {
 int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx) {
   if (!pool) return INT8KV_ERR_NULL_PTR;
   if (batch <= 0 || max_ctx < 0) return INT8KV_ERR_INVALID_ARG;
-  const int kind = decode_kernel_for(pool, 1);
-  if (pool->resident[kind] == 0) {
-    // Blocks the pool's decode kernel keeps resident at once (queried once);
-    // the CUDA-core kernel is taken as three per SM.
-    int8kv_pool* mp = const_cast<int8kv_pool*>(pool);
-    int n = 0;
-    if (kind != INT8KV_DECODE_SIMT) {
-      int prev = -1;
-      if (cudaGetDevice(&prev) == cudaSuccess && prev != pool->device)
-        cudaSetDevice(pool->device);
-      n = kind == INT8KV_DECODE_TCGEN05
-              ? decode_tc_resident_blocks(pool->head_dim, pool->n_groups)
-              : decode_mma_resident_blocks(pool->head_dim, pool->k_int8, pool->v_int8,
-                                           pool->n_groups);
-      if (prev >= 0 && prev != pool->device) cudaSetDevice(prev);
-    }
-    mp->resident[kind] = n > 0 ? n : 3 * pool->num_sms;
-  }
-  // units x splits blocks run in ceil(blocks / resident) waves, each as long as
-  // a block's ceil(pages / splits) pages plus about one page of prologue and
-  // epilogue; more than one split adds the combine (about two pages).  Take the
-  // split count with the shortest chain (the smallest on a tie).
-  const long long units = (long long)batch * pool->n_kv_heads;
-  const int ps = pool->page_size;
-  const int pages = max_ctx > 0 ? (max_ctx + ps - 1) / ps : 1;
-  const long long resident = pool->resident[kind];
-  const int top = pages < kMaxSplits ? pages : kMaxSplits;
-  long long best = -1;
-  int n = 1;
-  for (int s = 1; s <= top; ++s) {
-    const long long waves = (units * s + resident - 1) / resident;
-    const long long cost = waves * ((pages + s - 1) / s + 1) + (s > 1 ? 2 : 0);
-    if (best < 0 || cost < best) {
-      best = cost;
-      n = s;
-    }
-  }
-  return n;
+  return decode_splits_heuristic(pool, (long long)batch * pool->n_kv_heads, max_ctx, kMaxSplits);
 }
 
 int attn_decode_workspace_bytes(int batch, int n_heads, int n_kv_heads, int head_dim,
@@ -343,12 +360,8 @@ static int decode_entry(const int8kv_pool* pool, int layer, const uint16_t* q,
   if (!q || !seq_lens || !page_table || !out) return INT8KV_ERR_NULL_PTR;
   if (!aligned16(q) || !aligned16(out)) return INT8KV_ERR_ALIGNMENT;
   const int n_cg = (q_len * G + 7) / 8;   // blocks per (sequence, kv head) sharing the columns
-  if (n_splits == 0) {
-    int ctx = max_pages_per_seq * pool->page_size;
-    if (window > 0 && window + pool->page_size < ctx) ctx = window + pool->page_size;
-    n_splits = attn_decode_n_splits(pool, batch * n_cg, ctx);
-    if (n_splits < 0) return n_splits;
-  }
+  if (n_splits == 0)
+    n_splits = decode_auto_splits(pool, batch, q_len, G, max_pages_per_seq, window, 0);
   DecodeArgs a;
   a.q_len = q_len;
   a.n_cg = n_cg;
@@ -373,6 +386,7 @@ static int decode_entry(const int8kv_pool* pool, int layer, const uint16_t* q,
   a.n_splits = n_splits;
   const float scale = softmax_scale != 0.f ? softmax_scale : 1.0f / std::sqrt((float)pool->head_dim);
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.expire_polls = pool->expire_polls;
   const cudaError_t e = launch_decode(pool, layer, a, (cudaStream_t)stream);
   if (e == cudaErrorNotSupported) return INT8KV_ERR_UNSUPPORTED;
   return e == cudaSuccess ? INT8KV_OK : INT8KV_ERR_CUDA;
@@ -456,6 +470,14 @@ int attn_prefill_chunk_int8(const int8kv_pool* pool, int layer, const uint16_t* 
   return e == cudaSuccess ? INT8KV_OK : INT8KV_ERR_CUDA;
 }
 
+int kv_pool_test_expire_waits(int8kv_pool* pool, uint32_t max_polls) {
+  if (!pool) return INT8KV_ERR_NULL_PTR;
+  if (max_polls != 0 && decode_kernel_for(pool, 1) != INT8KV_DECODE_WARP_MMA)
+    return INT8KV_ERR_UNSUPPORTED;
+  pool->expire_polls = max_polls;
+  return INT8KV_OK;
+}
+
 int kv_pool_read_device_error(const int8kv_pool* pool, int32_t* out, void* stream) {
   if (!pool || !out || !pool->dev_error) return INT8KV_ERR_NULL_PTR;
   cudaStream_t s = (cudaStream_t)stream;
@@ -475,13 +497,9 @@ namespace int8kv {
 int decode_kernel_for(const int8kv_pool* pool, int G) {
   const PoolView v = layer_view(pool, 0);
   const bool mma_ok = pool->has_tmaps && decode_mma_supported(v, G);
-  const bool tc_ok = pool->has_tmaps && decode_tc_supported(v, pool->k_int8, pool->v_int8, G);
   switch (pool->decode_kernel) {
     case INT8KV_DECODE_WARP_MMA:
       if (mma_ok) return INT8KV_DECODE_WARP_MMA;
-      break;
-    case INT8KV_DECODE_TCGEN05:
-      if (tc_ok) return INT8KV_DECODE_TCGEN05;
       break;
     case INT8KV_DECODE_SIMT:
       return INT8KV_DECODE_SIMT;
@@ -510,9 +528,6 @@ cudaError_t launch_decode(const int8kv_pool* pool, int layer, const DecodeArgs& 
     e = launch_decode_mma(a, k8, v8, pool->tmap_k, pool->tmap_v, layer * pool->n_pages, stream);
     // up to 8 splits are combined inside the kernel (one cluster)
     if (e != cudaSuccess || a.n_splits <= 8) return e;
-  } else if (kind == INT8KV_DECODE_TCGEN05) {
-    e = launch_decode_tc(a, pool->tmap_k, pool->tmap_v, layer * pool->n_pages, stream);
-    if (e != cudaSuccess || a.n_splits == 1) return e;
   } else {
     e = launch_decode_simt(a, k8, v8, stream);
     if (e != cudaSuccess || a.n_splits == 1) return e;

@@ -30,9 +30,5 @@ bool decode_mma_supported(const PoolView& p, int G);
 int decode_mma_resident_blocks(int D, bool k8, bool v8, int ng);
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool k8, bool v8, const CUtensorMap& tmk,
                               const CUtensorMap& tmv, int layer_page0, cudaStream_t stream);
-bool decode_tc_supported(const PoolView& p, bool k8, bool v8, int G);
-int decode_tc_resident_blocks(int D, int ng);
-cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                             int layer_page0, cudaStream_t stream);
 
 }  // namespace int8kv

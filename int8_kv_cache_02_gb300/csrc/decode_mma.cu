@@ -131,7 +131,13 @@ __device__ __forceinline__ uint32_t v_pair(uint32_t w0, uint32_t w1, int k) {
 template <int D, bool KI8, bool VI8>
 __device__ __forceinline__ void issue_page(unsigned char* smem, uint64_t* full, int* stage_page,
                                            int st, int page, int row, const PoolView& p, int kvh,
-                                           const CUtensorMap* tmk, const CUtensorMap* tmv) {
+                                           const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                           bool expire) {
+  if (expire) {   // diagnostic: arm the stage for bytes no copy brings, issue nothing
+    stage_page[st] = page;
+    ptx::mbar_arrive_expect_tx(&full[st], 16);
+    return;
+  }
   mma::issue_page<D, KI8, VI8, true>(smem + st * Layout<D, KI8, VI8>::STAGE, &full[st],
                                      &stage_page[st], page, row, p, kvh, tmk, tmv);
 }
@@ -482,6 +488,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
 
   const PoolView& p = a.pool;
   const int split = blockIdx.x, kvh = blockIdx.y % p.Hkv, b = blockIdx.z;
+  const uint32_t max_polls = a.expire_polls ? a.expire_polls : kMaxPolls;   // bounded waits
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G;
   // B operand column c <-> (query, head) pair colg * 8 + c of the kv head's
@@ -604,7 +611,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       if (i < n_pg) {
         if (i == 0 || appends || !LY::DEFER)
           issue_page<D, KI8, VI8>(smem, full, stage_page, i, first[i], page_row(first[i]), p, kvh,
-                                  &tmk, &tmv);
+                                  &tmk, &tmv, a.expire_polls != 0);
         else
           stage_page[i] = first[i];   // kept for the request after page 0 lands; no consumer
                                       // reads it before that request's mbarrier completes
@@ -651,7 +658,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     const int last = n_pg - 1;
     int page = -1;
     if (last < LY::NS) {
-      if (ptx::mbar_wait(&full[last], 0, kMaxPolls)) {
+      if (ptx::mbar_wait(&full[last], 0, max_polls)) {
         page = stage_page[last];
         if (page >= 0) {
           unsigned char* sw = smem + last * LY::STAGE;
@@ -692,7 +699,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   {
     for (int i = 0; i < n_pg; ++i) {
       const int st = i % LY::NS;
-      if (!ptx::mbar_wait(&full[st], (i / LY::NS) & 1, kMaxPolls)) {
+      if (!ptx::mbar_wait(&full[st], (i / LY::NS) & 1, max_polls)) {
         flag_error(p.err, INT8KV_DEVERR_TIMEOUT);
         break;
       }
@@ -702,7 +709,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
           if (k < n_pg) {
             const int pg = stage_page[k];
             issue_page<D, KI8, VI8>(smem, full, stage_page, k, pg, page_row(pg), p, kvh, &tmk,
-                                    &tmv);
+                                    &tmv, a.expire_polls != 0);
           }
       }
       const int page = stage_page[st];
@@ -736,7 +743,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
           if (i + LY::NS < n_pg) {
             const int page = page_of(i + LY::NS);
             issue_page<D, KI8, VI8>(smem, full, stage_page, st, page, page_row(page), p, kvh,
-                                    &tmk, &tmv);
+                                    &tmk, &tmv, a.expire_polls != 0);
           }
         }
       }

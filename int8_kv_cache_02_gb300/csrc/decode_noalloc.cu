@@ -37,7 +37,8 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the scratch on `dev` (the current device).  The first call
-// per device looks it up; later calls reuse it.
+// per device looks it up; later calls reuse it.  The cached address assumes the
+// device's primary context lives as long as the process.
 int scratch_address(int dev, void** out) {
   if (dev < 0 || dev >= kMaxDevices) return INT8KV_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -59,16 +60,19 @@ extern "C" int attn_decode_int8_noalloc(const int8kv_pool* pool, int layer, cons
                                         void* stream) {
   if (!pool) return INT8KV_ERR_NULL_PTR;
   if (batch < 0 || n_heads <= 0 || n_splits < 0 || n_splits > int8kv::kMaxSplits ||
-      max_pages_per_seq <= 0 || n_heads % pool->n_kv_heads != 0)
+      max_pages_per_seq <= 0 || window < 0 || n_heads % pool->n_kv_heads != 0)
     return INT8KV_ERR_INVALID_ARG;
+  if (n_heads / pool->n_kv_heads > 8) return INT8KV_ERR_UNSUPPORTED;
   if (batch == 0) return INT8KV_OK;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return INT8KV_ERR_CUDA;
   if (dev != pool->device) return INT8KV_ERR_INVALID_ARG;   // the pool's device must be current
-  if (n_splits == 0) {
-    n_splits = attn_decode_n_splits(pool, batch, max_pages_per_seq * pool->page_size);
-    if (n_splits < 0) return n_splits;
-  }
+  // n_splits = 0: the count attn_decode_int8 would pick (same window and unit
+  // count), or, when that count's partials would not fit in the scratch, the
+  // best count among those that do
+  if (n_splits == 0)
+    n_splits = int8kv::decode_auto_splits(pool, batch, 1, n_heads / pool->n_kv_heads,
+                                          max_pages_per_seq, window, kNoAllocScratchBytes);
   int8kv::DecodeWorkspace ws;
   void* base = nullptr;
   const int st = scratch_address(dev, &base);

@@ -23,6 +23,7 @@ struct int8kv_pool {
   bool has_tmaps;    // TMA descriptors below are valid (shapes the tensor-core decode serves)
   int decode_kernel; // INT8KV_DECODE_*: the kernel its decode calls use (AUTO = the library's choice)
   int resident[4];   // per INT8KV_DECODE_* kernel: blocks resident at once (0 = not yet queried)
+  uint32_t expire_polls;   // diagnostic wait expiry of the decode calls (0: off)
   CUtensorMap tmap_k;              // K store as [rows][head_dim], 64-row x 128-byte swizzled boxes
   CUtensorMap tmap_v;              // V store, same
 };
@@ -84,7 +85,12 @@ struct DecodeArgs {
   // each (grid y = kv head + Hkv * column group).  Only the warp-level
   // tensor-core kernel serves q_len > 1.
   int q_len = 1, n_cg = 1;
+  // Diagnostic (kv_pool_test_expire_waits): nonzero makes the warp-level kernel
+  // issue no page copies, arm each stage for bytes that never arrive, and give
+  // up each wait after this many polls.
+  uint32_t expire_polls = 0;
 };
+
 
 struct PrefillArgs {
   PoolView pool;
@@ -102,7 +108,19 @@ cudaError_t launch_quant_append(const PoolView& pool, const uint16_t* k_new, con
                                 const int32_t* page_table, int max_pages, bool k_int8,
                                 bool v_int8, cudaStream_t stream, int pos_offset = 0);
 
-// The decode kernel (INT8KV_DECODE_WARP_MMA, _TCGEN05 or _SIMT) that serves a
+// Split count for units (sequence, kv head, column group) of at most max_ctx
+// positions: the shortest chain of waves x pages per block, at most max_splits.
+int decode_splits_heuristic(const int8kv_pool* pool, long long units, int max_ctx,
+                            int max_splits);
+
+// The split count a decode call with n_splits = 0 runs with: the heuristic for
+// the longest context the page table holds (or the window plus one page), over
+// batch x column groups x kv heads units; with max_workspace > 0, the largest
+// count whose workspace fits in it competes only with smaller ones.
+int decode_auto_splits(const int8kv_pool* pool, int batch, int q_len, int G, int max_pages,
+                       int window, size_t max_workspace);
+
+// The decode kernel (INT8KV_DECODE_WARP_MMA or _SIMT) that serves a
 // call with G query heads per kv head on this pool.
 int decode_kernel_for(const int8kv_pool* pool, int G);
 

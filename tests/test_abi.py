@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(L):
 def test_status_strings(L):
     from int8_kv_cache_02_gb300 import binding
     assert binding.int8kv_status_string(0) == "ok"
-    for s in range(-1, -9, -1):
+    for s in range(-1, -10, -1):
         assert binding.int8kv_status_string(s) != "unknown status"
 
 
@@ -97,3 +97,12 @@ def test_workspace_bytes(L):
     out = ctypes.c_size_t(0)
     assert L.attn_decode_workspace_bytes(1, 16, 2, 256, 0, ctypes.byref(out)) == -1
     assert L.attn_decode_workspace_bytes(1, 16, 2, 256, 100000, ctypes.byref(out)) == -1
+
+
+def test_pool_image_calls_reject_null_arguments(L):
+    out = ctypes.c_size_t(0)
+    assert L.kv_pool_image_bytes(None, 1, None, ctypes.byref(out)) == -2
+    assert L.kv_pool_save(None, 1, None, None, 1, None, 0, None, 0, None) == -2
+    assert L.kv_pool_load(None, None, 0, 1, None, 1, None, 0, None, None) == -2
+    from int8_kv_cache_02_gb300 import binding as b
+    assert b.int8kv_status_string(-9).startswith("pool image")

@@ -31,10 +31,10 @@ def _case(L=3000, seed=901):
     return q.cuda(), torch.tensor(lens, dtype=torch.int32, device="cuda"), pt.cuda(), dev
 
 
-def _raw_noalloc(L, dev, q, lens, pt, out, n_splits):
+def _raw_noalloc(L, dev, q, lens, pt, out, n_splits, window=0):
     return L.attn_decode_int8_noalloc(dev.handle, 0, ctypes.c_void_p(q.data_ptr()), q.shape[0],
                                       q.shape[1], ctypes.c_void_p(lens.data_ptr()),
-                                      ctypes.c_void_p(pt.data_ptr()), pt.shape[1], 0,
+                                      ctypes.c_void_p(pt.data_ptr()), pt.shape[1], window,
                                       ctypes.c_float(0.0), n_splits,
                                       ctypes.c_void_p(out.data_ptr()),
                                       ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
@@ -71,3 +71,58 @@ def test_noalloc_refuses_a_workspace_beyond_its_scratch():
     out = torch.zeros((64, 32, 128), dtype=torch.float32, device="cuda")
     assert _raw_noalloc(L, dev, q, lens, pt, out, 16) == -5          # INT8KV_ERR_CAPACITY
     assert binding.int8kv_status_string(-5).startswith("request exceeds")
+
+
+def test_noalloc_windowed_auto_split_matches_the_workspace_entry_point():
+    """With a sliding window and n_splits = 0 the split count is the one
+    attn_decode_int8 picks for the same call (sized to the window, not to the
+    page table), so the two entry points give the same bits."""
+    from int8_kv_cache_02_gb300 import binding
+    gu.lib_ready()
+    L = binding.lib()
+    q, lens, pt, dev = _case(L=9000, seed=902)
+    ref = torch.empty((2, 16, 256), dtype=torch.float32, device="cuda")
+    ns = binding.attn_decode_n_splits(dev, 2, 512 + 64)
+    assert ns < binding.attn_decode_n_splits(dev, 2, pt.shape[1] * 64)
+    binding.attn_decode_int8(dev, 0, q, lens, pt, ref, dev.decode_workspace(2, 16, ns), window=512)
+    for call in range(2):
+        out = torch.full((2, 16, 256), float("nan"), dtype=torch.float32, device="cuda")
+        assert _raw_noalloc(L, dev, q, lens, pt, out, 0, window=512) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"call {call}"
+    assert binding.kv_pool_read_device_error(dev) == 0
+
+
+def test_noalloc_auto_split_fits_the_scratch():
+    """n_splits = 0 on a batch whose heuristic split count would need more than
+    the scratch: the call picks the best count that fits instead of refusing,
+    and its output matches attn_decode_int8 at that count within the tolerance."""
+    from int8_kv_cache_02_gb300 import binding
+    gu.lib_ready()
+    L = binding.lib()
+    # 64 sequences, 32/8 heads, head_dim 128, page-table rows of 512 pages (the
+    # shape of the 64-sequence batch, short contexts): the heuristic's count for
+    # 32K positions needs far more than the 4 MiB scratch
+    B, H, Hkv, D = 64, 32, 8, 128
+    lens_l = [200 + 9 * b for b in range(B)]
+    qh, ks, vs = inputs.random_case(903, B, H, Hkv, D, lens_l)
+    pt, n_pages = inputs.page_table(lens_l, 64, seed=4, max_pages=512)
+    dev, _ = gu.make_pools(1, Hkv, D, 128, 64, n_pages, 0)
+    for b in range(B):
+        gu.fill_sequence(dev, None, 0, ks[b], vs[b], pt[b], oracle=False)
+    q, lens, ptd = qh.cuda(), torch.tensor(lens_l, dtype=torch.int32, device="cuda"), pt.cuda()
+    ns_ws = binding.attn_decode_n_splits(dev, B, pt.shape[1] * 64)
+    need = binding.attn_decode_workspace_bytes(B, H, Hkv, D, ns_ws)
+    assert need > 4 << 20
+    out = torch.full((B, H, D), float("nan"), dtype=torch.float32, device="cuda")
+    assert _raw_noalloc(L, dev, q, lens, ptd, out, 0) == 0
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    fits = [n for n in range(1, 257)
+            if binding.attn_decode_workspace_bytes(B, H, Hkv, D, n) <= 4 << 20]
+    ref = torch.empty_like(out)
+    ns = max(fits)
+    binding.attn_decode_int8(dev, 0, q, lens, ptd, ref, dev.decode_workspace(B, H, ns), n_splits=ns)
+    torch.cuda.synchronize()
+    gu.assert_attention_close(out.cpu().numpy(), ref.cpu().numpy().astype(np.float64), "auto fit")
+    assert binding.kv_pool_read_device_error(dev) == 0
