@@ -225,15 +225,26 @@ class DecodeState:
         return g
 
 
-def time_graph(g):
+def time_graph(g, reps=5):
+    """Median over `reps` timed replays of graph `g` (ms per replay), after one
+    untimed replay.  Before each timed replay the stream first runs a short
+    device-side sleep, so that the graph is already submitted when the start
+    event fires: the events then bracket the graph's kernels only, not the
+    host's submission of the graph."""
     import torch
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record()
     g.replay()
-    e1.record()
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1)
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(100_000)          # ~50 us at 2 GHz: covers the graph submission
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return statistics.median(times)
 
 
 def l2_bytes():
@@ -269,14 +280,44 @@ DECODE_SOURCES = ("common.cuh", "decode_combine.cu", "decode_common.cuh", "decod
                   "internal.h", "mma_common.cuh", "ptx.cuh", "quant_row.cuh")
 
 
-def decode_source_sha():
-    """Hash of the sources the timed decode step's kernels (the warp-level
-    tensor-core decode kernel and the combine) are built from."""
+def strip_comments(src):
+    """C/C++ source without its comments and blank lines (string and character
+    literals kept), so that a comment-only edit keeps a profile's source stamp."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).splitlines()]
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
+def source_sha(names):
+    """Hash of the comment-stripped sources `names` (files of csrc/)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "int8_kv_cache_02_gb300", "csrc")
-    for n in DECODE_SOURCES:
-        h.update(open(os.path.join(csrc, n), "rb").read())
+    for n in names:
+        h.update(strip_comments(open(os.path.join(csrc, n)).read()).encode())
     return h.hexdigest()[:16]
+
+
+def decode_source_sha():
+    """Source stamp of the timed decode step's kernels (the warp-level
+    tensor-core decode kernel and the combine)."""
+    return source_sha(DECODE_SOURCES)
 
 
 # --------------------------------------------------------------------------- oracle timing
@@ -519,8 +560,7 @@ def run_prefill(n_iter=20):
     with torch.cuda.graph(g):
         for _ in range(n_iter):
             step()
-    time_graph(g)
-    ms = min(time_graph(g) for _ in range(3)) / n_iter
+    ms = time_graph(g) / n_iter
     kv_bytes = L * 2 * (256 + 4 * 2) * 2
     return {"us_per_step": ms * 1e3, "TFLOPs": PREFILL_FLOPS / (ms * 1e-3) / 1e12,
             "algorithmic_flops": PREFILL_FLOPS, "kv_bytes": kv_bytes, "n_splits": ns,
@@ -567,8 +607,7 @@ def run_batched(n_iter=20):
             for _ in range(n_iter):
                 binding.attn_decode_int8(pool, layer, q, lens_d, ptd, out, ws, window=window,
                                          n_splits=ns)
-        time_graph(g)
-        us = min(time_graph(g) for _ in range(3)) / n_iter * 1e3
+        us = time_graph(g) / n_iter * 1e3
         vis = sum(min(L, window) if window else L for L in lens)
         byt = vis * per_pos + qo
         res["layer%d_window%d" % (layer, window)] = {
@@ -594,7 +633,6 @@ def run_extra(args):
         st = DecodeState(w, 131072, variant, copies, append_token=False)
         n = 60
         g = st.graph(n, append=False)
-        time_graph(g)
         ms = time_graph(g)
         us = ms / n * 1e3
         out[name] = {"us_per_step": us, "GBps": per / (us * 1e-6) / 1e9,

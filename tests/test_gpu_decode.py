@@ -281,53 +281,72 @@ def test_mma_path_ignores_garbage_beyond_the_context(variant):
 
 
 @pytest.mark.slow
-def test_batched_workload_full_size_sampled():
+def test_batched_workload_full_size_every_sequence():
     """64 sequences of 1024..32768 positions (8 kv heads, head_dim 128, one scale per
     (position, kv head), pages of 64), two layers: layer 0 full context, layer 1 a
-    512-position window.  The whole pool is built through the kernel; a sample of
-    sequences is checked against the oracle (codes, scales and attention)."""
+    512-position window.  The whole pool is built through the kernel; every
+    sequence of both layers is checked against the oracle: its codes and scales
+    bit for bit (SHA-256 of the position-major rows against the oracle's), and
+    its attention output at the split count the library picks and at a single
+    split.  The oracle runs in spawned worker processes, one sequence per job."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    import os
+
     from int8_kv_cache_02_gb300 import binding
-    from oracle import quant
+    from tests import batched_oracle as bo
     lens, qs = inputs.batched_lengths_and_q()
     lens = [int(x) for x in lens]
-    pt, n_pages = inputs.page_table(lens, 64, seed=11)
-    dev = binding.KVPool(2, 8, 128, 128, 64, n_pages, binding.K8V8)
-    ptd = pt.cuda()
-    zero = torch.zeros(1, dtype=torch.int32, device="cuda")
-    sample = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 7, 40})
-    kv = {}
-    for layer in (0, 1):
-        for b, L in enumerate(lens):
-            k, v = inputs.batched_kv(layer, b, L)
-            binding.kv_quant_append(dev, layer, k.reshape(1, L, 8, 128).cuda(),
-                                    v.reshape(1, L, 8, 128).cuda(), zero, ptd[b:b + 1])
-            if b in sample:
-                kv[(layer, b)] = (k, v)
-    lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
-    ns = binding.attn_decode_n_splits(dev, 64, pt.shape[1] * 64)
-    ws = dev.decode_workspace(64, 32, ns)
-    for layer, window in ((0, 0), (1, 512)):
-        out = torch.empty((64, 32, 128), dtype=torch.float32, device="cuda")
-        binding.attn_decode_int8(dev, layer, qs[layer].cuda(), lens_d, ptd, out, ws,
-                                 window=window, n_splits=ns)
-        torch.cuda.synchronize()
-        out = out.cpu().numpy()
-        assert np.isfinite(out).all()
-        kstore = dev.k_store[layer].cpu().numpy()
-        kscale = dev.k_scales[layer].cpu().numpy()
-        for b in sample:
-            k, v = kv[(layer, b)]
-            L = lens[b]
-            kc, ks = quant.quantize(k.numpy(), 128)
-            vc, vs = quant.quantize(v.numpy(), 128)
-            pos = np.arange(L)
-            pages = pt[b].numpy()[pos // 64]
-            assert np.array_equal(kstore[pages, :, pos % 64, :], kc)
-            assert np.array_equal(kscale[pages, :, pos % 64, :].view(np.uint16), ks.view(np.uint16))
-            ref = oatt.decode(qs[layer][b].numpy(), quant.dequantize(kc, ks, 128),
-                              quant.dequantize(vc, vs, 128), L, window=window)
-            gu.assert_attention_close(out[b], ref, f"layer {layer} seq {b} L {L}")
-    assert binding.kv_pool_read_device_error(dev) == 0
+    windows = {0: 0, 1: 512}
+    workers = max(1, min(16, (os.cpu_count() or 2) - 1))
+    one_thread = {k: "1" for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    saved = {k: os.environ.get(k) for k in one_thread}
+    os.environ.update(one_thread)          # inherited by the workers only (spawned below)
+    try:
+        ex = cf.ProcessPoolExecutor(workers, mp_context=mp.get_context("spawn"))
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    with ex:
+        jobs = {(layer, b): ex.submit(bo.oracle_sequence, layer, b, L, windows[layer])
+                for layer in (0, 1) for b, L in enumerate(lens)}
+        pt, n_pages = inputs.page_table(lens, 64, seed=11)
+        dev = binding.KVPool(2, 8, 128, 128, 64, n_pages, binding.K8V8)
+        ptd = pt.cuda()
+        zero = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for layer in (0, 1):
+            for b, L in enumerate(lens):
+                k, v = inputs.batched_kv(layer, b, L)
+                binding.kv_quant_append(dev, layer, k.reshape(1, L, 8, 128).cuda(),
+                                        v.reshape(1, L, 8, 128).cuda(), zero, ptd[b:b + 1])
+        lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        outs = {}
+        for layer, window in windows.items():
+            ns = binding.attn_decode_n_splits(dev, 64, window + 64 if window else pt.shape[1] * 64)
+            for n in sorted({ns, 1}):
+                out = torch.empty((64, 32, 128), dtype=torch.float32, device="cuda")
+                binding.attn_decode_int8(dev, layer, qs[layer].cuda(), lens_d, ptd, out,
+                                         dev.decode_workspace(64, 32, n), window=window,
+                                         n_splits=n)
+                torch.cuda.synchronize()
+                outs[(layer, n)] = out.cpu().numpy()
+        assert binding.kv_pool_read_device_error(dev) == 0
+        for layer in (0, 1):
+            kst, vst = dev.k_store[layer].cpu().numpy(), dev.v_store[layer].cpu().numpy()
+            ksc, vsc = dev.k_scales[layer].cpu().numpy(), dev.v_scales[layer].cpu().numpy()
+            for b, L in enumerate(lens):
+                pos = np.arange(L)
+                pages, slots = pt[b].numpy()[pos // 64], pos % 64
+                got = bo.codes_digest(kst[pages, :, slots, :], ksc[pages, :, slots, :],
+                                      vst[pages, :, slots, :], vsc[pages, :, slots, :])
+                want, ref = jobs[(layer, b)].result()
+                assert got == want, f"layer {layer} seq {b}: codes or scales differ"
+                for (ly, n), out in outs.items():
+                    if ly == layer:
+                        gu.assert_attention_close(out[b], ref, f"layer {layer} seq {b} L {L} ns {n}")
 
 
 @pytest.mark.parametrize("D,gs,ps,variant", [(256, 64, 64, 0), (128, 128, 64, 1), (256, 128, 64, 2),
@@ -456,8 +475,6 @@ def test_every_decode_kernel_matches_the_oracle(D, gs, variant):
     q, pt, dev, orc = _setup(600 + D + gs + variant, 3, 16, 2, D, gs, lens, variant, outliers=True)
     ref = _oracle(orc, 0, q, lens, pt)
     kinds = [binding.DECODE_WARP_MMA, binding.DECODE_SIMT]
-    if variant == binding.K8V8:
-        kinds.append(binding.DECODE_TCGEN05)
     outs = {}
     for kind in kinds:
         dev.set_decode_kernel(kind)
