@@ -17,7 +17,7 @@ Image layout (little-endian; every section starts on a 16-byte boundary):
   header, 48 bytes:
      0  4 bytes  magic b"I8KV"
      4  u32      format version, 3
-     8  u32      store variant (0 k8v8, 1 k8v16, 2 k16v8)
+     8  u32      store variant (0 k8v8, 1 k8v16, 2 k16v8, 3 k8v4)
     12  u32      n_layers
     16  u32      n_kv_heads
     20  u32      head_dim
@@ -27,11 +27,11 @@ Image layout (little-endian; every section starts on a 16-byte boundary):
     40  u64      0
   lengths: int32 [n_seqs], padded with zeros to a multiple of 16 bytes
   payload: for each sequence b, for each layer l, four sections (the scales
-  sections only for an int8 store), each padded with zeros to 16 bytes:
+  sections only for a quantized store), each padded with zeros to 16 bytes:
      K store   [L_b][n_kv_heads][head_dim]  int8 codes or fp16 values
-     V store   [L_b][n_kv_heads][head_dim]
+     V store   [L_b][n_kv_heads][head_dim]  (k8v4: [head_dim / 2] bytes of 4-bit codes)
      K scales  [L_b][n_kv_heads][head_dim / group_size] fp16
-     V scales  [L_b][n_kv_heads][head_dim / group_size] fp16
+     V scales  [L_b][n_kv_heads][head_dim / group_size] fp16  (k8v4: [head_dim / 32])
 
 The payload is position-major, so an image does not depend on the page size
 or the physical pages of the pool it came from: it can be loaded into any
@@ -57,13 +57,15 @@ def _pad16(n):
 
 
 def _sections(pool, L):
-    """(name, store, scales?, bytes) of the four sections of one (sequence, layer)."""
+    """(name, region, bytes) of the sections of one (sequence, layer): K store, V
+    store, then the scales region of each store that has one.  A section holds
+    the region's rows of positions 0..L-1, so its bytes are L x kv heads x the
+    region's row bytes."""
     out = []
-    for name, store, is8 in (("k", pool.k_store, pool.k_int8), ("v", pool.v_store, pool.v_int8)):
-        out.append((name, store, L * pool.n_kv_heads * pool.head_dim * (1 if is8 else 2)))
-    for name, scales, is8 in (("ks", pool.k_scales, pool.k_int8), ("vs", pool.v_scales, pool.v_int8)):
-        if is8:
-            out.append((name, scales, L * pool.n_kv_heads * pool.ng * 2))
+    for name, region in (("k", pool.k_store), ("v", pool.v_store), ("ks", pool.k_scales),
+                         ("vs", pool.v_scales)):
+        if region is not None:
+            out.append((name, region, L * pool.n_kv_heads * region.shape[-1] * region.itemsize))
     return out
 
 

@@ -21,15 +21,16 @@ at slot ``p % page_size``.
 
 import numpy as np
 
-from . import quant
+from . import q4, quant
 
-K8V8, K8V16, K16V8 = 0, 1, 2
-VARIANT_NAMES = {K8V8: "k8v8", K8V16: "k8v16", K16V8: "k16v8"}
+K8V8, K8V16, K16V8, K8V4 = 0, 1, 2, 3
+VARIANT_NAMES = {K8V8: "k8v8", K8V16: "k8v16", K16V8: "k16v8", K8V4: "k8v4"}
 
 
 def store_is_int8(variant: int):
-    """(K is int8, V is int8) for a store variant."""
-    return {K8V8: (True, True), K8V16: (True, False), K16V8: (False, True)}[variant]
+    """(K is int8, V is int8) for a store variant (k8v4: K int8, V 4-bit)."""
+    return {K8V8: (True, True), K8V16: (True, False), K16V8: (False, True),
+            K8V4: (True, False)}[variant]
 
 
 def bytes_per_cell(n_kv_heads: int, head_dim: int, gs: int, int8: bool) -> int:
@@ -45,7 +46,12 @@ def bytes_per_cell(n_kv_heads: int, head_dim: int, gs: int, int8: bool) -> int:
 
 
 class Pool:
-    """Host model of the paged pool; arrays are the raw regions."""
+    """Host model of the paged pool; arrays are the raw regions.
+
+    k8v4 (Strata pull request #2698, "Not in this PR": the 4-bit store with the
+    FWHT-256 rotation, see oracle/q4.py): V rows are rotated, then Q4_0; the V
+    store is uint8 [..., head_dim / 2] (two codes per byte) and the V scales
+    fp16 [..., head_dim / 32]."""
 
     def __init__(self, n_layers, n_kv_heads, head_dim, gs, page_size, n_pages, variant):
         assert head_dim % gs == 0
@@ -53,12 +59,17 @@ class Pool:
         self.gs, self.ng = gs, head_dim // gs
         self.page_size, self.n_pages, self.variant = page_size, n_pages, variant
         self.k_int8, self.v_int8 = store_is_int8(variant)
+        self.v_q4 = variant == K8V4
         body = (n_layers, n_pages, n_kv_heads, page_size, head_dim)
         sc = (n_layers, n_pages, n_kv_heads, page_size, self.ng)
         self.k_store = np.zeros(body, np.int8 if self.k_int8 else np.float16)
         self.v_store = np.zeros(body, np.int8 if self.v_int8 else np.float16)
         self.k_scales = np.zeros(sc, np.float16) if self.k_int8 else None
         self.v_scales = np.zeros(sc, np.float16) if self.v_int8 else None
+        if self.v_q4:
+            assert head_dim % q4.BLOCK == 0 and head_dim & (head_dim - 1) == 0
+            self.v_store = np.zeros(body[:-1] + (head_dim // 2,), np.uint8)
+            self.v_scales = np.zeros(body[:-1] + (head_dim // q4.BLOCK,), np.float16)
 
     def _slot(self, page_table_row, pos):
         return int(page_table_row[pos // self.page_size]), pos % self.page_size
@@ -75,12 +86,16 @@ class Pool:
         for b in range(n_seqs):
             for i in range(n_new):
                 page, slot = self._slot(page_table[b], int(seq_pos[b]) + i)
-                for new, store, scales, is8 in (
-                    (k_new, self.k_store, self.k_scales, self.k_int8),
-                    (v_new, self.v_store, self.v_scales, self.v_int8),
+                for new, store, scales, is8, is4 in (
+                    (k_new, self.k_store, self.k_scales, self.k_int8, False),
+                    (v_new, self.v_store, self.v_scales, self.v_int8, self.v_q4),
                 ):
                     x = new[b, i]                              # [n_kv_heads][head_dim]
-                    if is8:
+                    if is4:
+                        c, s = q4.quantize_rows(x)
+                        store[layer, page, :, slot, :] = c
+                        scales[layer, page, :, slot, :] = s
+                    elif is8:
                         c, s = quant.quantize(x, self.gs)
                         store[layer, page, :, slot, :] = c
                         scales[layer, page, :, slot, :] = s
@@ -99,11 +114,15 @@ class Pool:
         pos = np.arange(start, start + n)
         pages = np.asarray(page_table_row)[pos // self.page_size]
         slots = pos % self.page_size
-        for x, store, scales, is8 in (
-            (k_seq, self.k_store, self.k_scales, self.k_int8),
-            (v_seq, self.v_store, self.v_scales, self.v_int8),
+        for x, store, scales, is8, is4 in (
+            (k_seq, self.k_store, self.k_scales, self.k_int8, False),
+            (v_seq, self.v_store, self.v_scales, self.v_int8, self.v_q4),
         ):
-            if is8:
+            if is4:
+                c, s = q4.quantize_rows(x)
+                store[layer, pages, :, slots, :] = c
+                scales[layer, pages, :, slots, :] = s
+            elif is8:
                 c, s = quant.quantize(x, self.gs)
                 store[layer, pages, :, slots, :] = c
                 scales[layer, pages, :, slots, :] = s
@@ -120,12 +139,14 @@ class Pool:
         pages = np.asarray(page_table_row)[pos // self.page_size] if stop > start else np.zeros(0, int)
         slots = pos % self.page_size
         out = []
-        for store, scales, is8 in (
-            (self.k_store, self.k_scales, self.k_int8),
-            (self.v_store, self.v_scales, self.v_int8),
+        for store, scales, is8, is4 in (
+            (self.k_store, self.k_scales, self.k_int8, False),
+            (self.v_store, self.v_scales, self.v_int8, self.v_q4),
         ):
             rows = store[layer, pages, :, slots, :]             # [L][Hkv][D]
-            if is8:
+            if is4:   # dequantized and rotated back to the original basis
+                out.append(q4.dequantize_rows(rows, scales[layer, pages, :, slots, :]))
+            elif is8:
                 out.append(quant.dequantize(rows, scales[layer, pages, :, slots, :], self.gs))
             else:
                 out.append(rows.astype(np.float64))

@@ -221,3 +221,72 @@ def test_image_without_scales_is_caught(monkeypatch):
     real = im._sections
     monkeypatch.setattr(im, "_sections", lambda pool, L: real(pool, L)[:2])
     assert not _image_pins_hold()
+
+
+# ---- 4-bit store: mistakes planted in the oracle's FWHT or Q4_0 must fail a pin
+def _q4_pins_hold():
+    from tests import test_oracle_q4 as t
+    try:
+        t.test_q4_0_hand_computed_blocks()
+        t.test_fwht_hand_values()
+        t.test_fwht_order_of_operations()
+    except AssertionError:
+        return False
+    return True
+
+
+def test_q4_pins_hold_unmutated():
+    assert _q4_pins_hold()
+
+
+def test_q4_last_largest_value_is_caught(monkeypatch):
+    import oracle.q4 as m
+    real = np.argmax
+    monkeypatch.setattr(m, "np", _NP(argmax=lambda a, axis=None: a.shape[axis] - 1 - real(
+        np.flip(a, axis=axis), axis=axis)))
+    assert not _q4_pins_hold()
+
+
+def test_q4_scale_sign_is_caught(monkeypatch):
+    """d = m / 8 instead of m / -8: the largest value lands on the clamped end."""
+    import oracle.q4 as m
+
+    def plus_eighth(x32):
+        x = np.asarray(x32, dtype=np.float32)
+        g = x.reshape(x.shape[:-1] + (x.shape[-1] // 32, 32))
+        first = np.argmax(np.abs(g), axis=-1)
+        mx = np.take_along_axis(g, first[..., None], axis=-1)[..., 0]
+        d = mx * np.float32(0.125)
+        idv = np.where(d != 0, np.float32(1.0) / np.where(d != 0, d, 1), 0).astype(np.float32)
+        t = ((g * idv[..., None]).astype(np.float32) + np.float32(8.5)).astype(np.float32)
+        return np.minimum(np.floor(t), 15).astype(np.uint8).reshape(x.shape), d.astype(np.float16)
+
+    monkeypatch.setattr(m, "q4_0_quantize", plus_eighth)
+    assert not _q4_pins_hold()
+
+
+def test_fwht_without_normalisation_is_caught(monkeypatch):
+    import oracle.q4 as m
+    real = m.fwht
+    monkeypatch.setattr(m, "fwht", lambda x: real(x) * np.float32(np.sqrt(np.asarray(x).shape[-1])))
+    assert not _q4_pins_hold()
+
+
+def test_fwht_pairing_mistake_is_caught(monkeypatch):
+    import oracle.q4 as m
+    real = m.fwht
+
+    def reversed_stages(x):     # the same butterflies, stages taken from the largest stride
+        y = np.array(x, dtype=np.float32, copy=True)
+        n = y.shape[-1]
+        h = n // 2
+        while h >= 1:
+            v = y.reshape(y.shape[:-1] + (n // (2 * h), 2, h))
+            a, b = v[..., 0, :].copy(), v[..., 1, :].copy()
+            v[..., 0, :], v[..., 1, :] = a + b, a - b
+            h //= 2
+        return y * np.float32(1.0 / np.sqrt(n))
+
+    monkeypatch.setattr(m, "fwht", reversed_stages)
+    assert not _q4_pins_hold()
+    monkeypatch.setattr(m, "fwht", real)
