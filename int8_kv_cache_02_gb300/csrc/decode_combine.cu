@@ -31,6 +31,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ float w[kMaxSplits];
   __shared__ float2 part[kCombineWarps][32];
+  // The next kernel of the stream may launch now: a decode kernel that follows
+  // waits on this grid before it reads anything but its prefetch hints.
+  ptx::grid_launch_dependents();
   ptx::grid_dependency_wait();
   const size_t h = (size_t)b * a.H + hq;
   // every lane first puts its partial rows in flight (they do not depend on the

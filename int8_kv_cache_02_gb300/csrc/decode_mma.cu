@@ -512,8 +512,29 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     ptx::fence_mbar_init();
   }
   __syncthreads();
-  // Launched as a programmatic dependent: no global memory is read before the
-  // preceding kernel of the stream has completed.
+  // Launched as a programmatic dependent: nothing read before the preceding
+  // kernel of the stream has completed is used, except as a prefetch hint.
+  // Thread 0 reads the length and the first page id of its range through L2
+  // (never L1, so no stale line outlives the wait) and has L2 fetch that page,
+  // which overlaps its HBM latency with the end of the preceding kernel.  A
+  // length or page id that kernel still changes only makes the prefetch
+  // useless: the id is checked against the pool before use, and L2 is coherent
+  // with the writes that follow.
+  if (threadIdx.x == 0) {
+    int Ls = ptx::ldcg32(a.seq_lens + b);
+    Ls = Ls < 0 ? 0 : min(Ls, a.max_pages * kPage);
+    const int lo = a.window > 0 ? max(0, Ls - a.window) : 0;
+    int s0 = lo, s1 = lo;
+    split_range(lo, Ls, split, a.n_splits, kPage, &s0, &s1);
+    const int pg = s1 > s0 ? ptx::ldcg32(a.page_table + (size_t)b * a.max_pages + s0 / kPage) : -1;
+    if (pg >= 0 && pg < p.n_pages) {
+      const size_t r0 = ((size_t)pg * p.Hkv + kvh) * kPage;   // first row of the page-head
+      ptx::bulk_prefetch_l2((const char*)p.k + r0 * D * (KI8 ? 1 : 2), (KI8 ? 1 : 2) * D * kPage);
+      ptx::bulk_prefetch_l2((const char*)p.v + r0 * D * (VI8 ? 1 : 2), (VI8 ? 1 : 2) * D * kPage);
+      if (KI8) ptx::bulk_prefetch_l2(p.ks + r0 * NG, kPage * NG * 2);
+      if (VI8) ptx::bulk_prefetch_l2(p.vs + r0 * NG, kPage * NG * 2);
+    }
+  }
   ptx::grid_dependency_wait();
   ptx::grid_launch_dependents();
 

@@ -215,6 +215,20 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 
+// A 32-bit load served from L2 (never cached in L1): a value another grid may
+// still be writing, read only as a hint.
+__device__ __forceinline__ int ldcg32(const int32_t* p) {
+  int v;
+  asm volatile("ld.global.cg.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// Ask L2 to fetch [p, p + bytes) (16-byte aligned, a multiple of 16 bytes); no
+// data reaches the SM and nothing waits for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---- programmatic dependent launch ----------------------------------------------
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
