@@ -48,13 +48,17 @@ WORKLOAD = ("decode step (1-token append fused into the split-K GQA decode kerne
 B, H, HKV, D, GS, PS, CTX = 1, 16, 2, 256, 64, 64, 8192
 
 
-def step_bytes(ctx=CTX, hkv=HKV, h=H, d=D, gs=GS, k_int8=True, v_int8=True, append=True):
-    """Algorithmic bytes of one step: int8 KV + scales (fp16 for an fp16 store)
-    read once, q (fp16) read, O (fp32) written, and the appended token
-    (fp16 in, codes + scales out)."""
+def step_bytes(ctx=CTX, hkv=HKV, h=H, d=D, gs=GS, k_int8=True, v_int8=True, append=True,
+               v_q4=False):
+    """Algorithmic bytes of one step: int8 KV + scales (fp16 for an fp16 store;
+    4-bit codes + one fp16 scale per 32 values for the k8v4 V store) read once,
+    q (fp16) read, O (fp32) written, and the appended token (fp16 in, codes +
+    scales out)."""
     per_pos = 0
     for is8 in (k_int8, v_int8):
         per_pos += hkv * d + hkv * (d // gs) * 2 if is8 else hkv * d * 2
+    if v_q4:
+        per_pos += hkv * d // 2 + hkv * (d // 32) * 2 - hkv * d * 2   # instead of fp16 V
     n = ctx * per_pos + h * d * 2 + h * d * 4
     if append:
         n += 2 * hkv * d * 2 + per_pos
@@ -501,8 +505,8 @@ def run_ours(args, rank, world, local):
                 "eager": {"value": round(step_bytes() * n_e2e * world / e2e_eager_s / 1e9, 2),
                           "us_per_step": e2e_eager_s / n_e2e * 1e6,
                           "how": "the same three calls issued from Python every step"}},
-        "roofline": {"bound": "hbm", "kernel": "decode_mma_kernel (attn_decode_int8: split-K "
-                                               "partials; the combine kernel follows)",
+        "roofline": {"bound": "hbm", "kernel": "the attn_decode_int8 call: decode_mma_kernel "
+                                               "(split-K partials) + decode_combine_kernel",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": traffic, "algorithmic_bytes": decode_bytes(),
@@ -562,68 +566,162 @@ def run_prefill(n_iter=20):
             step()
     ms = time_graph(g) / n_iter
     kv_bytes = L * 2 * (256 + 4 * 2) * 2
-    return {"us_per_step": ms * 1e3, "TFLOPs": PREFILL_FLOPS / (ms * 1e-3) / 1e12,
+    tf = PREFILL_FLOPS / (ms * 1e-3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpeak, tkind = float(json.load(f)["bf16_tflops"]), "measured bf16 burst (fp16: same nominal rate)"
+    except Exception:
+        tpeak, tkind = 1900.0, "fallback"
+    return {"us_per_step": ms * 1e3, "TFLOPs": tf, "frac_of_tensor_peak": round(tf / tpeak, 4),
+            "peak_source": tkind,
             "algorithmic_flops": PREFILL_FLOPS, "kv_bytes": kv_bytes, "n_splits": ns,
             "note": "append of the 256-token chunk + causal attention; the 33,024-position "
                     "cache (34 MB) is L2-resident; paced by the CUDA-core work between the two MMA batches of a page"}
 
 
-def run_batched(n_iter=20):
-    """Batched decode over a paged pool: 64 sequences, lengths uniform in [1024, 32768],
-    32 query / 8 kv heads, head_dim 128, one scale per (position, kv head); layer 0
-    full context, layer 1 a 512-position window.  Decode kernel alone per layer."""
+def graph_us(issue, n_iter):
+    """Median µs per call of `issue(i)` (i = 0 .. n_iter-1) replayed from a CUDA graph."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(3):
+            issue(i)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n_iter):
+            issue(i)
+    return time_graph(g) / n_iter * 1e3
+
+
+def rate(byt, us, l2):
+    peak, kind = measured_peaks()
+    gbs = byt / (us * 1e-6) / 1e9
+    return {"us_per_step": us, "GBps": gbs, "frac_of_peak": round(gbs / peak, 4),
+            "peak_source": kind, "algorithmic_bytes": byt, "l2": l2}
+
+
+def run_batched(n_iter=20, window_copies=4):
+    """Batched decode over a paged pool: 64 sequences, lengths uniform in [1024, 32768]
+    (seed 3), 32 query / 8 kv heads, head_dim 128, one scale per (position, kv head);
+    layer 0 full context, and the 512-position window layer held in `window_copies`
+    copies (layers 1..) so that each replay reads HBM.  K/V are N(0,1) fp16 drawn
+    on the device from seeded generators (the parity tests draw the same shapes on
+    the CPU; the timing depends only on the shapes)."""
     import torch
 
     from int8_kv_cache_02_gb300 import binding, inputs
     lens, qs = inputs.batched_lengths_and_q()
     lens = [int(x) for x in lens]
     pt, n_pages = inputs.page_table(lens, PS, seed=11)
-    pool = binding.KVPool(2, 8, 128, 128, PS, n_pages, binding.K8V8)
+    n_layers = 1 + window_copies
+    pool = binding.KVPool(n_layers, 8, 128, 128, PS, n_pages, binding.K8V8)
     ptd = pt.cuda()
-    zero = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for layer in (0, 1):
+    g = torch.Generator(device="cuda")
+    for layer in range(n_layers):
         for b, L in enumerate(lens):
-            k, v = inputs.batched_kv(layer, b, L)
-            binding.kv_quant_append(pool, layer, k.reshape(1, L, 8, 128).cuda(),
-                                    v.reshape(1, L, 8, 128).cuda(), zero, ptd[b:b + 1])
+            g.manual_seed(5_000_000 + 1000 * layer + b)
+            start = 0 if layer == 0 else max(0, L - 512)
+            n = L - start
+            k = torch.randn((1, n, 8, 128), generator=g, device="cuda").half()
+            v = torch.randn((1, n, 8, 128), generator=g, device="cuda").half()
+            binding.kv_quant_append(pool, layer, k, v,
+                                    torch.tensor([start], dtype=torch.int32, device="cuda"),
+                                    ptd[b:b + 1])
+    torch.cuda.synchronize()
     lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
     out = torch.empty((64, 32, 128), dtype=torch.float32, device="cuda")
-    res = {"total_ctx": sum(lens)}
+    res = {"total_ctx": sum(lens), "inputs": "device-drawn N(0,1) fp16, seeded"}
     per_pos = 8 * 128 * 2 + 8 * 2 * 2        # int8 K, V rows + fp16 scales, all kv heads
     qo = 64 * 32 * 128 * (2 + 4)
-    for layer, window in ((0, 0), (1, 512)):
+    for name, window, layers in (("layer0_full", 0, [0]),
+                                 ("layer1_window512", 512, list(range(1, n_layers)))):
         ns = binding.attn_decode_n_splits(pool, 64, window + PS if window else pt.shape[1] * PS)
         ws = pool.decode_workspace(64, 32, ns)
-        q = qs[layer].cuda()
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            for _ in range(3):
-                binding.attn_decode_int8(pool, layer, q, lens_d, ptd, out, ws, window=window,
-                                         n_splits=ns)
-        torch.cuda.current_stream().wait_stream(s)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(n_iter):
-                binding.attn_decode_int8(pool, layer, q, lens_d, ptd, out, ws, window=window,
-                                         n_splits=ns)
-        us = time_graph(g) / n_iter * 1e3
+        q = qs[0 if window == 0 else 1].cuda()
+
+        def issue(i, window=window, layers=layers, ns=ns, ws=ws, q=q):
+            binding.attn_decode_int8(pool, layers[i % len(layers)], q, lens_d, ptd, out, ws,
+                                     window=window, n_splits=ns)
+
+        us = graph_us(issue, n_iter)
         vis = sum(min(L, window) if window else L for L in lens)
-        byt = vis * per_pos + qo
-        res["layer%d_window%d" % (layer, window)] = {
-            "us_per_step": us, "n_splits": ns, "GBps": byt / (us * 1e-6) / 1e9, "algorithmic_bytes": byt,
-            "l2": "HBM-resident (pool 4.5 GB)" if not window else "window of 512 per sequence "
-                  "(68 MB: partly L2-resident)"}
+        l2 = ("pool 4.5 GB per layer: HBM-resident" if not window else
+              f"{len(layers)} copies of the window layer ({len(layers) * vis * per_pos / 2**20:.0f} "
+              f"MiB) rotated: HBM-resident")
+        res[name] = dict(rate(vis * per_pos + qo, us, l2), n_splits=ns)
+    del pool
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_tiny():
+    """Tiny decode (batch 1, 8/2 heads, head_dim 128, 512 positions, one scale per
+    (position, kv head)) at 4 splits and a single pass.  272 KB: L2-resident and
+    bound by launch latency, not by HBM."""
+    import torch
+
+    from int8_kv_cache_02_gb300 import binding, inputs
+    w = inputs.tiny()
+    pt, n_pages = inputs.page_table([512], PS, seed=0)
+    pool = binding.KVPool(1, 2, 128, 128, PS, n_pages, binding.K8V8)
+    binding.kv_quant_append(pool, 0, w["k"].reshape(1, 512, 2, 128).cuda(),
+                            w["v"].reshape(1, 512, 2, 128).cuda(),
+                            torch.zeros(1, dtype=torch.int32, device="cuda"), pt.cuda())
+    q, ptd = w["q"].cuda(), pt.cuda()
+    lens = torch.tensor([512], dtype=torch.int32, device="cuda")
+    out = torch.empty((1, 8, 128), dtype=torch.float32, device="cuda")
+    byt = decode_bytes(ctx=512, hkv=2, h=8, d=128, gs=128)
+    res = {}
+    for ns in (4, 1):
+        ws = pool.decode_workspace(1, 8, ns)
+        us = graph_us(lambda i, ws=ws, ns=ns: binding.attn_decode_int8(
+            pool, 0, q, lens, ptd, out, ws, n_splits=ns), 200)
+        res[f"n_splits{ns}"] = rate(byt, us, "272 KB: L2-resident, launch-bound")
+    return res
+
+
+def run_windows(st, ctx, q_lens=(2, 4), n_iter=40):
+    """Query windows (speculative verify) over a DecodeState's rotating pools:
+    q_len queries per sequence, causal within the window."""
+    import torch
+
+    from int8_kv_cache_02_gb300 import binding
+    res = {}
+    for ql in q_lens:
+        gq = torch.Generator(device="cuda").manual_seed(77 + ql)
+        qw = torch.randn((1, ql, st.h, D), generator=gq, device="cuda").half()
+        outw = torch.empty((1, ql, st.h, D), dtype=torch.float32, device="cuda")
+        ns = binding.attn_decode_n_splits(st.pool, -(-ql * (st.h // HKV) // 8), ctx)
+        ws = st.pool.decode_workspace(ql, st.h, ns)
+
+        def issue(i, qw=qw, outw=outw, ns=ns, ws=ws):
+            c = i % st.copies
+            binding.attn_decode_multi_int8(st.pool, 0, qw, st.lens, st.pt[c:c + 1], outw, ws,
+                                           n_splits=ns)
+
+        us = graph_us(issue, n_iter)
+        byt = decode_bytes(ctx=ctx) + (ql - 1) * H * D * 6
+        res[f"q_len{ql}"] = dict(rate(byt, us, f"{st.copies} rotating pool copies"), n_splits=ns,
+                                 attn_tokens_per_s=ql * 1e6 / us)
     return res
 
 
 def run_extra(args):
-    """128K-context decode (k8v8 and k8v16), decode kernel alone, L2 defeated by copies;
-    and the prefill chunk."""
+    """Every workload besides the headline step: the tiny decode, the 128K-context
+    decode (k8v8 and k8v16), query windows at 8K and 128K, the 64-sequence batch
+    (both layers) and the prefill chunk.  Decode calls alone, L2 defeated by
+    rotating copies where the data would fit in it."""
     import torch
 
     from int8_kv_cache_02_gb300 import binding, inputs
-    out = {"prefill_chunk": run_prefill()}
+    out = {"tiny_512": run_tiny()}
+    w = inputs.grouped8k()
+    st = DecodeState(w, CTX, binding.K8V8, copies_for(decode_bytes()), append_token=False)
+    out["grouped8k_windows"] = run_windows(st, CTX)
+    del st
     torch.cuda.empty_cache()
     w = inputs.long128k()
     for name, variant, vi8 in (("long128k_k8v8", binding.K8V8, True),
@@ -633,13 +731,94 @@ def run_extra(args):
         st = DecodeState(w, 131072, variant, copies, append_token=False)
         n = 60
         g = st.graph(n, append=False)
-        ms = time_graph(g)
-        us = ms / n * 1e3
-        out[name] = {"us_per_step": us, "GBps": per / (us * 1e-6) / 1e9,
-                     "algorithmic_bytes": per, "n_splits": st.n_splits, "copies": copies}
+        us = time_graph(g) / n * 1e3
+        out[name] = dict(rate(per, us, f"{copies} rotating pool copies"), n_splits=st.n_splits,
+                         copies=copies)
+        if vi8:
+            out["long128k_windows"] = run_windows(st, 131072, n_iter=20)
         del st, g
         torch.cuda.empty_cache()
+    # k8v4 (V rotated + Q4_0; CUDA-core decode kernel) at 8K and 128K
+    for name, wf, ctx in (("grouped8k_k8v4", inputs.grouped8k, CTX),
+                          ("long128k_k8v4", inputs.long128k, 131072)):
+        per = decode_bytes(ctx=ctx, v_int8=False, v_q4=True)
+        copies = max(2, math.ceil(2 * l2_bytes() / per) + 1)
+        st = DecodeState(wf(), ctx, binding.K8V4, copies, append_token=False)
+        n = 40
+        g = st.graph(n, append=False)
+        us = time_graph(g) / n * 1e3
+        out[name] = dict(rate(per, us, f"{copies} rotating pool copies"), n_splits=st.n_splits,
+                         kernel="decode_simt_kernel + decode_combine_kernel")
+        del st, g
+        torch.cuda.empty_cache()
+    if not getattr(args, "no_batched", False):
+        out["batched_64seq"] = run_batched()
+    out["prefill_chunk"] = run_prefill()
     return out
+
+
+PROFILE_CASES = ("decode8k", "decode128k", "append256", "batched16", "prefill", "k8v4_8k")
+
+
+def run_profile_case(name, reps=5):
+    """Set up one workload and issue its call `reps` times, eagerly, with no
+    timing: the commands the ncu summaries under profiles/ are taken with.
+      decode8k    attn_decode_append_int8 on the 8K workload (decode + combine)
+      decode128k  attn_decode_int8 on the 128K workload, k8v8 (decode + combine)
+      append256   kv_quant_append of the prefill chunk's 256 tokens
+      batched16   attn_decode_int8 over 16 of the 64-sequence batch's sequences
+                  (head_dim 128, the same lengths; 1.1 GB instead of 4.5 GB)
+      prefill     append + attn_prefill_chunk_int8 of the 256-query chunk
+      k8v4_8k     attn_decode_int8 on the 8K workload in a k8v4 pool"""
+    import torch
+
+    from int8_kv_cache_02_gb300 import binding, inputs
+    if name in ("decode8k", "k8v4_8k"):
+        w = inputs.grouped8k()
+        variant = binding.K8V8 if name == "decode8k" else binding.K8V4
+        st = DecodeState(w, CTX, variant, 3, append_token=name == "decode8k")
+        for i in range(reps):
+            st.step(i % 3, append=name == "decode8k")
+    elif name == "decode128k":
+        st = DecodeState(inputs.long128k(), 131072, binding.K8V8, 3, append_token=False)
+        for i in range(reps):
+            st.step(i % 3, append=False)
+    elif name == "append256":
+        w = inputs.prefill()
+        start, n_new = w["start"], w["n_new"]
+        pt, n_pages = inputs.page_table([start + n_new], PS, seed=6)
+        pool = binding.KVPool(1, 2, 256, 64, PS, n_pages, binding.K8V8)
+        kc = w["k"][start:].reshape(1, n_new, 2, 256).cuda()
+        vc = w["v"][start:].reshape(1, n_new, 2, 256).cuda()
+        pos = torch.tensor([start], dtype=torch.int32, device="cuda")
+        for _ in range(reps):
+            binding.kv_quant_append(pool, 0, kc, vc, pos, pt.cuda())
+    elif name == "batched16":
+        lens, qs = inputs.batched_lengths_and_q()
+        lens = [int(x) for x in lens[:16]]
+        pt, n_pages = inputs.page_table(lens, PS, seed=11)
+        pool = binding.KVPool(1, 8, 128, 128, PS, n_pages, binding.K8V8)
+        ptd = pt.cuda()
+        g = torch.Generator(device="cuda")
+        for b, L in enumerate(lens):
+            g.manual_seed(5_000_000 + b)
+            k = torch.randn((1, L, 8, 128), generator=g, device="cuda").half()
+            v = torch.randn((1, L, 8, 128), generator=g, device="cuda").half()
+            binding.kv_quant_append(pool, 0, k, v, torch.zeros(1, dtype=torch.int32, device="cuda"),
+                                    ptd[b:b + 1])
+        lens_d = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        ns = binding.attn_decode_n_splits(pool, 16, pt.shape[1] * PS)
+        ws = pool.decode_workspace(16, 32, ns)
+        out = torch.empty((16, 32, 128), dtype=torch.float32, device="cuda")
+        q = qs[0][:16].contiguous().cuda()
+        for _ in range(reps):
+            binding.attn_decode_int8(pool, 0, q, lens_d, ptd, out, ws, n_splits=ns)
+    elif name == "prefill":
+        run_prefill(n_iter=reps)
+    else:
+        raise SystemExit(f"unknown profile case {name}; one of {', '.join(PROFILE_CASES)}")
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": name, "reps": reps}), flush=True)
 
 
 def run_reference(args, rank, world, local):
@@ -678,10 +857,13 @@ def main():
     ap.add_argument("--copies", type=int, default=0, help="pool copies (0: enough to defeat L2)")
     ap.add_argument("--no-extra", action="store_true", help="skip the 128K measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
-    ap.add_argument("--batched", action="store_true",
-                    help="with --extra-only: also the 64-sequence paged batch (slow setup)")
+    ap.add_argument("--no-batched", action="store_true",
+                    help="skip the 64-sequence paged batch among the extra workloads")
     ap.add_argument("--extra-only", action="store_true",
-                    help="run only the 128K measurements and print them (profiling aid)")
+                    help="run only the extra workloads and print them (profiling aid)")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES,
+                    help="set up one workload and issue its call a few times, untimed "
+                         "(the commands of the ncu summaries under profiles/)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -696,15 +878,20 @@ def main():
         else:
             dist.init_process_group("gloo")
     try:
-        if args.extra_only:
+        if args.profile_case:
+            import torch
+
+            from int8_kv_cache_02_gb300 import build
+            build.build()
+            torch.cuda.set_device(local)
+            run_profile_case(args.profile_case)
+        elif args.extra_only:
             import torch
 
             from int8_kv_cache_02_gb300 import build
             build.build()
             torch.cuda.set_device(local)
             res = run_extra(args)
-            if args.batched:
-                res["batched"] = run_batched()
             print(json.dumps(res), flush=True)
         elif args.impl == "reference":
             run_reference(args, rank, world, local)

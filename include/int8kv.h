@@ -26,16 +26,28 @@
  *     causal within the window (Strata #2698 "What it does": the verify
  *     windows of speculative decoding go through the decode kernels).
  *
- * Store variants (Strata #2698 "What it does": k8v8, and one-store variants):
+ * Store variants (Strata #2698 "What it does": k8v8, and one-store variants;
+ * "Not in this PR": k8v4 with the Hadamard rotation over head_dim 256):
  *     INT8KV_K8V8  K and V int8 with scales
  *     INT8KV_K8V16 K int8 with scales, V fp16
  *     INT8KV_K16V8 K fp16, V int8 with scales
+ *     INT8KV_K8V4  K int8 with scales; V rotated by the normalised fast
+ *                  Walsh-Hadamard transform over head_dim (y = H v / sqrt(D),
+ *                  butterflies in fp32 stage by stage, h = 1, 2, ..., D/2) and
+ *                  stored as Q4_0: blocks of 32 values, d = m * (-1/8) with m
+ *                  the block's first value of largest magnitude, code
+ *                  min(15, floor(fl(fl(x * (1/d)) + 8.5))), stored fp16(d) and
+ *                  two codes per byte (value 2i in the low nibble of byte i),
+ *                  value (code - 8) * d.  Decode rotates its output back.
+ *                  Served by the CUDA-core decode kernel; no prefill chunk.
  *
  * Pool layout in device memory (caller-allocated; the library never
  * allocates device memory):
  *     int8 store   int8    [n_layers][n_pages][n_kv_heads][page_size][head_dim]
  *     fp16 store   fp16    [n_layers][n_pages][n_kv_heads][page_size][head_dim]
+ *     4-bit store  uint8   [n_layers][n_pages][n_kv_heads][page_size][head_dim/2]
  *     scales       fp16    [n_layers][n_pages][n_kv_heads][page_size][head_dim/group_size]
+ *                          (of the 4-bit store: [...][head_dim/32])
  * Position p of sequence b lives on physical page page_table[b*max_pages + p/page_size],
  * slot p % page_size.
  *
@@ -90,7 +102,8 @@ extern "C" {
 typedef enum {
   INT8KV_K8V8 = 0,
   INT8KV_K8V16 = 1,
-  INT8KV_K16V8 = 2
+  INT8KV_K16V8 = 2,
+  INT8KV_K8V4 = 3
 } int8kv_variant;
 
 /* Regions of a pool, for int8kv_pool_region_bytes. */

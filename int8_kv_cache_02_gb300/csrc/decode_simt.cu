@@ -18,10 +18,13 @@
 // store variant); the tensor-core kernel in decode_mma.cu serves the shapes it
 // is specialised for.
 
+#include <cmath>
+
 #include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "decode_common.cuh"
+#include "q4_row.cuh"
 
 namespace int8kv {
 namespace {
@@ -52,9 +55,27 @@ __device__ __forceinline__ void load_row(const void* store, bool is_int8, const 
   }
 }
 
+// A row of the 4-bit store (k8v4): the lane's VPL values (code - 8) * d, in the
+// rotated basis, its block's fp16 scale d.
+template <int VPL>
+__device__ __forceinline__ void load_row_q4(const void* store, const uint16_t* scales, size_t row,
+                                            int D, int lane, float (&x)[VPL]) {
+  const uint8_t* src = (const uint8_t*)store + row * (D / 2) + lane * (VPL / 2);
+  uint32_t w;
+  if constexpr (VPL == 8)
+    w = __ldg(reinterpret_cast<const uint32_t*>(src));
+  else if constexpr (VPL == 4)
+    w = __ldg(reinterpret_cast<const uint16_t*>(src));
+  else
+    w = __ldg(src);
+  const float d = h2f(__ldg(scales + row * (D / 32) + (lane * VPL) / 32));
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) x[i] = (float)((int)((w >> (4 * i)) & 15u) - 8) * d;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeArgs a, bool k_int8,
-                                                                   bool v_int8) {
+                                                                   bool v_int8, float fwht_norm) {
   constexpr int VPL = D / 32;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -63,6 +84,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeArgs a, 
 
   __shared__ float s_m[kWarps][8], s_l[kWarps][8];
   __shared__ float s_o[kWarps][8][D];
+  __shared__ float s_r[8][D], s_M[8], s_L[8];   // k8v4: merged rows before the rotation back
 
   float qr[8][VPL];
 #pragma unroll
@@ -92,7 +114,10 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeArgs a, 
     const size_t row = row_index(p, pg, kvh, j % p.ps);
     float kf[VPL], vf[VPL];
     load_row<VPL>(p.k, k_int8, p.ks, row, D, p.ng, p.gs, lane, kf);
-    load_row<VPL>(p.v, v_int8, p.vs, row, D, p.ng, p.gs, lane, vf);
+    if (p.v4)
+      load_row_q4<VPL>(p.v, p.vs, row, D, lane, vf);
+    else
+      load_row<VPL>(p.v, v_int8, p.vs, row, D, p.ng, p.gs, lane, vf);
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
       if (g < G) {
@@ -140,12 +165,41 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeArgs a, 
       }
     }
     const size_t h = (size_t)b * a.H + kvh * G + g;
+    if (p.v4) {   // the merged row is in the rotated basis: rotated back below
+      if (d == 0) {
+        s_M[g] = M;
+        s_L[g] = Ls;
+      }
+      s_r[g][d] = O;
+      continue;
+    }
     if (a.n_splits == 1) {
       a.out[h * D + d] = Ls > 0.f ? O / Ls : 0.f;
     } else {
       a.ws.part_o[(h * a.n_splits + split) * D + d] = O;
       if (d == 0) a.ws.part_ml[h * a.n_splits + split] = make_float2(M, Ls);
     }
+  }
+  if (!p.v4) return;
+  // k8v4: rotate each merged row back (the FWHT is its own inverse; the combine
+  // of the splits is linear in their rows, so each split's row is rotated here)
+  __syncthreads();
+  for (int g = warp; g < G; g += kWarps) {
+    float x[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) x[i] = s_r[g][lane * VPL + i];
+    fwht_row<VPL>(x, lane, fwht_norm);
+    const size_t h = (size_t)b * a.H + kvh * G + g;
+    const float Ls = s_L[g];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int d = lane * VPL + i;
+      if (a.n_splits == 1)
+        a.out[h * D + d] = Ls > 0.f ? x[i] / Ls : 0.f;
+      else
+        a.ws.part_o[(h * a.n_splits + split) * D + d] = x[i];
+    }
+    if (a.n_splits > 1 && lane == 0) a.ws.part_ml[h * a.n_splits + split] = make_float2(s_M[g], Ls);
   }
 }
 
@@ -154,15 +208,16 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeArgs a, 
 cudaError_t launch_decode_simt(const DecodeArgs& a, bool k_int8, bool v_int8,
                                cudaStream_t stream) {
   const dim3 grid(a.n_splits, a.pool.Hkv, a.B);
+  const float norm = (float)(1.0 / std::sqrt((double)a.pool.D));   // FWHT scaling (k8v4)
   switch (a.pool.D) {
     case 64:
-      decode_simt_kernel<64><<<grid, kWarps * 32, 0, stream>>>(a, k_int8, v_int8);
+      decode_simt_kernel<64><<<grid, kWarps * 32, 0, stream>>>(a, k_int8, v_int8, norm);
       break;
     case 128:
-      decode_simt_kernel<128><<<grid, kWarps * 32, 0, stream>>>(a, k_int8, v_int8);
+      decode_simt_kernel<128><<<grid, kWarps * 32, 0, stream>>>(a, k_int8, v_int8, norm);
       break;
     case 256:
-      decode_simt_kernel<256><<<grid, kWarps * 32, 0, stream>>>(a, k_int8, v_int8);
+      decode_simt_kernel<256><<<grid, kWarps * 32, 0, stream>>>(a, k_int8, v_int8, norm);
       break;
     default:
       return cudaErrorNotSupported;

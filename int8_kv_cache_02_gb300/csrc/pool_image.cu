@@ -44,19 +44,28 @@ __host__ __device__ inline size_t pad16(size_t n) { return (n + 15) / 16 * 16; }
 
 struct ImageShape {
   int n_layers, Hkv, D, ng;
-  bool k8, v8;
+  bool k8, v8, v4;
 };
 
 ImageShape shape_of(const int8kv_pool* p) {
-  return ImageShape{p->n_layers, p->n_kv_heads, p->head_dim, p->n_groups, p->k_int8, p->v_int8};
+  return ImageShape{p->n_layers, p->n_kv_heads, p->head_dim, p->n_groups,
+                    p->k_int8, p->v_int8, p->v_q4};
+}
+
+// Bytes of one row (position, kv head) of each region: K store, V store, K
+// scales, V scales (0: no such region).
+__host__ __device__ inline void row_bytes_of(const ImageShape& s, long long (&r)[4]) {
+  r[0] = (long long)s.D * (s.k8 ? 1 : 2);
+  r[1] = s.v4 ? s.D / 2 : (long long)s.D * (s.v8 ? 1 : 2);
+  r[2] = s.k8 ? s.ng * 2 : 0;
+  r[3] = s.v4 ? (s.D / 32) * 2 : (s.v8 ? s.ng * 2 : 0);
 }
 
 // Bytes of the four sections of one (sequence, layer) with L positions.
 __host__ __device__ inline void section_bytes(const ImageShape& s, long long L, long long (&b)[4]) {
-  b[0] = L * s.Hkv * s.D * (s.k8 ? 1 : 2);
-  b[1] = L * s.Hkv * s.D * (s.v8 ? 1 : 2);
-  b[2] = s.k8 ? L * s.Hkv * s.ng * 2 : 0;
-  b[3] = s.v8 ? L * s.Hkv * s.ng * 2 : 0;
+  long long r[4];
+  row_bytes_of(s, r);
+  for (int i = 0; i < 4; ++i) b[i] = L * s.Hkv * r[i];
 }
 
 __host__ __device__ inline long long layer_bytes(const ImageShape& s, long long L) {
@@ -101,15 +110,15 @@ __global__ void __launch_bounds__(kThreadsImg) image_kernel(PoolView pv, ImageSh
     s_page[i] = lookup_page(page_table + (size_t)b * max_pages, pos / pv.ps, max_pages, pv);
   }
   __syncthreads();
-  const unsigned char* pk = (const unsigned char*)pv.k + (size_t)layer * pool_layer_rows * s.D * (s.k8 ? 1 : 2);
-  const unsigned char* pvv = (const unsigned char*)pv.v + (size_t)layer * pool_layer_rows * s.D * (s.v8 ? 1 : 2);
-  const unsigned char* pks = (const unsigned char*)(pv.ks) + (s.k8 ? (size_t)layer * pool_layer_rows * s.ng * 2 : 0);
-  const unsigned char* pvs = (const unsigned char*)(pv.vs) + (s.v8 ? (size_t)layer * pool_layer_rows * s.ng * 2 : 0);
+  long long rb[4];
+  row_bytes_of(s, rb);
+  const void* region[4] = {pv.k, pv.v, pv.ks, pv.vs};   // layer 0 of each region
   long long sec = off;
   for (int q = 0; q < 4; ++q) {
     if (sb[q] == 0) continue;
-    const unsigned char* base = q == 0 ? pk : q == 1 ? pvv : q == 2 ? pks : pvs;
-    const int row_bytes = (int)(sb[q] / ((long long)L * s.Hkv));   // bytes of one (position, head) row
+    const int row_bytes = (int)rb[q];                                // bytes of one (position, head) row
+    const unsigned char* base =
+        (const unsigned char*)region[q] + (size_t)layer * pool_layer_rows * row_bytes;
     unsigned char* dst0 = img + sec + (long long)p0 * s.Hkv * row_bytes;
     if (row_bytes % 16 == 0) {
       const int vpr = row_bytes / 16;                               // 16-byte pieces per row

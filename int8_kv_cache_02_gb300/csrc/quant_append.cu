@@ -14,9 +14,12 @@
 // absmax of a group of gs values is a butterfly max over the gs/VPL lanes that
 // hold it.  HBM-bound: per row 2*D bytes in, D + 2*D/gs bytes out per store.
 
+#include <cmath>
+
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "q4_row.cuh"
 #include "quant_row.cuh"
 
 namespace int8kv {
@@ -27,7 +30,7 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
     PoolView p, const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
     int n_seqs, int n_new, const int32_t* __restrict__ seq_pos,
     const int32_t* __restrict__ page_table, int max_pages, bool k_int8, bool v_int8,
-    int pos_offset) {
+    int pos_offset, float fwht_norm) {
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const long long n_rows = (long long)n_seqs * n_new * p.Hkv;
@@ -51,7 +54,10 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
                       (uint16_t*)p.ks + dst_row * p.ng, lane, lpg);
   else
     copy_row<VPL>(k_new + src_off, (uint16_t*)p.k + dst_row * p.D, lane);
-  if (v_int8)
+  if (p.v4)   // k8v4: rotated, then Q4_0 (D/2 bytes and D/32 scales per row)
+    quantize_row_q4<VPL>(v_new + src_off, (uint8_t*)p.v + dst_row * (p.D / 2),
+                         (uint16_t*)p.vs + dst_row * (p.D / 32), lane, fwht_norm);
+  else if (v_int8)
     quantize_row<VPL>(v_new + src_off, (int8_t*)p.v + dst_row * p.D,
                       (uint16_t*)p.vs + dst_row * p.ng, lane, lpg);
   else
@@ -68,21 +74,22 @@ cudaError_t launch_quant_append(const PoolView& pool, const uint16_t* k_new, con
   if (rows == 0) return cudaSuccess;
   const int warps = 8;
   const unsigned grid = (unsigned)((rows + warps - 1) / warps);
+  const float norm = (float)(1.0 / std::sqrt((double)pool.D));   // FWHT scaling of the 4-bit store
   switch (pool.D) {
     case 64:
       quant_append_kernel<2><<<grid, warps * 32, 0, stream>>>(pool, k_new, v_new, n_seqs, n_new,
                                                               seq_pos, page_table, max_pages,
-                                                              k_int8, v_int8, pos_offset);
+                                                              k_int8, v_int8, pos_offset, norm);
       break;
     case 128:
       quant_append_kernel<4><<<grid, warps * 32, 0, stream>>>(pool, k_new, v_new, n_seqs, n_new,
                                                               seq_pos, page_table, max_pages,
-                                                              k_int8, v_int8, pos_offset);
+                                                              k_int8, v_int8, pos_offset, norm);
       break;
     case 256:
       quant_append_kernel<8><<<grid, warps * 32, 0, stream>>>(pool, k_new, v_new, n_seqs, n_new,
                                                               seq_pos, page_table, max_pages,
-                                                              k_int8, v_int8, pos_offset);
+                                                              k_int8, v_int8, pos_offset, norm);
       break;
     default:
       return cudaErrorNotSupported;

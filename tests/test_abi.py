@@ -106,3 +106,16 @@ def test_pool_image_calls_reject_null_arguments(L):
     assert L.kv_pool_load(None, None, 0, 1, None, 1, None, 0, None, None) == -2
     from int8_kv_cache_02_gb300 import binding as b
     assert b.int8kv_status_string(-9).startswith("pool image")
+
+
+def test_k8v4_region_bytes(L):
+    """k8v4: K int8 codes + fp16 scales per group; V two 4-bit codes per byte and one
+    fp16 scale per 32 values (head_dim 256, 2 kv heads: 512 + 16 B of K and
+    256 + 32 B of V per position)."""
+    from int8_kv_cache_02_gb300 import binding as b
+    r = [b.int8kv_pool_region_bytes(1, 2, 256, 64, 64, 1, b.K8V4, k) for k in range(4)]
+    assert r == [64 * 512, 64 * 256, 64 * 16, 64 * 32]
+    a16 = ctypes.c_void_p(0x10000)
+    h = ctypes.c_void_p()
+    # the 4-bit store needs its scales
+    assert L.kv_pool_create(ctypes.byref(h), 1, 2, 256, 64, 64, 4, 3, a16, a16, a16, None, None) == -2
