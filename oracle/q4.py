@@ -25,8 +25,12 @@ Q4_0 (the ggml 4-bit format: blocks of 32 values, one fp16 scale each):
     stored: q (4 bits, 0..15) and fp16_rne(d); value (q - 8) * fp16(d)
   so the block's largest value maps to code 0 (-8 d), and codes run 0..15.
 
-Store layout: a row of D values is D/2 bytes, byte i holding value 2i in its
-low nibble and value 2i + 1 in its high nibble; scales fp16 [D/32] per row.
+Store layout (this library's own; the pages give none): a row of D values is
+D/2 bytes in 8 chunks of D/16 bytes.  Chunk r holds two bytes per block g of
+32 values: byte (D/16)*r + 2g + h holds value 32g + 4r + 2h in its low nibble
+and value 32g + 4r + 2h + 1 in its high nibble (r = 0..7, h = 0, 1).  So the
+8 chunks each carry 4 values of every block, which the tensor-core decode
+loads as one 16-byte piece per row and thread.  Scales: fp16 [D/32] per row.
 """
 
 import numpy as np
@@ -77,18 +81,34 @@ def q4_0_dequantize(codes, d16):
     return ((q.reshape(q.shape[:-1] + (D // BLOCK, BLOCK)) - 8.0) * d).reshape(q.shape)
 
 
+def byte_of_value(v, D):
+    """(byte, nibble) of value v in a packed row of D values (layout above)."""
+    g, w = divmod(v, BLOCK)
+    r, j = divmod(w, 4)
+    return (D // 16) * r + 2 * g + j // 2, j % 2
+
+
 def pack(codes):
-    """uint8 codes [..., D] (0..15) -> bytes [..., D // 2]: value 2i low nibble, 2i+1 high."""
+    """uint8 codes [..., D] (0..15) -> bytes [..., D // 2] in the layout above."""
     c = np.asarray(codes, dtype=np.uint8)
-    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+    D = c.shape[-1]
+    assert D % BLOCK == 0
+    out = np.zeros(c.shape[:-1] + (D // 2,), np.uint8)
+    for v in range(0, D, 2):          # values v (low nibble) and v + 1 (high) share a byte
+        byte, nib = byte_of_value(v, D)
+        assert nib == 0 and byte_of_value(v + 1, D) == (byte, 1)
+        out[..., byte] = c[..., v] | (c[..., v + 1] << 4)
+    return out
 
 
 def unpack(packed):
     """bytes [..., D // 2] -> codes [..., D]."""
     p = np.asarray(packed, dtype=np.uint8)
-    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), np.uint8)
-    out[..., 0::2] = p & 0x0F
-    out[..., 1::2] = p >> 4
+    D = 2 * p.shape[-1]
+    out = np.empty(p.shape[:-1] + (D,), np.uint8)
+    for v in range(D):
+        byte, nib = byte_of_value(v, D)
+        out[..., v] = (p[..., byte] >> (4 * nib)) & 0x0F
     return out
 
 
@@ -106,12 +126,16 @@ def dequantize_rows(packed, d16):
     return hadamard_fp64(r)
 
 
+_H = {}
+
+
 def hadamard_fp64(x):
     """H x / sqrt(n) in fp64 along the last axis, straight from the definition
     H_ij = (-1)^popcount(i & j)."""
     x = np.asarray(x, np.float64)
     n = x.shape[-1]
-    i = np.arange(n)
-    pc = np.vectorize(lambda v: bin(v).count("1"))(i[:, None] & i[None, :])
-    H = np.where(pc % 2 == 0, 1.0, -1.0) / np.sqrt(n)
-    return x @ H.T
+    if n not in _H:
+        i = np.arange(n)
+        pc = np.vectorize(lambda v: bin(v).count("1"))(i[:, None] & i[None, :])
+        _H[n] = np.where(pc % 2 == 0, 1.0, -1.0) / np.sqrt(n)
+    return x @ _H[n].T

@@ -67,10 +67,25 @@ def test_q4_0_error_bound_and_extreme_value():
     assert np.all(codes[np.arange(4000), first] == 0)
 
 
-def test_pack_is_two_values_per_byte_low_nibble_first():
-    c = np.array([[1, 2, 3, 4, 15, 0]], np.uint8)
-    assert q4.pack(c).tolist() == [[0x21, 0x43, 0x0F]]
-    assert np.array_equal(q4.unpack(q4.pack(c)), c)
+def test_pack_layout_hand_placed():
+    """Row of 64 values (2 blocks): byte 4r + 2g + h (chunks of 64/16 = 4 bytes)
+    holds values 32g + 4r + 2h (low nibble) and + 1 (high nibble)."""
+    c = np.zeros((1, 64), np.uint8)
+    c[0, 0], c[0, 1] = 1, 2          # g 0, r 0, h 0 -> byte 0
+    c[0, 2], c[0, 3] = 3, 4          # g 0, r 0, h 1 -> byte 1
+    c[0, 4] = 5                      # g 0, r 1, h 0 -> byte 4 (low)
+    c[0, 33] = 15                    # g 1, r 0, h 0 -> byte 2 (high)
+    c[0, 63] = 9                     # g 1, r 7, h 1 -> byte 4*7 + 2 + 1 = 31 (high)
+    b = q4.pack(c)[0]
+    assert b[0] == 0x21 and b[1] == 0x43 and b[4] == 0x05 and b[2] == 0xF0 and b[31] == 0x90
+    assert np.count_nonzero(b) == 5
+    rng = np.random.default_rng(1)
+    for D in (64, 128, 256):
+        r = rng.integers(0, 16, (3, D)).astype(np.uint8)
+        assert np.array_equal(q4.unpack(q4.pack(r)), r)
+        # every byte of a row is written exactly once
+        seen = sorted(q4.byte_of_value(v, D)[0] for v in range(0, D, 2))
+        assert seen == list(range(D // 2))
 
 
 def test_fwht_hand_values():
@@ -130,3 +145,6 @@ def test_k8v4_pool_context_one_and_identical_keys():
     err = np.linalg.norm(vh - v.astype(np.float64), axis=-1) / np.linalg.norm(v.astype(np.float64), axis=-1)
     assert err.max() < 0.15 and err.mean() < 0.12          # 4-bit blocks of 32
     assert P.v_store.shape[-1] == 128 and P.v_scales.shape[-1] == 8
+    # thread-chunk layout: chunk r of a row holds values 32g + 4r .. 32g + 4r + 3 of every block
+    codes = q4.unpack(P.v_store[0, 0, 0, :1])[0]
+    assert codes.shape == (256,)
