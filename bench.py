@@ -738,7 +738,7 @@ def run_extra(args):
             out["long128k_windows"] = run_windows(st, 131072, n_iter=20)
         del st, g
         torch.cuda.empty_cache()
-    # k8v4 (V rotated + Q4_0; CUDA-core decode kernel) at 8K and 128K
+    # k8v4 (V rotated + Q4_0; tensor-core decode kernel) at 8K and 128K
     for name, wf, ctx in (("grouped8k_k8v4", inputs.grouped8k, CTX),
                           ("long128k_k8v4", inputs.long128k, 131072)):
         per = decode_bytes(ctx=ctx, v_int8=False, v_q4=True)
@@ -748,7 +748,7 @@ def run_extra(args):
         g = st.graph(n, append=False)
         us = time_graph(g) / n * 1e3
         out[name] = dict(rate(per, us, f"{copies} rotating pool copies"), n_splits=st.n_splits,
-                         kernel="decode_simt_kernel + decode_combine_kernel")
+                         kernel="decode_mma_kernel (4-bit V) + decode_combine_kernel")
         del st, g
         torch.cuda.empty_cache()
     if not getattr(args, "no_batched", False):

@@ -37,9 +37,11 @@
  *                  stored as Q4_0: blocks of 32 values, d = m * (-1/8) with m
  *                  the block's first value of largest magnitude, code
  *                  min(15, floor(fl(fl(x * (1/d)) + 8.5))), stored fp16(d) and
- *                  two codes per byte (value 2i in the low nibble of byte i),
- *                  value (code - 8) * d.  Decode rotates its output back.
- *                  Served by the CUDA-core decode kernel; no prefill chunk.
+ *                  two codes per byte: byte (D/16)*r + 2g + h of a row holds
+ *                  value 32g + 4r + 2h in its low nibble and the next value in
+ *                  its high nibble (r = 0..7, h = 0..1, g the 32-value block);
+ *                  value (code - 8) * d.  Decode rotates its output back.  No
+ *                  prefill chunk.
  *
  * Pool layout in device memory (caller-allocated; the library never
  * allocates device memory):

@@ -55,6 +55,7 @@
 // position masks each column's keys beyond its query.
 
 #include <climits>
+#include <type_traits>
 
 #include <cooperative_groups.h>
 #include <cuda.h>
@@ -63,6 +64,7 @@
 #include "common.cuh"
 #include "decode_common.cuh"
 #include "mma_common.cuh"
+#include "q4_row.cuh"
 #include "quant_row.cuh"
 #include "ptx.cuh"
 
@@ -97,9 +99,9 @@ __device__ __forceinline__ int column_group(int Hkv) {
   return y / Hkv;
 }
 
-template <int D, bool KI8, bool VI8>
-struct Layout : mma::StagedPage<D, KI8, VI8> {
-  using SP = mma::StagedPage<D, KI8, VI8>;
+template <int D, bool KI8, bool VI8, bool VQ4>
+struct Layout : mma::StagedPage<D, KI8, VI8, VQ4> {
+  using SP = mma::StagedPage<D, KI8, VI8, VQ4>;
   // stage budget: three blocks per SM at head_dim 256, four at 128 (whose
   // accumulators fit in the 128 registers that leaves a thread)
   static constexpr int NS_FIT = ((D == 128 ? 52 : 70) * 1024) / SP::STAGE;
@@ -109,7 +111,7 @@ struct Layout : mma::StagedPage<D, KI8, VI8> {
   // stores conflict free: with int8 V a lane holds dims 8r + 2m (+1) of heads
   // 2t, 2t+1, placed at d + d/32 in rows of pitch = 1 (mod 16); with fp16 V,
   // dims r (+8) of the same heads in rows of pitch D + 4 (= 4 mod 16).
-  static constexpr int DP = VI8 ? ((D + D / 32) / 16 + 1) * 16 + 1 : D + 4;
+  static constexpr int DP = (VI8 || VQ4) ? ((D + D / 32) / 16 + 1) * 16 + 1 : D + 4;
   static constexpr int MERGE = kConsumerWarps * 8 * DP * 4 + 8 * D * 4;
   static constexpr int BARS = NS * SP::STAGE;
   static constexpr int SMEM = 1024 + BARS + 2 * NS * 8 + NS * 4 + 64;   // stages, barriers, page ids
@@ -118,7 +120,7 @@ struct Layout : mma::StagedPage<D, KI8, VI8> {
   // where the tile arithmetic paces the kernel (int8 K and V at head_dim 256):
   // there the smaller first burst lets every block start computing sooner; the
   // byte-bound variants lose more from the shallower start than they gain.
-  static constexpr bool DEFER = D == 256 && KI8 && VI8;
+  static constexpr bool DEFER = D == 256 && KI8 && (VI8 || VQ4);
 };
 
 // Codes at byte k of W0 and W1 -> exact f16x2 (lo = W0's, hi = W1's).
@@ -128,7 +130,26 @@ __device__ __forceinline__ uint32_t v_pair(uint32_t w0, uint32_t w1, int k) {
   return sub1152(lop_i8pair(ptx::prmt(w0, w1, sel)));
 }
 
-template <int D, bool KI8, bool VI8>
+// 4-bit store: x holds byte b of two keys' chunk words (bytes 0 and 2, and their
+// copies in bytes 1 and 3, as v_pair arranges them).  The low nibbles become
+// the f16x2 pair (q0 - 8, q1 - 8) with 0x6400 | q = 1024 + q and one subtraction
+// of 1032; the high nibbles with 0x6400 | 16 q = 1024 + 16 q, times 1/16, minus
+// 72.  All exact in fp16.
+__device__ __forceinline__ uint32_t q4_lo(uint32_t x) {
+  const uint32_t h = (x & 0x000F000Fu) | 0x64006400u;
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h),
+                            __half2half2(__ushort_as_half(0x6408)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t q4_hi(uint32_t x) {
+  const uint32_t h = (x & 0x00F000F0u) | 0x64006400u;
+  const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&h),
+                            __half2half2(__ushort_as_half(0x2C00)),
+                            __half2half2(__ushort_as_half(0xD480)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+template <int D, bool KI8, bool VI8, bool VQ4>
 __device__ __forceinline__ void issue_page(unsigned char* smem, uint64_t* full, int* stage_page,
                                            int st, int page, int row, const PoolView& p, int kvh,
                                            const CUtensorMap* tmk, const CUtensorMap* tmv,
@@ -138,7 +159,7 @@ __device__ __forceinline__ void issue_page(unsigned char* smem, uint64_t* full, 
     ptx::mbar_arrive_expect_tx(&full[st], 16);
     return;
   }
-  mma::issue_page<D, KI8, VI8, true>(smem + st * Layout<D, KI8, VI8>::STAGE, &full[st],
+  mma::issue_page<D, KI8, VI8, true, VQ4>(smem + st * Layout<D, KI8, VI8, VQ4>::STAGE, &full[st],
                                      &stage_page[st], page, row, p, kvh, tmk, tmv);
 }
 
@@ -215,20 +236,61 @@ struct NewRow {
   }
 };
 
+// The new token's V row for the 4-bit store (head_dim 256, 8 values a lane):
+// rotated and quantized by the warp as the append kernel does it, then written
+// over its staged row and to the pool in the chunked nibble order.
+struct NewRowQ4 {
+  static constexpr int D = 256, VPL = 8;
+  uint4 raw;
+  uint32_t packed;
+  uint16_t scale;
+  __device__ __forceinline__ void fetch(const uint16_t* src, int lane) {
+    raw = *reinterpret_cast<const uint4*>(src + lane * VPL);
+  }
+  __device__ __forceinline__ void quantize(int) {
+    float x[VPL];
+    const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+    for (int i = 0; i < VPL / 2; ++i) {
+      const float2 f = __half22float2(h2[i]);
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+    fwht_row<VPL>(x, threadIdx.x & 31, 0.0625f);
+    packed = q4_0_regs<VPL>(x, threadIdx.x & 31, scale);
+  }
+  __device__ __forceinline__ void stage(unsigned char* boxes, unsigned char* scales, int slot,
+                                        int lane, int, int) const {
+#pragma unroll
+    for (int q = 0; q < VPL / 2; ++q) {
+      const int byte = q4_byte_of(lane * VPL + 2 * q, D);
+      boxes[slot * 128 + ((((byte >> 4) ^ (slot & 7))) << 4) + (byte & 15)] = (uint8_t)(packed >> (8 * q));
+    }
+    if (lane % 4 == 0) reinterpret_cast<uint16_t*>(scales)[slot * (D / 32) + lane / 4] = scale;
+  }
+  __device__ __forceinline__ void store(void* values, uint16_t* scales, size_t row, int lane, int,
+                                        int) const {
+#pragma unroll
+    for (int q = 0; q < VPL / 2; ++q)
+      ((uint8_t*)values)[row * (D / 2) + q4_byte_of(lane * VPL + 2 * q, D)] = (uint8_t)(packed >> (8 * q));
+    if (lane % 4 == 0) scales[row * (D / 32) + lane / 4] = scale;
+  }
+};
+
 // One 16-token tile of one page for one warp: scores for the G heads, online
 // softmax (lazy: the reference max moves only when a score exceeds it by more
 // than 2^kTau), and the P.V accumulation.  FULL: every token of the tile is in
 // [j0, j1), so no masking.
-template <int D, bool KI8, bool VI8, int NG, bool FULL>
+template <int D, bool KI8, bool VI8, int NG, bool FULL, bool VQ4>
 __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, int lane, int tile0,
                                             int j0, int j1, const uint32_t (&qf)[D / 16][2],
                                             float scale_log2, float (&o)[D / 16][4], float& m0,
                                             float& m1, float& l0, float& l1, float (&cap)[NG],
                                             float (&sh)[NG], int (&vexp)[NG], int lim0, int lim1) {
-  using LY = Layout<D, KI8, VI8>;
+  using LY = Layout<D, KI8, VI8, VQ4>;
   constexpr int MACROS = D / 64, MTILES = D / 16;
-  constexpr int NGV = VI8 ? NG : 1;
-  constexpr int MPG = MACROS / NGV;   // 64-dim macros per V scale group
+  constexpr int NGV = VQ4 ? D / 32 : (VI8 ? NG : 1);   // V scale groups (4-bit store: of 32)
+  constexpr int MPG = VQ4 ? 0 : MACROS / NGV;   // 64-dim macros per V scale group
   const int r = lane >> 2, t = lane & 3;
   const int rowA = rho(r), rowB = rowA + 8;
   const int trA = warp * 16 + rowA, trB = warp * 16 + rowB;   // rows within the page
@@ -386,9 +448,107 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
       wa[g] = va[g] * sh[g];
       wb[g] = vb[g] * sh[g];
     }
+  } else if constexpr (VQ4) {
+    // 4-bit store: D/32 signed scales per key (d = m * -1/8).  One range 2^e per
+    // warp bounds |d| of every block (index 0 of the range arrays): the rotation
+    // makes the blocks' scales of a key alike, and a block far below the range
+    // only loses bits of weights that are already negligible.
+    float va[NGV], vb[NGV];
+    {
+      const uint4 xa = *reinterpret_cast<const uint4*>(sb + LY::VS_OFF + trA * (NGV * 2));
+      const uint4 xb = *reinterpret_cast<const uint4*>(sb + LY::VS_OFF + trB * (NGV * 2));
+      const uint32_t wa32[4] = {xa.x, xa.y, xa.z, xa.w}, wb32[4] = {xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&wa32[i]));
+        const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&wb32[i]));
+        va[2 * i] = fa.x;
+        va[2 * i + 1] = fa.y;
+        vb[2 * i] = fb.x;
+        vb[2 * i + 1] = fb.y;
+      }
+    }
+    float mx = 0.f;
+#pragma unroll
+    for (int g = 0; g < NGV; ++g) {
+      if constexpr (!FULL) {
+        va[g] = vA ? va[g] : 0.f;
+        vb[g] = vB ? vb[g] : 0.f;
+      }
+      mx = fmaxf(mx, fmaxf(fabsf(va[g]), fabsf(vb[g])));
+    }
+    if (__any_sync(0xffffffffu, mx >= cap[0])) {
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      if (mx >= cap[0]) {   // warp-uniform
+        const int ne = exponent_of(mx) + 1;
+        if (vexp[0] != INT_MIN) {
+          const float f = pow2f(vexp[0] - ne);
+#pragma unroll
+          for (int j = 0; j < MTILES; ++j) {
+            o[j][0] *= f;
+            o[j][1] *= f;
+            o[j][2] *= f;
+            o[j][3] *= f;
+          }
+        }
+        vexp[0] = ne;
+        cap[0] = pow2f(ne);
+        sh[0] = pow2f(kPShift - ne);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < NGV; ++g) {
+      wa[g] = va[g] * sh[0];
+      wb[g] = vb[g] * sh[0];
+    }
   } else {
     wa[0] = (FULL || vA) ? pow2f(kPShift) : 0.f;
     wb[0] = (FULL || vB) ? pow2f(kPShift) : 0.f;
+  }
+
+  if constexpr (VQ4) {
+    // ---- P.V for the 4-bit store: each key's chunk r (16 bytes: values
+    // 32g + 4r .. 32g + 4r + 3 of every block g) is one load; M-tile (g, h) takes
+    // rows r <-> value 32g + 4r + 2h (low nibble of byte 2g + h), r + 8 <-> the
+    // next value (high nibble)
+    const int tk[4] = {warp * 16 + tokS0, warp * 16 + tokS1, warp * 16 + 8 + tokS0,
+                       warp * 16 + 8 + tokS1};
+    uint4 qv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      qv[j] = *reinterpret_cast<const uint4*>(sb + LY::V_OFF + tk[j] * 128 + ((r ^ (tk[j] & 7)) << 4));
+#pragma unroll
+    for (int g = 0; g < NGV; ++g) {
+      const float p0 = pr[0] * wa[g], p1 = pr[1] * wa[g], p2 = pr[2] * wb[g], p3 = pr[3] * wb[g];
+      const uint32_t h01 = ptx::pack_f16x2(p0, p1), h23 = ptx::pack_f16x2(p2, p3);
+      const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+      const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+      const uint32_t e01 = ptx::pack_f16x2(p0 - f01.x, p1 - f01.y);
+      const uint32_t e23 = ptx::pack_f16x2(p2 - f23.x, p3 - f23.y);
+      const uint32_t bh0 = ptx::movmatrix_trans(h01), bh1 = ptx::movmatrix_trans(h23);
+      const uint32_t bl0 = ptx::movmatrix_trans(e01), bl1 = ptx::movmatrix_trans(e23);
+      const int wi = g >> 1;   // the word of the chunk that holds block g's bytes
+      const uint32_t w0 = wi == 0 ? qv[0].x : wi == 1 ? qv[0].y : wi == 2 ? qv[0].z : qv[0].w;
+      const uint32_t w1 = wi == 0 ? qv[1].x : wi == 1 ? qv[1].y : wi == 2 ? qv[1].z : qv[1].w;
+      const uint32_t w2 = wi == 0 ? qv[2].x : wi == 1 ? qv[2].y : wi == 2 ? qv[2].z : qv[2].w;
+      const uint32_t w3 = wi == 0 ? qv[3].x : wi == 1 ? qv[3].y : wi == 2 ? qv[3].z : qv[3].w;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int bsel = 2 * (g & 1) + hh;   // byte 2g + hh of the chunk, within word wi
+        const uint32_t sel = (uint32_t)bsel | ((uint32_t)bsel << 4) | ((uint32_t)(4 + bsel) << 8) |
+                             ((uint32_t)(4 + bsel) << 12);
+        const uint32_t x01 = ptx::prmt(w0, w1, sel), x23 = ptx::prmt(w2, w3, sel);
+        uint32_t af[4];
+        af[0] = q4_lo(x01);
+        af[1] = q4_hi(x01);
+        af[2] = q4_lo(x23);
+        af[3] = q4_hi(x23);
+        ptx::mma_f16(o[2 * g + hh], af, bh0, bh1);
+        ptx::mma_f16(o[2 * g + hh], af, bl0, bl1);
+      }
+    }
+    return;
   }
 
   // ---- P.V per V group: P' as an f16 hi + lo pair, transposed into the B fragment
@@ -465,11 +625,11 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
 // WIN: a window of q_len queries per sequence (attn_decode_multi_int8); without
 // it the kernel serves one query per sequence and none of the window's column
 // arithmetic is compiled in.
-template <int D, bool KI8, bool VI8, int NG, bool WIN>
+template <int D, bool KI8, bool VI8, int NG, bool WIN, bool VQ4>
 __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 3)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, int layer_page0) {
-  using LY = Layout<D, KI8, VI8>;
+  using LY = Layout<D, KI8, VI8, VQ4>;
   constexpr int KSTEPS = D / 16;     // 16-dim k-steps of q.K^T
   constexpr int MACROS = D / 64;     // 64-dim groups
   constexpr int MTILES = D / 16;     // 16-dim M-tiles of P.V
@@ -530,9 +690,11 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     if (pg >= 0 && pg < p.n_pages) {
       const size_t r0 = ((size_t)pg * p.Hkv + kvh) * kPage;   // first row of the page-head
       ptx::bulk_prefetch_l2((const char*)p.k + r0 * D * (KI8 ? 1 : 2), (KI8 ? 1 : 2) * D * kPage);
-      ptx::bulk_prefetch_l2((const char*)p.v + r0 * D * (VI8 ? 1 : 2), (VI8 ? 1 : 2) * D * kPage);
+      constexpr int VROW = VQ4 ? D / 2 : (VI8 ? D : 2 * D);   // bytes of a V row
+      ptx::bulk_prefetch_l2((const char*)p.v + r0 * VROW, VROW * kPage);
       if (KI8) ptx::bulk_prefetch_l2(p.ks + r0 * NG, kPage * NG * 2);
       if (VI8) ptx::bulk_prefetch_l2(p.vs + r0 * NG, kPage * NG * 2);
+      if (VQ4) ptx::bulk_prefetch_l2(p.vs + r0 * (D / 32), kPage * (D / 32) * 2);
     }
   }
   ptx::grid_dependency_wait();
@@ -601,7 +763,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   const bool app_k = appends && warp == app_slot / 16;
   const bool app_v = appends && warp == ((app_slot / 16) ^ 1);
   NewRow<D, KI8> nk;
-  NewRow<D, VI8> nv;
+  std::conditional_t<VQ4, NewRowQ4, NewRow<D, VI8>> nv;
   if (app_k) nk.fetch(a.k_new + ((size_t)b * p.Hkv + kvh) * D, lane);
   if (app_v) nv.fetch(a.v_new + ((size_t)b * p.Hkv + kvh) * D, lane);
 
@@ -631,7 +793,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     for (int i = 0; i < LY::NS; ++i)
       if (i < n_pg) {
         if (i == 0 || appends || !LY::DEFER)
-          issue_page<D, KI8, VI8>(smem, full, stage_page, i, first[i], page_row(first[i]), p, kvh,
+          issue_page<D, KI8, VI8, VQ4>(smem, full, stage_page, i, first[i], page_row(first[i]), p, kvh,
                                   &tmk, &tmv, a.expire_polls != 0);
         else
           stage_page[i] = first[i];   // kept for the request after page 0 lands; no consumer
@@ -729,7 +891,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
         for (int k = 1; k < LY::NS; ++k)
           if (k < n_pg) {
             const int pg = stage_page[k];
-            issue_page<D, KI8, VI8>(smem, full, stage_page, k, pg, page_row(pg), p, kvh, &tmk,
+            issue_page<D, KI8, VI8, VQ4>(smem, full, stage_page, k, pg, page_row(pg), p, kvh, &tmk,
                                     &tmv, a.expire_polls != 0);
           }
       }
@@ -739,10 +901,10 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
         const unsigned char* sb = smem + st * LY::STAGE;
         // a tile that ends by the first query's position needs no per-column test
         if (tile0 >= j0 && tile0 + 16 <= j1 && (!WIN || tile0 + 16 <= s_q0[warp] + 1)) {
-          decode_tile<D, KI8, VI8, NG, true>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
+          decode_tile<D, KI8, VI8, NG, true, VQ4>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
                                              m0, m1, l0, l1, cap, sh, vexp, 0, 0);
         } else if constexpr (!WIN) {
-          decode_tile<D, KI8, VI8, NG, false>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
+          decode_tile<D, KI8, VI8, NG, false, VQ4>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
                                               m0, m1, l0, l1, cap, sh, vexp, INT_MAX, INT_MAX);
         } else {
           // causal limits of the lane's columns 2t, 2t + 1 (a dead column: L - 1)
@@ -750,7 +912,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
           auto lim = [&](int c) {
             return c < nc ? q0 + (column_group(p.Hkv) * 8 + c) / G : q0 + a.q_len - 1;
           };
-          decode_tile<D, KI8, VI8, NG, false>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
+          decode_tile<D, KI8, VI8, NG, false, VQ4>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
                                               m0, m1, l0, l1, cap, sh, vexp, lim(c0), lim(c0 + 1));
         }
       }
@@ -763,7 +925,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
             kConsumerWarps - 1) {
           if (i + LY::NS < n_pg) {
             const int page = page_of(i + LY::NS);
-            issue_page<D, KI8, VI8>(smem, full, stage_page, st, page, page_row(page), p, kvh,
+            issue_page<D, KI8, VI8, VQ4>(smem, full, stage_page, st, page, page_row(page), p, kvh,
                                     &tmk, &tmv, a.expire_polls != 0);
           }
         }
@@ -780,7 +942,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   __syncthreads();   // every stage consumed: the stage memory becomes the merge buffer
 
   constexpr int DP = LY::DP;
-  auto pos = [](int d) { return VI8 ? d + (d >> 5) : d; };   // place of dim d in a row
+  auto pos = [](int d) { return (VI8 || VQ4) ? d + (d >> 5) : d; };   // place of dim d in a row
   float* s_o = reinterpret_cast<float*>(smem);                // [warp][head 8][DP]
   if (r == 0) {
     s_m[warp][2 * t] = m0;
@@ -798,6 +960,10 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       dy = dx + 1;
       const int g = (mc * 64) / gs;
       u = vexp[g] == INT_MIN ? 0.f : pow2f(vexp[g] - kPShift);
+    } else if constexpr (VQ4) {   // M-tile (g, h) = j: rows r, r + 8 <-> values 32g + 4r + 2h, + 1
+      dx = 32 * (j >> 1) + 4 * r + 2 * (j & 1);
+      dy = dx + 1;
+      u = vexp[0] == INT_MIN ? 0.f : pow2f(vexp[0] - kPShift);
     } else {
       dx = mc * 64 + mt * 16 + r;
       dy = dx + 8;
@@ -826,7 +992,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   };
 
   // ---- this block's partial (M, L, O~) of its split
-  if (a.n_splits > kMaxCluster) {
+  if (!VQ4 && a.n_splits > kMaxCluster) {
     // many splits: the partial goes to the workspace and the combine kernel
     // (launched next, as a programmatic dependent) reduces the splits.
     // Thread: 4 consecutive dims (one 16-byte store) of heads g0, g0 + stride,
@@ -878,6 +1044,33 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       O = fmaf(s_o[((size_t)w * 8 + g) * DP + pos(d)], s_f[w][g], O);
     cta_o[g * D + d] = O;
   }
+  if constexpr (VQ4) {
+    // The 4-bit store's rows were rotated: rotate each column's merged row back
+    // (the FWHT is its own inverse, and the combine is linear in the rows).
+    // Warp w takes columns w, w + 4; a lane 8 consecutive dims.
+    __syncthreads();
+    for (int g = warp; g < nc; g += kConsumerWarps) {
+      float x[8];
+      float4* row = reinterpret_cast<float4*>(cta_o + g * D + lane * 8);
+      const float4 x0 = row[0], x1 = row[1];
+      x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+      x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+      fwht_row<8>(x, lane, 0.0625f);
+      row[0] = make_float4(x[0], x[1], x[2], x[3]);
+      row[1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+    __syncthreads();
+    if (a.n_splits > kMaxCluster) {   // the partial goes to the workspace; the combine follows
+      for (int e = threadIdx.x; e < nc * (D / 4); e += kThreads) {
+        const int g = e / (D / 4), d = (e - g * (D / 4)) * 4;
+        const size_t h = col_row(g);
+        *reinterpret_cast<float4*>(a.ws.part_o + (h * a.n_splits + split) * D + d) =
+            *reinterpret_cast<const float4*>(cta_o + g * D + d);
+        if (d == 0) a.ws.part_ml[h * a.n_splits + split] = make_float2(s_m[0][g], s_inv[g]);
+      }
+      return;
+    }
+  }
 
   // ---- up to 8 splits form one cluster: block `rank` combines dims
   // [rank*D/CS, (rank+1)*D/CS) over the cluster's splits, reading their partials
@@ -923,11 +1116,11 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   cluster.sync();   // no block leaves while others read its shared memory
 }
 
-template <int D, bool KI8, bool VI8, int NG, bool WIN>
+template <int D, bool KI8, bool VI8, int NG, bool WIN, bool VQ4>
 cudaError_t launch_typed(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                          int layer_page0, cudaStream_t stream) {
-  using LY = Layout<D, KI8, VI8>;
-  auto kern = decode_mma_kernel<D, KI8, VI8, NG, WIN>;
+  using LY = Layout<D, KI8, VI8, VQ4>;
+  auto kern = decode_mma_kernel<D, KI8, VI8, NG, WIN, VQ4>;
   static bool configured[64] = {};   // per device: the attribute belongs to the device's function
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -960,46 +1153,49 @@ cudaError_t launch_typed(const DecodeArgs& a, const CUtensorMap& tmk, const CUte
 }  // namespace
 
 bool decode_mma_supported(const PoolView& p, int G) {
-  return G <= 8 && p.ps == kPage && (p.D == 128 || p.D == 256) && p.gs >= 64 && p.gs % 64 == 0;
+  return G <= 8 && p.ps == kPage && (p.D == 128 || p.D == 256) && p.gs >= 64 && p.gs % 64 == 0 &&
+         (!p.v4 || p.D == 256);   // the 4-bit V store: head_dim 256 (one 128-byte box a row)
 }
 
-template <int D, bool KI8, bool VI8, bool WIN>
+template <int D, bool KI8, bool VI8, bool WIN, bool VQ4>
 cudaError_t launch_ng(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                       int layer_page0, cudaStream_t stream) {
   switch (a.pool.ng) {
-    case 1: return launch_typed<D, KI8, VI8, 1, WIN>(a, tmk, tmv, layer_page0, stream);
-    case 2: return launch_typed<D, KI8, VI8, 2, WIN>(a, tmk, tmv, layer_page0, stream);
+    case 1: return launch_typed<D, KI8, VI8, 1, WIN, VQ4>(a, tmk, tmv, layer_page0, stream);
+    case 2: return launch_typed<D, KI8, VI8, 2, WIN, VQ4>(a, tmk, tmv, layer_page0, stream);
     case 4:
       if constexpr (D == 256)
-        return launch_typed<D, KI8, VI8, 4, WIN>(a, tmk, tmv, layer_page0, stream);
+        return launch_typed<D, KI8, VI8, 4, WIN, VQ4>(a, tmk, tmv, layer_page0, stream);
       return cudaErrorNotSupported;
     default: return cudaErrorNotSupported;
   }
 }
 
-template <int D, bool KI8, bool VI8>
+template <int D, bool KI8, bool VI8, bool VQ4>
 cudaError_t launch_win(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                        int layer_page0, cudaStream_t stream) {
-  return a.q_len > 1 ? launch_ng<D, KI8, VI8, true>(a, tmk, tmv, layer_page0, stream)
-                     : launch_ng<D, KI8, VI8, false>(a, tmk, tmv, layer_page0, stream);
+  return a.q_len > 1 ? launch_ng<D, KI8, VI8, true, VQ4>(a, tmk, tmv, layer_page0, stream)
+                     : launch_ng<D, KI8, VI8, false, VQ4>(a, tmk, tmv, layer_page0, stream);
 }
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool k8, bool v8, const CUtensorMap& tmk,
                               const CUtensorMap& tmv, int layer_page0, cudaStream_t stream) {
   if (a.pool.D == 256) {
-    if (k8 && v8) return launch_win<256, true, true>(a, tmk, tmv, layer_page0, stream);
-    if (k8) return launch_win<256, true, false>(a, tmk, tmv, layer_page0, stream);
-    return launch_win<256, false, true>(a, tmk, tmv, layer_page0, stream);
+    if (a.pool.v4) return launch_win<256, true, false, true>(a, tmk, tmv, layer_page0, stream);
+    if (k8 && v8) return launch_win<256, true, true, false>(a, tmk, tmv, layer_page0, stream);
+    if (k8) return launch_win<256, true, false, false>(a, tmk, tmv, layer_page0, stream);
+    return launch_win<256, false, true, false>(a, tmk, tmv, layer_page0, stream);
   }
-  if (k8 && v8) return launch_win<128, true, true>(a, tmk, tmv, layer_page0, stream);
-  if (k8) return launch_win<128, true, false>(a, tmk, tmv, layer_page0, stream);
-  return launch_win<128, false, true>(a, tmk, tmv, layer_page0, stream);
+  if (a.pool.v4) return cudaErrorNotSupported;
+  if (k8 && v8) return launch_win<128, true, true, false>(a, tmk, tmv, layer_page0, stream);
+  if (k8) return launch_win<128, true, false, false>(a, tmk, tmv, layer_page0, stream);
+  return launch_win<128, false, true, false>(a, tmk, tmv, layer_page0, stream);
 }
 
-template <int D, bool KI8, bool VI8, int NG>
+template <int D, bool KI8, bool VI8, int NG, bool VQ4>
 int resident_typed() {
-  using LY = Layout<D, KI8, VI8>;
-  auto kern = decode_mma_kernel<D, KI8, VI8, NG, false>;
+  using LY = Layout<D, KI8, VI8, VQ4>;
+  auto kern = decode_mma_kernel<D, KI8, VI8, NG, false, VQ4>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM) !=
       cudaSuccess)
     return 0;
@@ -1012,19 +1208,20 @@ int resident_typed() {
   return per_sm * sms;
 }
 
-template <int D, bool KI8, bool VI8>
+template <int D, bool KI8, bool VI8, bool VQ4 = false>
 int resident_ng(int ng) {
-  if (ng == 1) return resident_typed<D, KI8, VI8, 1>();
-  if (ng == 2) return resident_typed<D, KI8, VI8, 2>();
+  if (ng == 1) return resident_typed<D, KI8, VI8, 1, VQ4>();
+  if (ng == 2) return resident_typed<D, KI8, VI8, 2, VQ4>();
   if constexpr (D == 256)
-    if (ng == 4) return resident_typed<D, KI8, VI8, 4>();
+    if (ng == 4) return resident_typed<D, KI8, VI8, 4, VQ4>();
   return 0;
 }
 
 // Blocks of the tensor-core kernel for this shape that the current device keeps
 // resident at once; 0 if unknown.
-int decode_mma_resident_blocks(int D, bool k8, bool v8, int ng) {
+int decode_mma_resident_blocks(int D, bool k8, bool v8, int ng, bool v4) {
   if (D == 256) {
+    if (v4) return resident_ng<256, true, false, true>(ng);
     if (k8 && v8) return resident_ng<256, true, true>(ng);
     if (k8) return resident_ng<256, true, false>(ng);
     return resident_ng<256, false, true>(ng);

@@ -60,17 +60,14 @@ __device__ __forceinline__ void load_row(const void* store, bool is_int8, const 
 template <int VPL>
 __device__ __forceinline__ void load_row_q4(const void* store, const uint16_t* scales, size_t row,
                                             int D, int lane, float (&x)[VPL]) {
-  const uint8_t* src = (const uint8_t*)store + row * (D / 2) + lane * (VPL / 2);
-  uint32_t w;
-  if constexpr (VPL == 8)
-    w = __ldg(reinterpret_cast<const uint32_t*>(src));
-  else if constexpr (VPL == 4)
-    w = __ldg(reinterpret_cast<const uint16_t*>(src));
-  else
-    w = __ldg(src);
+  const uint8_t* src = (const uint8_t*)store + row * (D / 2);
   const float d = h2f(__ldg(scales + row * (D / 32) + (lane * VPL) / 32));
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) x[i] = (float)((int)((w >> (4 * i)) & 15u) - 8) * d;
+  for (int p = 0; p < VPL / 2; ++p) {   // the lane's value pairs, one byte each
+    const uint32_t b = __ldg(src + q4_byte_of(lane * VPL + 2 * p, D));
+    x[2 * p] = (float)((int)(b & 15u) - 8) * d;
+    x[2 * p + 1] = (float)((int)(b >> 4) - 8) * d;
+  }
 }
 
 template <int D>

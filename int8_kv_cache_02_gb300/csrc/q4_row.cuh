@@ -49,6 +49,14 @@ __device__ __forceinline__ void fwht_row(float (&x)[VPL], int lane, float norm) 
   for (int i = 0; i < VPL; ++i) x[i] = __fmul_rn(x[i], norm);
 }
 
+// Byte of a packed 4-bit row of D values that holds value v (v even: low
+// nibble, v + 1: high nibble): the row is 8 chunks of D/16 bytes, byte
+// (D/16)*r + 2g + h holding values 32g + 4r + 2h and 32g + 4r + 2h + 1.
+__host__ __device__ __forceinline__ int q4_byte_of(int v, int D) {
+  const int g = v >> 5, w = v & 31;
+  return (D / 16) * (w >> 2) + 2 * g + ((w & 3) >> 1);
+}
+
 // Q4_0 codes (VPL nibbles packed two per byte, low nibble first) and the fp16
 // scale of the lane's block (every lane of the block gets it).
 template <int VPL>
@@ -98,13 +106,10 @@ __device__ __forceinline__ void quantize_row_q4(const uint16_t* src, uint8_t* ds
   fwht_row<VPL>(x, lane, norm);
   uint16_t scale;
   const uint32_t packed = q4_0_regs<VPL>(x, lane, scale);
-  uint8_t* d = dst_codes + lane * (VPL / 2);
-  if constexpr (VPL == 8)
-    *reinterpret_cast<uint32_t*>(d) = packed;
-  else if constexpr (VPL == 4)
-    *reinterpret_cast<uint16_t*>(d) = (uint16_t)packed;
-  else
-    *d = (uint8_t)packed;
+  constexpr int D = 32 * VPL;
+#pragma unroll
+  for (int p = 0; p < VPL / 2; ++p)   // the lane's value pairs, each one byte of the row
+    dst_codes[q4_byte_of(lane * VPL + 2 * p, D)] = (uint8_t)(packed >> (8 * p));
   if (lane % (32 / VPL) == 0) dst_scales[lane * VPL / 32] = scale;
 }
 

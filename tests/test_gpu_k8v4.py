@@ -59,8 +59,9 @@ def test_append_is_bit_exact(D, gs):
     assert binding.kv_pool_read_device_error(dev) == 0
 
 
-def _decode(dev, q, lens, pt, n_splits, window=0):
+def _decode(dev, q, lens, pt, n_splits, window=0, kind=0):
     from int8_kv_cache_02_gb300 import binding
+    dev.set_decode_kernel(kind)
     B, H, D = q.shape
     out = torch.full((B, H, D), float("nan"), dtype=torch.float32, device="cuda")
     binding.attn_decode_int8(dev, 0, q.cuda(), torch.tensor(lens, dtype=torch.int32, device="cuda"),
@@ -80,11 +81,14 @@ def test_decode_matches_oracle(D, gs, H, Hkv, n_splits):
     dev, orc = gu.make_pools(1, Hkv, D, gs, 64, n_pages, K8V4)
     for b in range(len(lens)):
         gu.fill_sequence(dev, orc, 0, ks[b], vs[b], pt[b])
+    # head_dim 256: the tensor-core kernel (AUTO) and the CUDA-core one; 128: CUDA cores
+    kinds = [binding.DECODE_AUTO, binding.DECODE_SIMT] if D == 256 else [binding.DECODE_AUTO]
     for window in (0, 200):
-        got = _decode(dev, q, lens, pt, n_splits, window)
         ref = np.stack([oatt.decode(q[b].numpy(), *orc.gather(0, pt[b].numpy(), L), L, window=window)
                         for b, L in enumerate(lens)])
-        gu.assert_attention_close(got, ref, f"k8v4 D{D} H{H} ns{n_splits} w{window}")
+        for kind in kinds:
+            got = _decode(dev, q, lens, pt, n_splits, window, kind)
+            gu.assert_attention_close(got, ref, f"k8v4 D{D} H{H} ns{n_splits} w{window} kind{kind}")
     assert binding.kv_pool_read_device_error(dev) == 0
 
 
@@ -131,11 +135,15 @@ def test_fused_step_and_image_round_trip():
     gu.regions_equal(c_dev, c_orc)
 
 
-def test_k8v4_pools_refuse_the_tensor_core_paths():
+def test_k8v4_kernel_choice_and_refusals():
+    """head_dim 256 decodes on the tensor-core kernel (one 128-byte box of codes a
+    row); head_dim 128 only on the CUDA cores; the prefill chunk refuses k8v4."""
     from int8_kv_cache_02_gb300 import binding
-    dev, _ = gu.make_pools(1, 2, 256, 64, 64, 4, K8V4)
+    small, _ = gu.make_pools(1, 2, 128, 64, 64, 4, K8V4)
     with pytest.raises(binding.Int8KVError):
-        dev.set_decode_kernel(binding.DECODE_WARP_MMA)
+        small.set_decode_kernel(binding.DECODE_WARP_MMA)
+    dev, _ = gu.make_pools(1, 2, 256, 64, 64, 4, K8V4)
+    dev.set_decode_kernel(binding.DECODE_WARP_MMA)
     q = torch.zeros((8, 16, 256), dtype=torch.float16, device="cuda")
     out = torch.zeros((8, 16, 256), dtype=torch.float32, device="cuda")
     with pytest.raises(binding.Int8KVError) as e:
@@ -162,3 +170,32 @@ def test_grouped8k_workload_k8v4():
     got = _decode(dev, w["q"], [L], pt, ns)
     ref = oatt.decode(w["q"][0].numpy(), *orc.gather(0, pt[0].numpy(), L), L)
     gu.assert_attention_close(got[0], ref, "k8v4 8K")
+
+
+@pytest.mark.parametrize("q_len,n_splits", [(3, 1), (2, 5), (4, 12)])
+def test_query_windows_k8v4(q_len, n_splits):
+    """Query windows over a k8v4 pool (tensor-core kernel): query i of a window at
+    position L - q_len + i sees keys 0 .. L - q_len + i."""
+    from int8_kv_cache_02_gb300 import binding
+    lens = [700, 90]
+    B, H = 2, 16
+    g = torch.Generator().manual_seed(70 + q_len)
+    qw = inputs.normal_f16((B, q_len, H, 256), g)
+    _, ks, vs = inputs.random_case(71 + q_len, B, H, 2, 256, lens, outliers=True)
+    pt, n_pages = inputs.page_table(lens, 64, seed=9)
+    dev, orc = gu.make_pools(1, 2, 256, 64, 64, n_pages, K8V4)
+    for b in range(B):
+        gu.fill_sequence(dev, orc, 0, ks[b], vs[b], pt[b])
+    out = torch.full((B, q_len, H, 256), float("nan"), dtype=torch.float32, device="cuda")
+    binding.attn_decode_multi_int8(dev, 0, qw.cuda(), torch.tensor(lens, dtype=torch.int32,
+                                                                     device="cuda"),
+                                   pt.cuda(), out, dev.decode_workspace(B * q_len, H, n_splits),
+                                   n_splits=n_splits)
+    torch.cuda.synchronize()
+    ref = np.zeros((B, q_len, H, 256))
+    for b, L in enumerate(lens):
+        kh, vh = orc.gather(0, pt[b].numpy(), L)
+        for i in range(q_len):
+            ref[b, i] = oatt.decode(qw[b, i].numpy(), kh, vh, L - q_len + i + 1)
+    gu.assert_attention_close(out.cpu().numpy(), ref, f"k8v4 window {q_len}")
+    assert binding.kv_pool_read_device_error(dev) == 0
