@@ -17,7 +17,7 @@ Image layout (little-endian; every section starts on a 16-byte boundary):
   header, 48 bytes:
      0  4 bytes  magic b"I8KV"
      4  u32      format version, 3
-     8  u32      store variant (0 k8v8, 1 k8v16, 2 k16v8, 3 k8v4)
+     8  u32      store variant (0 k8v8, 1 k8v16, 2 k16v8, 3 k8v4, 4 q4_0)
     12  u32      n_layers
     16  u32      n_kv_heads
     20  u32      head_dim
@@ -28,7 +28,7 @@ Image layout (little-endian; every section starts on a 16-byte boundary):
   lengths: int32 [n_seqs], padded with zeros to a multiple of 16 bytes
   payload: for each sequence b, for each layer l, four sections (the scales
   sections only for a quantized store), each padded with zeros to 16 bytes:
-     K store   [L_b][n_kv_heads][head_dim]  int8 codes or fp16 values
+     K store   [L_b][n_kv_heads][head_dim]  int8 codes or fp16 values  (q4_0: as V of k8v4)
      V store   [L_b][n_kv_heads][head_dim]  (k8v4: [head_dim / 2] bytes of 4-bit codes)
      K scales  [L_b][n_kv_heads][head_dim / group_size] fp16
      V scales  [L_b][n_kv_heads][head_dim / group_size] fp16  (k8v4: [head_dim / 32])

@@ -23,14 +23,19 @@ import numpy as np
 
 from . import q4, quant
 
-K8V8, K8V16, K16V8, K8V4 = 0, 1, 2, 3
-VARIANT_NAMES = {K8V8: "k8v8", K8V16: "k8v16", K16V8: "k16v8", K8V4: "k8v4"}
+K8V8, K8V16, K16V8, K8V4, Q4_0 = 0, 1, 2, 3, 4
+VARIANT_NAMES = {K8V8: "k8v8", K8V16: "k8v16", K16V8: "k16v8", K8V4: "k8v4", Q4_0: "q4_0"}
 
 
 def store_is_int8(variant: int):
-    """(K is int8, V is int8) for a store variant (k8v4: K int8, V 4-bit)."""
+    """(K is int8, V is int8) for a store variant (k8v4: K int8, V 4-bit; q4_0: both 4-bit)."""
     return {K8V8: (True, True), K8V16: (True, False), K16V8: (False, True),
-            K8V4: (True, False)}[variant]
+            K8V4: (True, False), Q4_0: (False, False)}[variant]
+
+
+def store_is_q4(variant: int):
+    """(K is 4-bit, V is 4-bit) for a store variant."""
+    return {K8V4: (False, True), Q4_0: (True, True)}.get(variant, (False, False))
 
 
 def bytes_per_cell(n_kv_heads: int, head_dim: int, gs: int, int8: bool) -> int:
@@ -51,7 +56,10 @@ class Pool:
     k8v4 (Strata pull request #2698, "Not in this PR": the 4-bit store with the
     FWHT-256 rotation, see oracle/q4.py): V rows are rotated, then Q4_0; the V
     store is uint8 [..., head_dim / 2] (two codes per byte) and the V scales
-    fp16 [..., head_dim / 32]."""
+    fp16 [..., head_dim / 32].  q4_0 (the same page's --kv q4_0): K and V both.
+    gather returns rows rotated back in fp64, so attention over them is
+    attention with the rotated queries over the rotated keys (the rotation is
+    orthonormal)."""
 
     def __init__(self, n_layers, n_kv_heads, head_dim, gs, page_size, n_pages, variant):
         assert head_dim % gs == 0
@@ -59,15 +67,19 @@ class Pool:
         self.gs, self.ng = gs, head_dim // gs
         self.page_size, self.n_pages, self.variant = page_size, n_pages, variant
         self.k_int8, self.v_int8 = store_is_int8(variant)
-        self.v_q4 = variant == K8V4
+        self.k_q4, self.v_q4 = store_is_q4(variant)
         body = (n_layers, n_pages, n_kv_heads, page_size, head_dim)
         sc = (n_layers, n_pages, n_kv_heads, page_size, self.ng)
         self.k_store = np.zeros(body, np.int8 if self.k_int8 else np.float16)
         self.v_store = np.zeros(body, np.int8 if self.v_int8 else np.float16)
         self.k_scales = np.zeros(sc, np.float16) if self.k_int8 else None
         self.v_scales = np.zeros(sc, np.float16) if self.v_int8 else None
-        if self.v_q4:
+        if self.k_q4 or self.v_q4:
             assert head_dim % q4.BLOCK == 0 and head_dim & (head_dim - 1) == 0
+        if self.k_q4:
+            self.k_store = np.zeros(body[:-1] + (head_dim // 2,), np.uint8)
+            self.k_scales = np.zeros(body[:-1] + (head_dim // q4.BLOCK,), np.float16)
+        if self.v_q4:
             self.v_store = np.zeros(body[:-1] + (head_dim // 2,), np.uint8)
             self.v_scales = np.zeros(body[:-1] + (head_dim // q4.BLOCK,), np.float16)
 
@@ -87,7 +99,7 @@ class Pool:
             for i in range(n_new):
                 page, slot = self._slot(page_table[b], int(seq_pos[b]) + i)
                 for new, store, scales, is8, is4 in (
-                    (k_new, self.k_store, self.k_scales, self.k_int8, False),
+                    (k_new, self.k_store, self.k_scales, self.k_int8, self.k_q4),
                     (v_new, self.v_store, self.v_scales, self.v_int8, self.v_q4),
                 ):
                     x = new[b, i]                              # [n_kv_heads][head_dim]
@@ -115,7 +127,7 @@ class Pool:
         pages = np.asarray(page_table_row)[pos // self.page_size]
         slots = pos % self.page_size
         for x, store, scales, is8, is4 in (
-            (k_seq, self.k_store, self.k_scales, self.k_int8, False),
+            (k_seq, self.k_store, self.k_scales, self.k_int8, self.k_q4),
             (v_seq, self.v_store, self.v_scales, self.v_int8, self.v_q4),
         ):
             if is4:
@@ -140,7 +152,7 @@ class Pool:
         slots = pos % self.page_size
         out = []
         for store, scales, is8, is4 in (
-            (self.k_store, self.k_scales, self.k_int8, False),
+            (self.k_store, self.k_scales, self.k_int8, self.k_q4),
             (self.v_store, self.v_scales, self.v_int8, self.v_q4),
         ):
             rows = store[layer, pages, :, slots, :]             # [L][Hkv][D]

@@ -148,3 +148,22 @@ def test_k8v4_pool_context_one_and_identical_keys():
     # thread-chunk layout: chunk r of a row holds values 32g + 4r .. 32g + 4r + 3 of every block
     codes = q4.unpack(P.v_store[0, 0, 0, :1])[0]
     assert codes.shape == (256,)
+
+
+def test_q4_0_pool_closed_forms_and_rotation_invariance():
+    """q4_0: K and V both rotated and 4-bit.  Context 1 returns the stored V row;
+    the scores equal those of the rotated query against the rotated, dequantized
+    keys (what a kernel computes), because the rotation is orthonormal."""
+    rng = np.random.default_rng(12)
+    P = opool.Pool(1, 2, 128, 128, 16, 3, opool.Q4_0)
+    assert P.k_store.dtype == np.uint8 and P.k_store.shape[-1] == 64 and P.k_scales.shape[-1] == 4
+    k = rng.standard_normal((30, 2, 128)).astype(np.float16)
+    v = rng.standard_normal((30, 2, 128)).astype(np.float16)
+    P.append_contiguous(0, k, v, 0, np.arange(2))
+    kh, vh = P.gather(0, np.arange(2), 30)
+    q = rng.standard_normal((4, 128)).astype(np.float16)
+    assert np.allclose(oatt.decode(q, kh, vh, 1), np.repeat(vh[0], 2, axis=0), atol=1e-12)
+    rows = P.k_store[0, 0, 0, :16]                   # kv head 0, positions 0..15
+    k_rot = q4.q4_0_dequantize(q4.unpack(rows), P.k_scales[0, 0, 0, :16])
+    q_rot = q4.hadamard_fp64(q[0].astype(np.float64))
+    assert np.allclose(k_rot @ q_rot, kh[:16, 0] @ q[0].astype(np.float64), atol=1e-9)
