@@ -49,16 +49,19 @@ B, H, HKV, D, GS, PS, CTX = 1, 16, 2, 256, 64, 64, 8192
 
 
 def step_bytes(ctx=CTX, hkv=HKV, h=H, d=D, gs=GS, k_int8=True, v_int8=True, append=True,
-               v_q4=False):
+               v_q4=False, k_q4=False):
     """Algorithmic bytes of one step: int8 KV + scales (fp16 for an fp16 store;
-    4-bit codes + one fp16 scale per 32 values for the k8v4 V store) read once,
+    4-bit codes + one fp16 scale per 32 values for a 4-bit store) read once,
     q (fp16) read, O (fp32) written, and the appended token (fp16 in, codes +
     scales out)."""
     per_pos = 0
-    for is8 in (k_int8, v_int8):
-        per_pos += hkv * d + hkv * (d // gs) * 2 if is8 else hkv * d * 2
-    if v_q4:
-        per_pos += hkv * d // 2 + hkv * (d // 32) * 2 - hkv * d * 2   # instead of fp16 V
+    for is8, is4 in ((k_int8, k_q4), (v_int8, v_q4)):
+        if is4:
+            per_pos += hkv * d // 2 + hkv * (d // 32) * 2
+        elif is8:
+            per_pos += hkv * d + hkv * (d // gs) * 2
+        else:
+            per_pos += hkv * d * 2
     n = ctx * per_pos + h * d * 2 + h * d * 4
     if append:
         n += 2 * hkv * d * 2 + per_pos
@@ -749,6 +752,19 @@ def run_extra(args):
         us = time_graph(g) / n * 1e3
         out[name] = dict(rate(per, us, f"{copies} rotating pool copies"), n_splits=st.n_splits,
                          kernel="decode_mma_kernel (4-bit V) + decode_combine_kernel")
+        del st, g
+        torch.cuda.empty_cache()
+    # q4_0 (K and V rotated + Q4_0; CUDA-core decode kernel) at 8K and 128K
+    for name, wf, ctx in (("grouped8k_q4_0", inputs.grouped8k, CTX),
+                          ("long128k_q4_0", inputs.long128k, 131072)):
+        per = decode_bytes(ctx=ctx, k_int8=False, v_int8=False, k_q4=True, v_q4=True)
+        copies = max(2, math.ceil(2 * l2_bytes() / per) + 1)
+        st = DecodeState(wf(), ctx, binding.Q4_0, copies, append_token=False)
+        n = 20
+        g = st.graph(n, append=False)
+        us = time_graph(g) / n * 1e3
+        out[name] = dict(rate(per, us, f"{copies} rotating pool copies"), n_splits=st.n_splits,
+                         kernel="decode_simt_kernel (4-bit K and V) + decode_combine_kernel")
         del st, g
         torch.cuda.empty_cache()
     if not getattr(args, "no_batched", False):

@@ -42,6 +42,13 @@
  *                  its high nibble (r = 0..7, h = 0..1, g the 32-value block);
  *                  value (code - 8) * d.  Decode rotates its output back.  No
  *                  prefill chunk.
+ *     INT8KV_Q4_0  K and V both as V of INT8KV_K8V4 (Strata #2698 "Not in this
+ *                  PR": --kv q4_0): the rows of K are rotated before they are
+ *                  stored, decode rotates each query the same way (scores are
+ *                  unchanged, the transform being orthonormal) and the output
+ *                  back.  Decode on the CUDA-core kernel only, one query per
+ *                  sequence (no query windows, no prefill chunk); group_size
+ *                  is validated but no store uses it.
  *
  * Pool layout in device memory (caller-allocated; the library never
  * allocates device memory):
@@ -105,7 +112,8 @@ typedef enum {
   INT8KV_K8V8 = 0,
   INT8KV_K8V16 = 1,
   INT8KV_K16V8 = 2,
-  INT8KV_K8V4 = 3
+  INT8KV_K8V4 = 3,
+  INT8KV_Q4_0 = 4
 } int8kv_variant;
 
 /* Regions of a pool, for int8kv_pool_region_bytes. */
@@ -188,8 +196,8 @@ int kv_pool_set_decode_kernel(int8kv_pool* pool, int kind);
  * split) blocks run in waves of as many blocks as the pool's decode kernel
  * keeps resident on the pool's device (queried once per pool and kernel); the
  * count with the shortest chain of waves x (pages per block + 1), plus 2 when
- * the splits need combining, is returned: at least 1, at most the pages of
- * max_ctx and 256.
+ * the splits need combining, is returned (the smallest on a tie): at least 1,
+ * at most the pages of max_ctx and 256.
  * Returns >= 1, or a negative status (NULL_PTR, INVALID_ARG). */
 int attn_decode_n_splits(const int8kv_pool* pool, int batch, int max_ctx);
 

@@ -17,8 +17,8 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libint8kv.so")
 
-K8V8, K8V16, K16V8, K8V4 = 0, 1, 2, 3
-VARIANTS = {"k8v8": K8V8, "k8v16": K8V16, "k16v8": K16V8, "k8v4": K8V4}
+K8V8, K8V16, K16V8, K8V4, Q4_0 = 0, 1, 2, 3, 4
+VARIANTS = {"k8v8": K8V8, "k8v16": K8V16, "k16v8": K16V8, "k8v4": K8V4, "q4_0": Q4_0}
 REGION_K_STORE, REGION_V_STORE, REGION_K_SCALES, REGION_V_SCALES = 0, 1, 2, 3
 DEVERR_PAGE_ID, DEVERR_LENGTH, DEVERR_TIMEOUT = 1, 2, 4
 ERR_FORMAT = -9
@@ -330,12 +330,17 @@ class KVPool:
         sshape = (n_layers, n_pages, n_kv_heads, page_size, ng)
         k8 = variant in (K8V8, K8V16, K8V4)
         v8 = variant in (K8V8, K16V8)
-        v4 = variant == K8V4
+        k4 = variant == Q4_0
+        v4 = variant in (K8V4, Q4_0)
         self.k_store = torch.zeros(shape, dtype=torch.int8 if k8 else torch.float16, device=dev)
         self.v_store = torch.zeros(shape, dtype=torch.int8 if v8 else torch.float16, device=dev)
         self.k_scales = torch.zeros(sshape, dtype=torch.float16, device=dev) if k8 else None
         self.v_scales = torch.zeros(sshape, dtype=torch.float16, device=dev) if v8 else None
-        if v4:   # 4-bit V: two codes per byte, one fp16 scale per 32 values
+        if k4:   # 4-bit stores: two codes per byte, one fp16 scale per 32 values
+            self.k_store = torch.zeros(shape[:-1] + (head_dim // 2,), dtype=torch.uint8, device=dev)
+            self.k_scales = torch.zeros(shape[:-1] + (head_dim // 32,), dtype=torch.float16,
+                                        device=dev)
+        if v4:
             self.v_store = torch.zeros(shape[:-1] + (head_dim // 2,), dtype=torch.uint8, device=dev)
             self.v_scales = torch.zeros(shape[:-1] + (head_dim // 32,), dtype=torch.float16,
                                         device=dev)

@@ -30,21 +30,22 @@ bool valid_group(int d, int gs) {
   return gs >= d / 32;
 }
 
-// Stores of a variant: K int8, V int8, V 4-bit (k8v4); the rest are fp16.
-bool variant_stores(int variant, bool* k8, bool* v8, bool* v4) {
-  *v4 = false;
+// Stores of a variant: K int8, V int8, K 4-bit, V 4-bit; the rest are fp16.
+bool variant_stores(int variant, bool* k8, bool* v8, bool* k4, bool* v4) {
+  *k4 = *v4 = false;
   switch (variant) {
     case INT8KV_K8V8: *k8 = true; *v8 = true; return true;
     case INT8KV_K8V16: *k8 = true; *v8 = false; return true;
     case INT8KV_K16V8: *k8 = false; *v8 = true; return true;
     case INT8KV_K8V4: *k8 = true; *v8 = false; *v4 = true; return true;
+    case INT8KV_Q4_0: *k8 = false; *v8 = false; *k4 = true; *v4 = true; return true;
     default: return false;
   }
 }
 
 bool variant_int8(int variant, bool* k8, bool* v8) {
-  bool v4;
-  return variant_stores(variant, k8, v8, &v4);
+  bool k4, v4;
+  return variant_stores(variant, k8, v8, &k4, &v4);
 }
 
 int shape_status(int n_layers, int n_kv_heads, int head_dim, int group_size, int page_size,
@@ -197,15 +198,19 @@ int int8kv_pool_region_bytes(int n_layers, int n_kv_heads, int head_dim, int gro
   const int st = shape_status(n_layers, n_kv_heads, head_dim, group_size, page_size, n_pages,
                               variant);
   if (st != INT8KV_OK) return st;
-  bool k8, v8, v4;
-  variant_stores(variant, &k8, &v8, &v4);
+  bool k8, v8, k4, v4;
+  variant_stores(variant, &k8, &v8, &k4, &v4);
   const size_t rows = (size_t)n_layers * n_pages * n_kv_heads * page_size;
   switch (region) {
-    case INT8KV_REGION_K_STORE: *out_bytes = rows * head_dim * (k8 ? 1 : 2); break;
+    case INT8KV_REGION_K_STORE:
+      *out_bytes = k4 ? rows * head_dim / 2 : rows * head_dim * (k8 ? 1 : 2);
+      break;
     case INT8KV_REGION_V_STORE:
       *out_bytes = v4 ? rows * head_dim / 2 : rows * head_dim * (v8 ? 1 : 2);
       break;
-    case INT8KV_REGION_K_SCALES: *out_bytes = k8 ? rows * (head_dim / group_size) * 2 : 0; break;
+    case INT8KV_REGION_K_SCALES:
+      *out_bytes = k4 ? rows * (head_dim / 32) * 2 : (k8 ? rows * (head_dim / group_size) * 2 : 0);
+      break;
     case INT8KV_REGION_V_SCALES:
       *out_bytes = v4 ? rows * (head_dim / 32) * 2 : (v8 ? rows * (head_dim / group_size) * 2 : 0);
       break;
@@ -222,11 +227,11 @@ int kv_pool_create(int8kv_pool** out, int n_layers, int n_kv_heads, int head_dim
   const int st = shape_status(n_layers, n_kv_heads, head_dim, group_size, page_size, n_pages,
                               variant);
   if (st != INT8KV_OK) return st;
-  bool k8, v8, v4;
-  variant_stores(variant, &k8, &v8, &v4);
+  bool k8, v8, k4, v4;
+  variant_stores(variant, &k8, &v8, &k4, &v4);
   if (!k_store || !v_store) return INT8KV_ERR_NULL_PTR;
-  if ((k8 && !k_scales) || ((v8 || v4) && !v_scales)) return INT8KV_ERR_NULL_PTR;
-  if ((!k8 && k_scales) || (!v8 && !v4 && v_scales)) return INT8KV_ERR_INVALID_ARG;
+  if (((k8 || k4) && !k_scales) || ((v8 || v4) && !v_scales)) return INT8KV_ERR_NULL_PTR;
+  if ((!k8 && !k4 && k_scales) || (!v8 && !v4 && v_scales)) return INT8KV_ERR_INVALID_ARG;
   if (!aligned16(k_store) || !aligned16(v_store) || !aligned16(k_scales) ||
       !aligned16(v_scales))
     return INT8KV_ERR_ALIGNMENT;
@@ -247,6 +252,7 @@ int kv_pool_create(int8kv_pool** out, int n_layers, int n_kv_heads, int head_dim
   p->variant = variant;
   p->k_int8 = k8;
   p->v_int8 = v8;
+  p->k_q4 = k4;
   p->v_q4 = v4;
   p->k_store = k_store;
   p->v_store = v_store;
@@ -260,8 +266,10 @@ int kv_pool_create(int8kv_pool** out, int n_layers, int n_kv_heads, int head_dim
   for (int k = 0; k < 4; ++k) p->resident[k] = 0;
   p->expire_polls = 0;
   // TMA descriptors for the tensor-core kernels; the 4-bit V store is mapped as
-  // rows of head_dim / 2 bytes (head_dim 256 only: one 128-byte box a row)
-  if (page_size == 64 && (head_dim == 128 || head_dim == 256) && (!v4 || head_dim == 256)) {
+  // rows of head_dim / 2 bytes (head_dim 256 only: one 128-byte box a row).  A
+  // 4-bit K store is decoded on the CUDA cores only.
+  if (page_size == 64 && (head_dim == 128 || head_dim == 256) && (!v4 || head_dim == 256) &&
+      !k4) {
     const size_t rows = (size_t)n_layers * n_pages * n_kv_heads * page_size;
     if (rows >= (1ull << 31) || !make_store_map(&p->tmap_k, k_store, k8, head_dim, rows) ||
         !make_store_map(&p->tmap_v, v_store, v8 || v4, v4 ? head_dim / 2 : head_dim, rows)) {

@@ -1154,7 +1154,8 @@ cudaError_t launch_typed(const DecodeArgs& a, const CUtensorMap& tmk, const CUte
 
 bool decode_mma_supported(const PoolView& p, int G) {
   return G <= 8 && p.ps == kPage && (p.D == 128 || p.D == 256) && p.gs >= 64 && p.gs % 64 == 0 &&
-         (!p.v4 || p.D == 256);   // the 4-bit V store: head_dim 256 (one 128-byte box a row)
+         (!p.v4 || p.D == 256) &&   // the 4-bit V store: head_dim 256 (one 128-byte box a row)
+         !p.k4;                     // a 4-bit K store: the CUDA-core kernel
 }
 
 template <int D, bool KI8, bool VI8, bool WIN, bool VQ4>

@@ -16,7 +16,11 @@
 //
 // This kernel is the general path (any G <= 8, head_dim 64/128/256, every
 // store variant); the tensor-core kernel in decode_mma.cu serves the shapes it
-// is specialised for.
+// is specialised for.  The 4-bit stores (Strata pull request #2698, "Not in
+// this PR": k8v4 and --kv q4_0 with the Hadamard rotation) hold rotated rows:
+// with a rotated K store each query is rotated by the same normalised FWHT
+// before its scores (q.k = Hq.Hk, H orthonormal); with a rotated V store the
+// merged output rows are rotated back.
 
 #include <cmath>
 
@@ -55,8 +59,8 @@ __device__ __forceinline__ void load_row(const void* store, bool is_int8, const 
   }
 }
 
-// A row of the 4-bit store (k8v4): the lane's VPL values (code - 8) * d, in the
-// rotated basis, its block's fp16 scale d.
+// A row of a 4-bit store: the lane's VPL values (code - 8) * d, in the rotated
+// basis, d its block's fp16 scale.
 template <int VPL>
 __device__ __forceinline__ void load_row_q4(const void* store, const uint16_t* scales, size_t row,
                                             int D, int lane, float (&x)[VPL]) {
@@ -81,7 +85,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeArgs a, 
 
   __shared__ float s_m[kWarps][8], s_l[kWarps][8];
   __shared__ float s_o[kWarps][8][D];
-  __shared__ float s_r[8][D], s_M[8], s_L[8];   // k8v4: merged rows before the rotation back
+  __shared__ float s_r[8][D], s_M[8], s_L[8];   // 4-bit V: merged rows before the rotation back
 
   float qr[8][VPL];
 #pragma unroll
@@ -89,6 +93,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeArgs a, 
 #pragma unroll
     for (int i = 0; i < VPL; ++i)
       qr[g][i] = g < G ? h2f(__ldg(a.q + ((size_t)b * a.H + kvh * G + g) * D + lane * VPL + i)) : 0.f;
+  if (p.k4) {   // rotated keys: rotate the queries the same way
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      if (g < G) fwht_row<VPL>(qr[g], lane, fwht_norm);
+  }
 
   const int L = clamp_length(__ldg(a.seq_lens + b), a.max_pages, p);
   const int lo = a.window > 0 ? max(0, L - a.window) : 0;
@@ -110,7 +119,10 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeArgs a, 
     if (pg < 0) continue;
     const size_t row = row_index(p, pg, kvh, j % p.ps);
     float kf[VPL], vf[VPL];
-    load_row<VPL>(p.k, k_int8, p.ks, row, D, p.ng, p.gs, lane, kf);
+    if (p.k4)
+      load_row_q4<VPL>(p.k, p.ks, row, D, lane, kf);
+    else
+      load_row<VPL>(p.k, k_int8, p.ks, row, D, p.ng, p.gs, lane, kf);
     if (p.v4)
       load_row_q4<VPL>(p.v, p.vs, row, D, lane, vf);
     else
@@ -178,7 +190,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeArgs a, 
     }
   }
   if (!p.v4) return;
-  // k8v4: rotate each merged row back (the FWHT is its own inverse; the combine
+  // 4-bit V: rotate each merged row back (the FWHT is its own inverse; the combine
   // of the splits is linear in their rows, so each split's row is rotated here)
   __syncthreads();
   for (int g = warp; g < G; g += kWarps) {
@@ -205,7 +217,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeArgs a, 
 cudaError_t launch_decode_simt(const DecodeArgs& a, bool k_int8, bool v_int8,
                                cudaStream_t stream) {
   const dim3 grid(a.n_splits, a.pool.Hkv, a.B);
-  const float norm = (float)(1.0 / std::sqrt((double)a.pool.D));   // FWHT scaling (k8v4)
+  const float norm = (float)(1.0 / std::sqrt((double)a.pool.D));   // FWHT scaling (4-bit stores)
   switch (a.pool.D) {
     case 64:
       decode_simt_kernel<64><<<grid, kWarps * 32, 0, stream>>>(a, k_int8, v_int8, norm);

@@ -13,7 +13,7 @@
 struct int8kv_pool {
   int n_layers, n_kv_heads, head_dim, group_size, n_groups, page_size, n_pages, variant;
   bool k_int8, v_int8;
-  bool v_q4;         // k8v4: V rotated (FWHT) and stored as Q4_0 (4-bit codes, fp16 per 32)
+  bool k_q4, v_q4;   // K / V rotated (FWHT) and stored as Q4_0 (4-bit codes, fp16 per 32)
   void* k_store;
   void* v_store;
   uint16_t* k_scales;
@@ -39,19 +39,22 @@ struct PoolView {
   const uint16_t* vs;       // V scales of the layer, or null
   int32_t* err;             // device error word, or null
   int n_pages, Hkv, D, gs, ng, ps;
-  bool v4;                  // V store: Q4_0 codes [..][D/2] bytes, scales [..][D/32] (vs)
+  bool k4;                  // K store: Q4_0 codes [..][D/2] bytes, scales [..][D/32] (ks)
+  bool v4;                  // V store: the same (vs)
 };
 
 inline PoolView layer_view(const int8kv_pool* p, int layer) {
   PoolView v;
   const size_t rows = (size_t)p->n_pages * p->n_kv_heads * p->page_size;
   const size_t kb = p->k_int8 ? 1 : 2, vb = p->v_int8 ? 1 : 2;
-  // bytes of one V row and fp16 scales of one V row
+  // bytes of one row and fp16 scales of one row, per store
+  const size_t krow = p->k_q4 ? p->head_dim / 2 : p->head_dim * kb;
+  const size_t ksrow = p->k_q4 ? p->head_dim / 32 : p->n_groups;
   const size_t vrow = p->v_q4 ? p->head_dim / 2 : p->head_dim * vb;
   const size_t vsrow = p->v_q4 ? p->head_dim / 32 : p->n_groups;
-  v.k = (const char*)p->k_store + (size_t)layer * rows * p->head_dim * kb;
+  v.k = (const char*)p->k_store + (size_t)layer * rows * krow;
   v.v = (const char*)p->v_store + (size_t)layer * rows * vrow;
-  v.ks = p->k_scales ? p->k_scales + (size_t)layer * rows * p->n_groups : nullptr;
+  v.ks = p->k_scales ? p->k_scales + (size_t)layer * rows * ksrow : nullptr;
   v.vs = p->v_scales ? p->v_scales + (size_t)layer * rows * vsrow : nullptr;
   v.err = p->dev_error;
   v.n_pages = p->n_pages;
@@ -60,6 +63,7 @@ inline PoolView layer_view(const int8kv_pool* p, int layer) {
   v.gs = p->group_size;
   v.ng = p->n_groups;
   v.ps = p->page_size;
+  v.k4 = p->k_q4;
   v.v4 = p->v_q4;
   return v;
 }

@@ -44,20 +44,20 @@ __host__ __device__ inline size_t pad16(size_t n) { return (n + 15) / 16 * 16; }
 
 struct ImageShape {
   int n_layers, Hkv, D, ng;
-  bool k8, v8, v4;
+  bool k8, v8, k4, v4;
 };
 
 ImageShape shape_of(const int8kv_pool* p) {
   return ImageShape{p->n_layers, p->n_kv_heads, p->head_dim, p->n_groups,
-                    p->k_int8, p->v_int8, p->v_q4};
+                    p->k_int8, p->v_int8, p->k_q4, p->v_q4};
 }
 
 // Bytes of one row (position, kv head) of each region: K store, V store, K
 // scales, V scales (0: no such region).
 __host__ __device__ inline void row_bytes_of(const ImageShape& s, long long (&r)[4]) {
-  r[0] = (long long)s.D * (s.k8 ? 1 : 2);
+  r[0] = s.k4 ? s.D / 2 : (long long)s.D * (s.k8 ? 1 : 2);
   r[1] = s.v4 ? s.D / 2 : (long long)s.D * (s.v8 ? 1 : 2);
-  r[2] = s.k8 ? s.ng * 2 : 0;
+  r[2] = s.k4 ? (s.D / 32) * 2 : (s.k8 ? s.ng * 2 : 0);
   r[3] = s.v4 ? (s.D / 32) * 2 : (s.v8 ? s.ng * 2 : 0);
 }
 

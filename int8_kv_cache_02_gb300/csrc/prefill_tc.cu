@@ -592,7 +592,7 @@ static cudaError_t launch_prefill_tc(const int8kv_pool* pool, int layer, const P
 }
 
 bool prefill_supported(const int8kv_pool* pool, int G) {
-  return pool->has_tmaps && !pool->v_q4 && pool->page_size == kPage && pool->group_size >= 64 &&
+  return pool->has_tmaps && !pool->v_q4 && !pool->k_q4 && pool->page_size == kPage && pool->group_size >= 64 &&
          (pool->head_dim == 128 || pool->head_dim == 256) && (G == 1 || G == 2 || G == 4 || G == 8);
 }
 

@@ -49,12 +49,15 @@ __global__ void __launch_bounds__(256) quant_append_kernel(
   const size_t dst_row = row_index(p, page, kvh, pos % p.ps);
   const size_t src_off = (size_t)row * p.D;
   const int lpg = p.gs / VPL;  // lanes per scale group
-  if (k_int8)
+  if (p.k4)   // q4_0: K rotated, then Q4_0
+    quantize_row_q4<VPL>(k_new + src_off, (uint8_t*)p.k + dst_row * (p.D / 2),
+                         (uint16_t*)p.ks + dst_row * (p.D / 32), lane, fwht_norm);
+  else if (k_int8)
     quantize_row<VPL>(k_new + src_off, (int8_t*)p.k + dst_row * p.D,
                       (uint16_t*)p.ks + dst_row * p.ng, lane, lpg);
   else
     copy_row<VPL>(k_new + src_off, (uint16_t*)p.k + dst_row * p.D, lane);
-  if (p.v4)   // k8v4: rotated, then Q4_0 (D/2 bytes and D/32 scales per row)
+  if (p.v4)   // k8v4, q4_0: rotated, then Q4_0 (D/2 bytes and D/32 scales per row)
     quantize_row_q4<VPL>(v_new + src_off, (uint8_t*)p.v + dst_row * (p.D / 2),
                          (uint16_t*)p.vs + dst_row * (p.D / 32), lane, fwht_norm);
   else if (v_int8)

@@ -119,3 +119,17 @@ def test_k8v4_region_bytes(L):
     h = ctypes.c_void_p()
     # the 4-bit store needs its scales
     assert L.kv_pool_create(ctypes.byref(h), 1, 2, 256, 64, 64, 4, 3, a16, a16, a16, None, None) == -2
+
+
+def test_q4_0_region_bytes(L):
+    """q4_0: K and V both two 4-bit codes per byte and one fp16 scale per 32 values
+    (head_dim 128, 2 kv heads: 128 + 16 B per store and position); both scales
+    regions are required."""
+    from int8_kv_cache_02_gb300 import binding as b
+    r = [b.int8kv_pool_region_bytes(1, 2, 128, 128, 64, 1, b.Q4_0, k) for k in range(4)]
+    assert r == [64 * 128, 64 * 128, 64 * 16, 64 * 16]
+    a16 = ctypes.c_void_p(0x10000)
+    h = ctypes.c_void_p()
+    assert L.kv_pool_create(ctypes.byref(h), 1, 2, 128, 128, 64, 4, 4, a16, a16, None, a16, None) == -2
+    assert L.kv_pool_create(ctypes.byref(h), 1, 2, 128, 128, 64, 4, 4, a16, a16, a16, None, None) == -2
+    assert L.kv_pool_create(ctypes.byref(h), 1, 2, 128, 128, 64, 4, 5, a16, a16, a16, a16, None) == -1
