@@ -46,9 +46,12 @@
  *                  PR": --kv q4_0): the rows of K are rotated before they are
  *                  stored, decode rotates each query the same way (scores are
  *                  unchanged, the transform being orthonormal) and the output
- *                  back.  Decode on the CUDA-core kernel only, one query per
- *                  sequence (no query windows, no prefill chunk); group_size
- *                  is validated but no store uses it.
+ *                  back.  At head_dim 256 the tensor-core decode serves it
+ *                  (query windows included; a rotated query must stay within
+ *                  the fp16 range, as it is fed as an fp16 hi + lo pair); at
+ *                  64 and 128 the CUDA-core kernel, one query per sequence.
+ *                  No prefill chunk.  group_size is validated but no store
+ *                  uses it.
  *
  * Pool layout in device memory (caller-allocated; the library never
  * allocates device memory):

@@ -126,7 +126,7 @@ static void query_residency(const int8kv_pool* pool, int kind) {
     int prev = -1;
     if (cudaGetDevice(&prev) == cudaSuccess && prev != pool->device) cudaSetDevice(pool->device);
     n = decode_mma_resident_blocks(pool->head_dim, pool->k_int8, pool->v_int8, pool->n_groups,
-                                   pool->v_q4);
+                                   pool->v_q4, pool->k_q4);
     if (prev >= 0 && prev != pool->device) cudaSetDevice(prev);
   }
   mp->resident[kind] = n > 0 ? n : 3 * pool->num_sms;
@@ -265,13 +265,12 @@ int kv_pool_create(int8kv_pool** out, int n_layers, int n_kv_heads, int head_dim
   p->decode_kernel = INT8KV_DECODE_AUTO;
   for (int k = 0; k < 4; ++k) p->resident[k] = 0;
   p->expire_polls = 0;
-  // TMA descriptors for the tensor-core kernels; the 4-bit V store is mapped as
-  // rows of head_dim / 2 bytes (head_dim 256 only: one 128-byte box a row).  A
-  // 4-bit K store is decoded on the CUDA cores only.
-  if (page_size == 64 && (head_dim == 128 || head_dim == 256) && (!v4 || head_dim == 256) &&
-      !k4) {
+  // TMA descriptors for the tensor-core kernels; a 4-bit store is mapped as
+  // rows of head_dim / 2 bytes (head_dim 256 only: one 128-byte box a row)
+  if (page_size == 64 && (head_dim == 128 || head_dim == 256) && (!v4 || head_dim == 256)) {
     const size_t rows = (size_t)n_layers * n_pages * n_kv_heads * page_size;
-    if (rows >= (1ull << 31) || !make_store_map(&p->tmap_k, k_store, k8, head_dim, rows) ||
+    if (rows >= (1ull << 31) ||
+        !make_store_map(&p->tmap_k, k_store, k8 || k4, k4 ? head_dim / 2 : head_dim, rows) ||
         !make_store_map(&p->tmap_v, v_store, v8 || v4, v4 ? head_dim / 2 : head_dim, rows)) {
       delete p;
       return INT8KV_ERR_CUDA;

@@ -27,7 +27,7 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, bool k_int8, bool v_int8,
                                cudaStream_t stream);
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t stream);
 bool decode_mma_supported(const PoolView& p, int G);
-int decode_mma_resident_blocks(int D, bool k8, bool v8, int ng, bool v4);
+int decode_mma_resident_blocks(int D, bool k8, bool v8, int ng, bool v4, bool k4);
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool k8, bool v8, const CUtensorMap& tmk,
                               const CUtensorMap& tmv, int layer_page0, cudaStream_t stream);
 

@@ -99,12 +99,15 @@ __device__ __forceinline__ int column_group(int Hkv) {
   return y / Hkv;
 }
 
-template <int D, bool KI8, bool VI8, bool VQ4>
-struct Layout : mma::StagedPage<D, KI8, VI8, VQ4> {
-  using SP = mma::StagedPage<D, KI8, VI8, VQ4>;
+template <int D, bool KI8, bool VI8, bool VQ4, bool KQ4 = false>
+struct Layout : mma::StagedPage<D, KI8, VI8, VQ4, KQ4> {
+  using SP = mma::StagedPage<D, KI8, VI8, VQ4, KQ4>;
+  // 4-bit K: the rotated queries' score fragments, fp16 hi + lo pairs, 16 bytes
+  // per (k-step, column, lane quarter)
+  static constexpr int QFB = KQ4 ? D * 32 : 0;
   // stage budget: three blocks per SM at head_dim 256, four at 128 (whose
   // accumulators fit in the 128 registers that leaves a thread)
-  static constexpr int NS_FIT = ((D == 128 ? 52 : 70) * 1024) / SP::STAGE;
+  static constexpr int NS_FIT = ((D == 128 ? 52 : 70) * 1024 - QFB) / SP::STAGE;
   static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 4 ? 4 : NS_FIT);
   // epilogue buffers (reuse the stages): warp partials [warp][head 8][DP], block
   // partial [8][D].  Row pitch DP and dim placement make the warps' fragment
@@ -114,13 +117,14 @@ struct Layout : mma::StagedPage<D, KI8, VI8, VQ4> {
   static constexpr int DP = (VI8 || VQ4) ? ((D + D / 32) / 16 + 1) * 16 + 1 : D + 4;
   static constexpr int MERGE = kConsumerWarps * 8 * DP * 4 + 8 * D * 4;
   static constexpr int BARS = NS * SP::STAGE;
-  static constexpr int SMEM = 1024 + BARS + 2 * NS * 8 + NS * 4 + 64;   // stages, barriers, page ids
+  static constexpr int QF_OFF = (BARS + 2 * NS * 8 + NS * 4 + 64 + 127) / 128 * 128;
+  static constexpr int SMEM = 1024 + QF_OFF + QFB;   // stages, barriers, page ids, q fragments
   static_assert(MERGE <= NS * SP::STAGE, "merge buffer must fit in the stages");
   // Request pages 1 .. NS-1 only once page 0 has landed (see the kernel).  Only
   // where the tile arithmetic paces the kernel (int8 K and V at head_dim 256):
   // there the smaller first burst lets every block start computing sooner; the
   // byte-bound variants lose more from the shallower start than they gain.
-  static constexpr bool DEFER = D == 256 && KI8 && (VI8 || VQ4);
+  static constexpr bool DEFER = D == 256 && (KI8 || KQ4) && (VI8 || VQ4);
 };
 
 // Codes at byte k of W0 and W1 -> exact f16x2 (lo = W0's, hi = W1's).
@@ -149,7 +153,7 @@ __device__ __forceinline__ uint32_t q4_hi(uint32_t x) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-template <int D, bool KI8, bool VI8, bool VQ4>
+template <int D, bool KI8, bool VI8, bool VQ4, bool KQ4 = false>
 __device__ __forceinline__ void issue_page(unsigned char* smem, uint64_t* full, int* stage_page,
                                            int st, int page, int row, const PoolView& p, int kvh,
                                            const CUtensorMap* tmk, const CUtensorMap* tmv,
@@ -159,8 +163,9 @@ __device__ __forceinline__ void issue_page(unsigned char* smem, uint64_t* full, 
     ptx::mbar_arrive_expect_tx(&full[st], 16);
     return;
   }
-  mma::issue_page<D, KI8, VI8, true, VQ4>(smem + st * Layout<D, KI8, VI8, VQ4>::STAGE, &full[st],
-                                     &stage_page[st], page, row, p, kvh, tmk, tmv);
+  mma::issue_page<D, KI8, VI8, true, VQ4, KQ4>(smem + st * Layout<D, KI8, VI8, VQ4, KQ4>::STAGE,
+                                               &full[st], &stage_page[st], page, row, p, kvh, tmk,
+                                               tmv);
 }
 
 template <int NG>
@@ -281,13 +286,14 @@ struct NewRowQ4 {
 // softmax (lazy: the reference max moves only when a score exceeds it by more
 // than 2^kTau), and the P.V accumulation.  FULL: every token of the tile is in
 // [j0, j1), so no masking.
-template <int D, bool KI8, bool VI8, int NG, bool FULL, bool VQ4>
+template <int D, bool KI8, bool VI8, int NG, bool FULL, bool VQ4, bool KQ4>
 __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, int lane, int tile0,
                                             int j0, int j1, const uint32_t (&qf)[D / 16][2],
-                                            float scale_log2, float (&o)[D / 16][4], float& m0,
-                                            float& m1, float& l0, float& l1, float (&cap)[NG],
-                                            float (&sh)[NG], int (&vexp)[NG], int lim0, int lim1) {
-  using LY = Layout<D, KI8, VI8, VQ4>;
+                                            const uint4* qfrag, float scale_log2,
+                                            float (&o)[D / 16][4], float& m0, float& m1, float& l0,
+                                            float& l1, float (&cap)[NG], float (&sh)[NG],
+                                            int (&vexp)[NG], int lim0, int lim1) {
+  using LY = Layout<D, KI8, VI8, VQ4, KQ4>;
   constexpr int MACROS = D / 64, MTILES = D / 16;
   constexpr int NGV = VQ4 ? D / 32 : (VI8 ? NG : 1);   // V scale groups (4-bit store: of 32)
   constexpr int MPG = VQ4 ? 0 : MACROS / NGV;   // 64-dim macros per V scale group
@@ -303,7 +309,55 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
 
   // ---- scores: s[0..1] token A heads (2t, 2t+1); s[2..3] token B
   float s[4] = {0.f, 0.f, 0.f, 0.f};
-  if constexpr (KI8) {
+  if constexpr (KQ4) {
+    // 4-bit K (rotated rows, Q4_0 blocks of 32 values, signed fp16 scales): the
+    // lane loads chunks t and t + 4 of its two rows, values 32g + 4t + j and
+    // 32g + 16 + 4t + j of every block g.  Block g is two k-steps (chunk t, then
+    // t + 4); in each, k-slots (2t, 2t + 1) take the low nibbles of bytes 2g and
+    // 2g + 1 (values 4t + 0, 4t + 2 of the chunk's group) and slots (2t + 8,
+    // 2t + 9) their high nibbles (4t + 1, 4t + 3); the rotated query fragments
+    // follow the same order, as fp16 hi + lo pairs (two MMAs per k-step).
+    const int sa_ = rowA, sb_ = rowB & 7;
+    const unsigned char* kA = sb + LY::K_OFF + trA * 128;
+    const unsigned char* kB = sb + LY::K_OFF + trB * 128;
+    const uint4 ca[2] = {*reinterpret_cast<const uint4*>(kA + ((t ^ sa_) << 4)),
+                         *reinterpret_cast<const uint4*>(kA + (((t + 4) ^ sa_) << 4))};
+    const uint4 cb[2] = {*reinterpret_cast<const uint4*>(kB + ((t ^ sb_) << 4)),
+                         *reinterpret_cast<const uint4*>(kB + (((t + 4) ^ sb_) << 4))};
+    const uint4 dsa = *reinterpret_cast<const uint4*>(sb + LY::KS_OFF + trA * 16);
+    const uint4 dsb = *reinterpret_cast<const uint4*>(sb + LY::KS_OFF + trB * 16);
+    const uint32_t dA[4] = {dsa.x, dsa.y, dsa.z, dsa.w}, dB[4] = {dsb.x, dsb.y, dsb.z, dsb.w};
+    const uint4* qv = qfrag + r * 4 + t;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int wi = g >> 1;
+        const uint32_t wa = wi == 0 ? ca[h].x : wi == 1 ? ca[h].y : wi == 2 ? ca[h].z : ca[h].w;
+        const uint32_t wb = wi == 0 ? cb[h].x : wi == 1 ? cb[h].y : wi == 2 ? cb[h].z : cb[h].w;
+        const uint32_t sel = (g & 1) ? 0x4342u : 0x4140u;   // bytes 2g, 2g + 1 -> bytes 0, 2
+        const uint32_t xa = ptx::prmt(wa, 0u, sel), xb = ptx::prmt(wb, 0u, sel);
+        uint32_t af[4];
+        af[0] = q4_lo(xa);
+        af[1] = q4_lo(xb);
+        af[2] = q4_hi(xa);
+        af[3] = q4_hi(xb);
+        const uint4 qq = qv[(g * 2 + h) * 32];
+        ptx::mma_f16(acc, af, qq.x, qq.y);
+        ptx::mma_f16(acc, af, qq.z, qq.w);
+      }
+      const uint32_t pa = dA[g >> 1], pb = dB[g >> 1];
+      const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pa));
+      const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
+      const float sa = ((g & 1) ? fa.y : fa.x) * scale_log2;
+      const float sbb = ((g & 1) ? fb.y : fb.x) * scale_log2;
+      s[0] = fmaf(acc[0], sa, s[0]);
+      s[1] = fmaf(acc[1], sa, s[1]);
+      s[2] = fmaf(acc[2], sbb, s[2]);
+      s[3] = fmaf(acc[3], sbb, s[3]);
+    }
+  } else if constexpr (KI8) {
     float ka[NG], kb[NG];
     load_row_scales<NG>(sb + LY::KS_OFF, trA, ka);
     load_row_scales<NG>(sb + LY::KS_OFF, trB, kb);
@@ -625,11 +679,13 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
 // WIN: a window of q_len queries per sequence (attn_decode_multi_int8); without
 // it the kernel serves one query per sequence and none of the window's column
 // arithmetic is compiled in.
-template <int D, bool KI8, bool VI8, int NG, bool WIN, bool VQ4>
+template <int D, bool KI8, bool VI8, int NG, bool WIN, bool VQ4, bool KQ4 = false>
 __global__ void __launch_bounds__(kThreads, D == 128 ? 4 : 3)
 decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, int layer_page0) {
-  using LY = Layout<D, KI8, VI8, VQ4>;
+  static_assert(!KQ4 || (D == 256 && VQ4 && !KI8 && !VI8 && NG == 1),
+                "4-bit K: head_dim 256, with the 4-bit V store");
+  using LY = Layout<D, KI8, VI8, VQ4, KQ4>;
   constexpr int KSTEPS = D / 16;     // 16-dim k-steps of q.K^T
   constexpr int MACROS = D / 64;     // 64-dim groups
   constexpr int MTILES = D / 16;     // 16-dim M-tiles of P.V
@@ -689,10 +745,12 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     const int pg = s1 > s0 ? ptx::ldcg32(a.page_table + (size_t)b * a.max_pages + s0 / kPage) : -1;
     if (pg >= 0 && pg < p.n_pages) {
       const size_t r0 = ((size_t)pg * p.Hkv + kvh) * kPage;   // first row of the page-head
-      ptx::bulk_prefetch_l2((const char*)p.k + r0 * D * (KI8 ? 1 : 2), (KI8 ? 1 : 2) * D * kPage);
+      constexpr int KROW = KQ4 ? D / 2 : (KI8 ? D : 2 * D);   // bytes of a K row
       constexpr int VROW = VQ4 ? D / 2 : (VI8 ? D : 2 * D);   // bytes of a V row
+      ptx::bulk_prefetch_l2((const char*)p.k + r0 * KROW, KROW * kPage);
       ptx::bulk_prefetch_l2((const char*)p.v + r0 * VROW, VROW * kPage);
       if (KI8) ptx::bulk_prefetch_l2(p.ks + r0 * NG, kPage * NG * 2);
+      if (KQ4) ptx::bulk_prefetch_l2(p.ks + r0 * (D / 32), kPage * (D / 32) * 2);
       if (VI8) ptx::bulk_prefetch_l2(p.vs + r0 * NG, kPage * NG * 2);
       if (VQ4) ptx::bulk_prefetch_l2(p.vs + r0 * (D / 32), kPage * (D / 32) * 2);
     }
@@ -730,7 +788,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
       if constexpr (KI8)
         qraw[v] = live ? ptx::ldg128(qh + (v >> 1) * 64 + 16 * t + 8 * (v & 1)) : make_uint4(0, 0, 0, 0);
     }
-    if constexpr (!KI8) {
+    if constexpr (!KI8 && !KQ4) {
       const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qh);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
@@ -762,7 +820,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   const int app_slot = (L - 1) & (kPage - 1);
   const bool app_k = appends && warp == app_slot / 16;
   const bool app_v = appends && warp == ((app_slot / 16) ^ 1);
-  NewRow<D, KI8> nk;
+  std::conditional_t<KQ4, NewRowQ4, NewRow<D, KI8>> nk;
   std::conditional_t<VQ4, NewRowQ4, NewRow<D, VI8>> nv;
   if (app_k) nk.fetch(a.k_new + ((size_t)b * p.Hkv + kvh) * D, lane);
   if (app_v) nv.fetch(a.v_new + ((size_t)b * p.Hkv + kvh) * D, lane);
@@ -793,7 +851,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     for (int i = 0; i < LY::NS; ++i)
       if (i < n_pg) {
         if (i == 0 || appends || !LY::DEFER)
-          issue_page<D, KI8, VI8, VQ4>(smem, full, stage_page, i, first[i], page_row(first[i]), p, kvh,
+          issue_page<D, KI8, VI8, VQ4, KQ4>(smem, full, stage_page, i, first[i], page_row(first[i]), p, kvh,
                                   &tmk, &tmv, a.expire_polls != 0);
         else
           stage_page[i] = first[i];   // kept for the request after page 0 lands; no consumer
@@ -808,7 +866,48 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
     return i < kPagesCached ? s_pages[i] : lookup_page(ptrow, p_first + i, a.max_pages, p);
   };
   uint32_t qf[KSTEPS][2];
-  if constexpr (KI8) {
+  const uint4* qfrag = reinterpret_cast<const uint4*>(smem + LY::QF_OFF);
+  if constexpr (KQ4) {
+    // Rotated queries for the 4-bit K store: warp w rotates columns w and w + 4
+    // (a lane 8 consecutive dims; the same fp32 FWHT as the store), splits each
+    // value into an fp16 hi + lo pair and stores them in the tile's k-slot order:
+    // dims 8 lane + 4u + j are values 32g + 16h + 4t + j with g = lane / 4,
+    // h = (lane / 2) & 1, t = 2 (lane & 1) + u; the piece of (g, h, column c,
+    // t) holds the pairs (j0, j2), (j1, j3) of hi, then of lo.
+    uint4* qw = reinterpret_cast<uint4*>(smem + LY::QF_OFF);
+    for (int c = warp; c < 8; c += kConsumerWarps) {
+      float x[8];
+      if (c < ncol()) {
+        const uint4 raw = ptx::ldg128(a.q + col_row(c) * D + lane * 8);
+        const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(h2[i]);
+          x[2 * i] = f.x;
+          x[2 * i + 1] = f.y;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = 0.f;
+      }
+      fwht_row<8>(x, lane, 0.0625f);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        uint16_t hi[4], lo[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __half h = __float2half_rn(x[4 * u + j]);
+          hi[j] = __half_as_ushort(h);
+          lo[j] = __half_as_ushort(__float2half_rn(x[4 * u + j] - __half2float(h)));
+        }
+        const int g = lane >> 2, h = (lane >> 1) & 1, tt = 2 * (lane & 1) + u;
+        qw[((g * 2 + h) * 8 + c) * 4 + tt] =
+            make_uint4(hi[0] | ((uint32_t)hi[2] << 16), hi[1] | ((uint32_t)hi[3] << 16),
+                       lo[0] | ((uint32_t)lo[2] << 16), lo[1] | ((uint32_t)lo[3] << 16));
+      }
+    }
+    __syncthreads();
+  } else if constexpr (KI8) {
 #pragma unroll
     for (int mc = 0; mc < MACROS; ++mc) {
       // dims 64mc + 16t .. +16: k-step i takes (4i, 4i+2) and (4i+1, 4i+3)
@@ -891,7 +990,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
         for (int k = 1; k < LY::NS; ++k)
           if (k < n_pg) {
             const int pg = stage_page[k];
-            issue_page<D, KI8, VI8, VQ4>(smem, full, stage_page, k, pg, page_row(pg), p, kvh, &tmk,
+            issue_page<D, KI8, VI8, VQ4, KQ4>(smem, full, stage_page, k, pg, page_row(pg), p, kvh, &tmk,
                                     &tmv, a.expire_polls != 0);
           }
       }
@@ -901,10 +1000,12 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
         const unsigned char* sb = smem + st * LY::STAGE;
         // a tile that ends by the first query's position needs no per-column test
         if (tile0 >= j0 && tile0 + 16 <= j1 && (!WIN || tile0 + 16 <= s_q0[warp] + 1)) {
-          decode_tile<D, KI8, VI8, NG, true, VQ4>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
+          decode_tile<D, KI8, VI8, NG, true, VQ4, KQ4>(sb, warp, lane, tile0, j0, j1, qf, qfrag,
+              a.scale_log2, o,
                                              m0, m1, l0, l1, cap, sh, vexp, 0, 0);
         } else if constexpr (!WIN) {
-          decode_tile<D, KI8, VI8, NG, false, VQ4>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
+          decode_tile<D, KI8, VI8, NG, false, VQ4, KQ4>(sb, warp, lane, tile0, j0, j1, qf, qfrag,
+              a.scale_log2, o,
                                               m0, m1, l0, l1, cap, sh, vexp, INT_MAX, INT_MAX);
         } else {
           // causal limits of the lane's columns 2t, 2t + 1 (a dead column: L - 1)
@@ -912,7 +1013,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
           auto lim = [&](int c) {
             return c < nc ? q0 + (column_group(p.Hkv) * 8 + c) / G : q0 + a.q_len - 1;
           };
-          decode_tile<D, KI8, VI8, NG, false, VQ4>(sb, warp, lane, tile0, j0, j1, qf, a.scale_log2, o,
+          decode_tile<D, KI8, VI8, NG, false, VQ4, KQ4>(sb, warp, lane, tile0, j0, j1, qf, qfrag,
+              a.scale_log2, o,
                                               m0, m1, l0, l1, cap, sh, vexp, lim(c0), lim(c0 + 1));
         }
       }
@@ -925,7 +1027,7 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
             kConsumerWarps - 1) {
           if (i + LY::NS < n_pg) {
             const int page = page_of(i + LY::NS);
-            issue_page<D, KI8, VI8, VQ4>(smem, full, stage_page, st, page, page_row(page), p, kvh,
+            issue_page<D, KI8, VI8, VQ4, KQ4>(smem, full, stage_page, st, page, page_row(page), p, kvh,
                                     &tmk, &tmv, a.expire_polls != 0);
           }
         }
@@ -1116,11 +1218,11 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   cluster.sync();   // no block leaves while others read its shared memory
 }
 
-template <int D, bool KI8, bool VI8, int NG, bool WIN, bool VQ4>
+template <int D, bool KI8, bool VI8, int NG, bool WIN, bool VQ4, bool KQ4 = false>
 cudaError_t launch_typed(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
                          int layer_page0, cudaStream_t stream) {
-  using LY = Layout<D, KI8, VI8, VQ4>;
-  auto kern = decode_mma_kernel<D, KI8, VI8, NG, WIN, VQ4>;
+  using LY = Layout<D, KI8, VI8, VQ4, KQ4>;
+  auto kern = decode_mma_kernel<D, KI8, VI8, NG, WIN, VQ4, KQ4>;
   static bool configured[64] = {};   // per device: the attribute belongs to the device's function
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1153,9 +1255,11 @@ cudaError_t launch_typed(const DecodeArgs& a, const CUtensorMap& tmk, const CUte
 }  // namespace
 
 bool decode_mma_supported(const PoolView& p, int G) {
-  return G <= 8 && p.ps == kPage && (p.D == 128 || p.D == 256) && p.gs >= 64 && p.gs % 64 == 0 &&
+  // group_size only shapes an int8 store (q4_0 has none)
+  const bool groups_ok = (p.k4 && p.v4) || (p.gs >= 64 && p.gs % 64 == 0);
+  return G <= 8 && p.ps == kPage && (p.D == 128 || p.D == 256) && groups_ok &&
          (!p.v4 || p.D == 256) &&   // the 4-bit V store: head_dim 256 (one 128-byte box a row)
-         !p.k4;                     // a 4-bit K store: the CUDA-core kernel
+         (!p.k4 || p.v4);           // a 4-bit K store comes with a 4-bit V store (q4_0)
 }
 
 template <int D, bool KI8, bool VI8, bool WIN, bool VQ4>
@@ -1181,6 +1285,12 @@ cudaError_t launch_win(const DecodeArgs& a, const CUtensorMap& tmk, const CUtens
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool k8, bool v8, const CUtensorMap& tmk,
                               const CUtensorMap& tmv, int layer_page0, cudaStream_t stream) {
+  if (a.pool.k4) {   // q4_0: head_dim 256 only
+    if (a.pool.D != 256 || !a.pool.v4) return cudaErrorNotSupported;
+    return a.q_len > 1
+               ? launch_typed<256, false, false, 1, true, true, true>(a, tmk, tmv, layer_page0, stream)
+               : launch_typed<256, false, false, 1, false, true, true>(a, tmk, tmv, layer_page0, stream);
+  }
   if (a.pool.D == 256) {
     if (a.pool.v4) return launch_win<256, true, false, true>(a, tmk, tmv, layer_page0, stream);
     if (k8 && v8) return launch_win<256, true, true, false>(a, tmk, tmv, layer_page0, stream);
@@ -1193,10 +1303,10 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, bool k8, bool v8, const CUten
   return launch_win<128, false, true, false>(a, tmk, tmv, layer_page0, stream);
 }
 
-template <int D, bool KI8, bool VI8, int NG, bool VQ4>
+template <int D, bool KI8, bool VI8, int NG, bool VQ4, bool KQ4 = false>
 int resident_typed() {
-  using LY = Layout<D, KI8, VI8, VQ4>;
-  auto kern = decode_mma_kernel<D, KI8, VI8, NG, false, VQ4>;
+  using LY = Layout<D, KI8, VI8, VQ4, KQ4>;
+  auto kern = decode_mma_kernel<D, KI8, VI8, NG, false, VQ4, KQ4>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM) !=
       cudaSuccess)
     return 0;
@@ -1220,7 +1330,8 @@ int resident_ng(int ng) {
 
 // Blocks of the tensor-core kernel for this shape that the current device keeps
 // resident at once; 0 if unknown.
-int decode_mma_resident_blocks(int D, bool k8, bool v8, int ng, bool v4) {
+int decode_mma_resident_blocks(int D, bool k8, bool v8, int ng, bool v4, bool k4) {
+  if (k4) return D == 256 && v4 ? resident_typed<256, false, false, 1, true, true>() : 0;
   if (D == 256) {
     if (v4) return resident_ng<256, true, false, true>(ng);
     if (k8 && v8) return resident_ng<256, true, true>(ng);

@@ -19,12 +19,12 @@ constexpr int kBoxBytes = kPage * 128;     // one swizzled TMA box: 64 rows x 12
 constexpr uint32_t kMaxPolls = 1u << 22;   // bounded mbarrier waits (well over any copy time)
 
 // One staged page of one kv head: K rows, V rows (int8: 128-dim boxes; fp16:
-// 64-dim boxes; 4-bit (VQ4, head_dim 256): one 128-byte box of packed codes per
-// row; each box 64 rows x 128 B, 128-byte swizzle), then the K and V scales
-// rows ([64][ng] fp16 of an int8 store; [64][D/32] of the 4-bit store).
-template <int D, bool KI8, bool VI8, bool VQ4 = false>
+// 64-dim boxes; 4-bit (VQ4 / KQ4, head_dim 256): one 128-byte box of packed
+// codes per row; each box 64 rows x 128 B, 128-byte swizzle), then the K and V
+// scales rows ([64][ng] fp16 of an int8 store; [64][D/32] of a 4-bit store).
+template <int D, bool KI8, bool VI8, bool VQ4 = false, bool KQ4 = false>
 struct StagedPage {
-  static constexpr int KBYTES = KI8 ? D * kPage : 2 * D * kPage;
+  static constexpr int KBYTES = KQ4 ? D / 2 * kPage : (KI8 ? D * kPage : 2 * D * kPage);
   static constexpr int VBYTES = VQ4 ? D / 2 * kPage : (VI8 ? D * kPage : 2 * D * kPage);
   static constexpr int KBOXES = KBYTES / kBoxBytes;
   static constexpr int VBOXES = VBYTES / kBoxBytes;
@@ -33,7 +33,7 @@ struct StagedPage {
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = KBYTES;
   static constexpr int KS_OFF = KBYTES + VBYTES;
-  static constexpr int VS_OFF = KS_OFF + (KI8 ? SCALE_BYTES : 0);
+  static constexpr int VS_OFF = KS_OFF + (KI8 ? SCALE_BYTES : (KQ4 ? VQ4_SCALE_BYTES : 0));
   static constexpr int RAW = VS_OFF + (VI8 ? SCALE_BYTES : (VQ4 ? VQ4_SCALE_BYTES : 0));
   static constexpr int STAGE = (RAW + 1023) / 1024 * 1024;
 };
@@ -64,11 +64,11 @@ __device__ __forceinline__ int exponent_of(float x) {   // floor(log2 x), x > 0 
 // stage's barrier with no bytes) into stage `st`.  kStream: the page is read
 // once (decode), so its L2 lines go first; otherwise (prefill: every query tile
 // of the kv head reads it) the default policy keeps it for the other blocks.
-template <int D, bool KI8, bool VI8, bool kStream = false, bool VQ4 = false>
+template <int D, bool KI8, bool VI8, bool kStream = false, bool VQ4 = false, bool KQ4 = false>
 __device__ __forceinline__ void issue_page(unsigned char* stage, uint64_t* full_bar, int* stage_page,
                                            int page, int row, const PoolView& p, int kvh,
                                            const CUtensorMap* tmk, const CUtensorMap* tmv) {
-  using SP = StagedPage<D, KI8, VI8, VQ4>;
+  using SP = StagedPage<D, KI8, VI8, VQ4, KQ4>;
   *stage_page = page;
   if (page < 0) {
     ptx::mbar_arrive(full_bar);
@@ -76,13 +76,15 @@ __device__ __forceinline__ void issue_page(unsigned char* stage, uint64_t* full_
   }
   const int ng = p.ng;
   constexpr uint32_t VSB = VQ4 ? SP::VQ4_SCALE_BYTES : 0;   // 4-bit store: D/32 scales a row
-  const uint32_t tx = SP::KBYTES + SP::VBYTES + (KI8 ? kPage * ng * 2 : 0) +
+  constexpr uint32_t KSB = KQ4 ? SP::VQ4_SCALE_BYTES : 0;
+  const uint32_t tx = SP::KBYTES + SP::VBYTES + (KI8 ? kPage * ng * 2 : KSB) +
                       (VI8 ? kPage * ng * 2 : VSB);
   ptx::mbar_arrive_expect_tx(full_bar, tx);
-  constexpr int KX = KI8 ? 128 : 64;   // box width in elements
+  constexpr int KX = (KI8 || KQ4) ? 128 : 64;   // box width in elements
   constexpr int VX = (VI8 || VQ4) ? 128 : 64;
   const size_t srow = ((size_t)page * p.Hkv + kvh) * kPage * ng;
   const size_t vsrow = ((size_t)page * p.Hkv + kvh) * kPage * (VQ4 ? D / 32 : ng);
+  const size_t q4row = ((size_t)page * p.Hkv + kvh) * kPage * (D / 32);   // 4-bit K scales
   if constexpr (kStream) {
     const uint64_t pol = ptx::policy_evict_first();
 #pragma unroll
@@ -92,6 +94,7 @@ __device__ __forceinline__ void issue_page(unsigned char* stage, uint64_t* full_
     for (int bx = 0; bx < SP::VBOXES; ++bx)
       ptx::tma_load_2d_hint(stage + SP::V_OFF + bx * kBoxBytes, tmv, bx * VX, row, full_bar, pol);
     if (KI8) ptx::bulk_load_hint(stage + SP::KS_OFF, p.ks + srow, kPage * ng * 2, full_bar, pol);
+    if (KQ4) ptx::bulk_load_hint(stage + SP::KS_OFF, p.ks + q4row, KSB, full_bar, pol);
     if (VI8) ptx::bulk_load_hint(stage + SP::VS_OFF, p.vs + srow, kPage * ng * 2, full_bar, pol);
     if (VQ4) ptx::bulk_load_hint(stage + SP::VS_OFF, p.vs + vsrow, VSB, full_bar, pol);
   } else {
@@ -102,6 +105,7 @@ __device__ __forceinline__ void issue_page(unsigned char* stage, uint64_t* full_
     for (int bx = 0; bx < SP::VBOXES; ++bx)
       ptx::tma_load_2d(stage + SP::V_OFF + bx * kBoxBytes, tmv, bx * VX, row, full_bar);
     if (KI8) ptx::bulk_load(stage + SP::KS_OFF, p.ks + srow, kPage * ng * 2, full_bar);
+    if (KQ4) ptx::bulk_load(stage + SP::KS_OFF, p.ks + q4row, KSB, full_bar);
     if (VI8) ptx::bulk_load(stage + SP::VS_OFF, p.vs + srow, kPage * ng * 2, full_bar);
     if (VQ4) ptx::bulk_load(stage + SP::VS_OFF, p.vs + vsrow, VSB, full_bar);
   }

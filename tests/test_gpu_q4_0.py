@@ -44,8 +44,9 @@ def test_append_is_bit_exact(D, gs):
     assert binding.kv_pool_read_device_error(dev) == 0
 
 
-def _decode(dev, q, lens, pt, n_splits, window=0):
+def _decode(dev, q, lens, pt, n_splits, window=0, kind=0):
     from int8_kv_cache_02_gb300 import binding
+    dev.set_decode_kernel(kind)
     B, H, D = q.shape
     out = torch.full((B, H, D), float("nan"), dtype=torch.float32, device="cuda")
     binding.attn_decode_int8(dev, 0, q.cuda(), torch.tensor(lens, dtype=torch.int32, device="cuda"),
@@ -56,7 +57,7 @@ def _decode(dev, q, lens, pt, n_splits, window=0):
 
 
 @pytest.mark.parametrize("D,gs,H,Hkv", [(256, 64, 16, 2), (128, 128, 8, 2), (64, 32, 12, 4),
-                                        (128, 64, 32, 8)])
+                                        (128, 64, 32, 8), (256, 32, 12, 4), (256, 256, 8, 8)])
 @pytest.mark.parametrize("n_splits", [1, 4, 16])
 def test_decode_matches_oracle(D, gs, H, Hkv, n_splits):
     from int8_kv_cache_02_gb300 import binding
@@ -66,19 +67,23 @@ def test_decode_matches_oracle(D, gs, H, Hkv, n_splits):
     dev, orc = gu.make_pools(1, Hkv, D, gs, 64, n_pages, Q4_0)
     for b in range(len(lens)):
         gu.fill_sequence(dev, orc, 0, ks[b], vs[b], pt[b])
+    # head_dim 256: the tensor-core kernel (AUTO) and the CUDA-core one; else CUDA cores
+    kinds = [binding.DECODE_AUTO, binding.DECODE_SIMT] if D == 256 else [binding.DECODE_AUTO]
     for window in (0, 200):
         ref = np.stack([oatt.decode(q[b].numpy(), *orc.gather(0, pt[b].numpy(), L), L, window=window)
                         for b, L in enumerate(lens)])
-        got = _decode(dev, q, lens, pt, n_splits, window)
-        gu.assert_attention_close(got, ref, f"q4_0 D{D} H{H} ns{n_splits} w{window}")
+        for kind in kinds:
+            got = _decode(dev, q, lens, pt, n_splits, window, kind)
+            gu.assert_attention_close(got, ref, f"q4_0 D{D} H{H} ns{n_splits} w{window} kind{kind}")
     assert binding.kv_pool_read_device_error(dev) == 0
 
 
-def test_closed_forms():
+@pytest.mark.parametrize("D", [128, 256])
+def test_closed_forms(D):
     """Context 1 returns the stored V row (rotated back); identical keys give the
     mean of the stored V rows, whatever the query."""
     from int8_kv_cache_02_gb300 import binding
-    D, H, Hkv = 128, 4, 1
+    H, Hkv = 4, 1
     g = torch.Generator().manual_seed(9)
     k_row = inputs.normal_f16((1, Hkv, D), g)
     ks = k_row.expand(40, Hkv, D).contiguous()
@@ -137,27 +142,59 @@ def test_fused_step_and_image_round_trip():
     gu.regions_equal(c_dev, c_orc)
 
 
-def test_q4_0_refusals():
-    """A 4-bit K store decodes on the CUDA cores only: the tensor-core kernel, query
-    windows and the prefill chunk are refused (UNSUPPORTED), not served another way."""
+def test_q4_0_kernel_choice_and_refusals():
+    """head_dim 256 decodes on the tensor-core kernel (a row of either store is one
+    128-byte box); head_dim 128 only on the CUDA cores, which serve no query
+    windows; the prefill chunk refuses q4_0 (UNSUPPORTED, not served another way)."""
     from int8_kv_cache_02_gb300 import binding
     dev, _ = gu.make_pools(1, 2, 256, 64, 64, 4, Q4_0)
+    dev.set_decode_kernel(binding.DECODE_WARP_MMA)
+    small, _ = gu.make_pools(1, 2, 128, 64, 64, 4, Q4_0)
     with pytest.raises(binding.Int8KVError):
-        dev.set_decode_kernel(binding.DECODE_WARP_MMA)
+        small.set_decode_kernel(binding.DECODE_WARP_MMA)
     q = torch.zeros((8, 16, 256), dtype=torch.float16, device="cuda")
     out = torch.zeros((8, 16, 256), dtype=torch.float32, device="cuda")
     with pytest.raises(binding.Int8KVError) as e:
         binding.attn_prefill_chunk_int8(dev, 0, q, 0, torch.zeros(4, dtype=torch.int32,
                                                                   device="cuda"), out, None)
     assert e.value.status == -6
-    qw = torch.zeros((1, 2, 16, 256), dtype=torch.float16, device="cuda")
-    ow = torch.zeros((1, 2, 16, 256), dtype=torch.float32, device="cuda")
+    qw = torch.zeros((1, 2, 16, 128), dtype=torch.float16, device="cuda")
+    ow = torch.zeros((1, 2, 16, 128), dtype=torch.float32, device="cuda")
     with pytest.raises(binding.Int8KVError) as e:
-        binding.attn_decode_multi_int8(dev, 0, qw, torch.tensor([10], dtype=torch.int32,
-                                                                device="cuda"),
+        binding.attn_decode_multi_int8(small, 0, qw, torch.tensor([10], dtype=torch.int32,
+                                                                  device="cuda"),
                                        torch.zeros((1, 4), dtype=torch.int32, device="cuda"), ow,
-                                       dev.decode_workspace(2, 16, 1), n_splits=1)
+                                       small.decode_workspace(2, 16, 1), n_splits=1)
     assert e.value.status == -6
+
+
+@pytest.mark.parametrize("q_len,n_splits", [(3, 1), (2, 5), (4, 12)])
+def test_query_windows_q4_0(q_len, n_splits):
+    """Query windows over a q4_0 pool (tensor-core kernel): query i of a window at
+    position L - q_len + i sees keys 0 .. L - q_len + i; every query is rotated."""
+    from int8_kv_cache_02_gb300 import binding
+    lens = [700, 90]
+    B, H = 2, 16
+    g = torch.Generator().manual_seed(80 + q_len)
+    qw = inputs.normal_f16((B, q_len, H, 256), g)
+    _, ks, vs = inputs.random_case(81 + q_len, B, H, 2, 256, lens, outliers=True)
+    pt, n_pages = inputs.page_table(lens, 64, seed=19)
+    dev, orc = gu.make_pools(1, 2, 256, 64, 64, n_pages, Q4_0)
+    for b in range(B):
+        gu.fill_sequence(dev, orc, 0, ks[b], vs[b], pt[b])
+    out = torch.full((B, q_len, H, 256), float("nan"), dtype=torch.float32, device="cuda")
+    binding.attn_decode_multi_int8(dev, 0, qw.cuda(), torch.tensor(lens, dtype=torch.int32,
+                                                                     device="cuda"),
+                                   pt.cuda(), out, dev.decode_workspace(B * q_len, H, n_splits),
+                                   n_splits=n_splits)
+    torch.cuda.synchronize()
+    ref = np.zeros((B, q_len, H, 256))
+    for b, L in enumerate(lens):
+        kh, vh = orc.gather(0, pt[b].numpy(), L)
+        for i in range(q_len):
+            ref[b, i] = oatt.decode(qw[b, i].numpy(), kh, vh, L - q_len + i + 1)
+    gu.assert_attention_close(out.cpu().numpy(), ref, f"q4_0 window {q_len}")
+    assert binding.kv_pool_read_device_error(dev) == 0
 
 
 @pytest.mark.slow
