@@ -284,7 +284,7 @@ def traffic_from_profiles(kernel_src_sha):
 
 
 DECODE_SOURCES = ("common.cuh", "decode_combine.cu", "decode_common.cuh", "decode_mma.cu",
-                  "internal.h", "mma_common.cuh", "ptx.cuh", "quant_row.cuh")
+                  "internal.h", "mma_common.cuh", "ptx.cuh", "q4_row.cuh", "quant_row.cuh")
 
 
 def strip_comments(src):

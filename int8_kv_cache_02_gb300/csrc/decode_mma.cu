@@ -736,7 +736,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   // length or page id that kernel still changes only makes the prefetch
   // useless: the id is checked against the pool before use, and L2 is coherent
   // with the writes that follow.
-  if (threadIdx.x == 0) {
+  const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);   // launch order
+  if (threadIdx.x == 0 && lin < a.pf_blocks) {
     int Ls = ptx::ldcg32(a.seq_lens + b);
     Ls = Ls < 0 ? 0 : min(Ls, a.max_pages * kPage);
     const int lo = a.window > 0 ? max(0, Ls - a.window) : 0;

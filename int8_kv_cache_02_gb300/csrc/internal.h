@@ -99,6 +99,10 @@ struct DecodeArgs {
   // issue no page copies, arm each stage for bytes that never arrive, and give
   // up each wait after this many polls.
   uint32_t expire_polls = 0;
+  // Blocks (in launch order) that prefetch their first page to L2 before the
+  // grid dependency: the first wave only (later blocks start after it has
+  // resolved, and the prefetch would only lengthen their prologue).
+  int pf_blocks = 0;
 };
 
 
