@@ -72,7 +72,7 @@ struct TLayout {
   static constexpr int KH_OFF = ST_OFF + kNS * SP::STAGE;   // converted K page (int8 K only)
   static constexpr int VH_OFF = KH_OFF + (KI8 ? kPage * D * 2 : 0);   // converted V page
   static constexpr int KSF_OFF = VH_OFF + (VI8 ? kPage * D * 2 : 0);   // fp32 K scales x scale [key][NG]
-  static constexpr int VSF_OFF = KSF_OFF + kPage * 4 * 4;               // fp32 V scales [key][NG]
+  static constexpr int VSF_OFF = KSF_OFF + kPage * 4 * 4;               // fp32 V scales [NG][key]
   static constexpr int BAR_OFF = VSF_OFF + kPage * 4 * 4;
   static constexpr int SMEM = 1024 + BAR_OFF + 128;
   // tensor memory: S_g / P'_g region, then O
@@ -159,6 +159,40 @@ __device__ __forceinline__ void convert_side(const unsigned char* src, unsigned 
   }
 }
 
+// The same over threads [t0, kThreads) only (the first warp issues the score
+// MMAs meanwhile): chunk c of thread t is t - t0 + k * (kThreads - t0).
+template <int D, int T0>
+__device__ __forceinline__ void convert_side_from(const unsigned char* src, unsigned char* dst) {
+  constexpr int CPR = D / 16;
+  constexpr int NT = kThreads - T0;
+  constexpr int N = kPage * CPR;
+  constexpr int PER = (N + NT - 1) / NT;
+  const int me = (int)threadIdx.x - T0;
+  if (me < 0) return;
+  uint4 w[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int c = me + k * NT;
+    if (c < N) {
+      const int g8 = c >> 3, row = (g8 / CPR) * 8 + (c & 7), cc = g8 % CPR;
+      w[k] = *reinterpret_cast<const uint4*>(src + (cc >> 3) * kBoxBytes + swz(row, cc & 7));
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int c = me + k * NT;
+    if (c < N) {
+      const int g8 = c >> 3, row = (g8 / CPR) * 8 + (c & 7), cc = g8 % CPR;
+      uint4 lo, hi;
+      codes_to_f16(w[k], lo, hi);
+      unsigned char* box = dst + (cc >> 2) * kBoxBytes;
+      const int c16 = (cc & 3) * 2;
+      *reinterpret_cast<uint4*>(box + swz(row, c16)) = lo;
+      *reinterpret_cast<uint4*>(box + swz(row, c16 + 1)) = hi;
+    }
+  }
+}
+
 // Zero the fp16 rows of a staged side whose keys fall outside [j0, j1) (they
 // may hold any bits, and 0 * NaN would reach O).
 template <int D>
@@ -238,12 +272,12 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
 
   const int32_t* ptrow = a.page_table;
   auto page_row = [&](int page) { return ((layer_page0 + page) * p.Hkv + kvh) * kPage; };
-  auto issue = [&](int i) {
+  auto issue_id = [&](int i, int page) {   // page: a checked id, or -1
     const int st = i % kNS;
-    const int page = lookup_page(ptrow, p_first + i, a.max_pages, p);
     mma::issue_page<D, KI8, VI8>(smem + LY::ST_OFF + st * SP::STAGE, &full[st], &stage_page[st],
                                  page, page_row(page), p, kvh, &tmk, &tmv);
   };
+  auto issue = [&](int i) { issue_id(i, lookup_page(ptrow, p_first + i, a.max_pages, p)); };
   if (tid == 0) {
     ptx::prefetch_tensormap(&tmk);
     ptx::prefetch_tensormap(&tmv);
@@ -267,8 +301,16 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
   __shared__ float s_vmax[4];
   __shared__ float s_mx[kParts][kRows];   // the parts' score maxima (then sums) of each row
 
+  constexpr int kRefill = 32;   // the thread that refills the ring (not in the issuing warp)
   for (int i = 0; i < n_pg; ++i) {
     const int st = i % kNS;
+    // the id of the page the freed stage takes next: loaded now, checked at use,
+    // so that the load's latency passes under the wait and the K conversion
+    const int ri = i - 1 + kNS;
+    const bool refill = tid == kRefill && i > 0 && ri < n_pg;
+    const bool ri_in_row = p_first + ri < a.max_pages;
+    int raw_next = -1;
+    if (refill && ri_in_row) raw_next = ptx::ldg32(ptrow + p_first + ri);
     bool bad = !ptx::mbar_wait(&full[st], (i / kNS) & 1, kMaxPolls);
     unsigned char* sb = smem + LY::ST_OFF + st * SP::STAGE;
     const int page = stage_page[st];
@@ -283,50 +325,45 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
         if (tid < kPage * NG)
           reinterpret_cast<float*>(smem + LY::KSF_OFF)[tid] =
               __half2float(reinterpret_cast<const __half*>(sb + SP::KS_OFF)[tid]) * a.scale_log2;
+      // The V scales are staged too: their table (as [group][key]) and each
+      // group's largest scale among the keys in [j0, j1) (warp 1 + g takes group
+      // g) are formed here, in the wait for the previous P.V batch; both were
+      // last read before this iteration began.
+      if constexpr (VI8) {
+        if (tid < kPage * NG)
+          reinterpret_cast<float*>(smem + LY::VSF_OFF)[(tid % NG) * kPage + tid / NG] =
+              __half2float(reinterpret_cast<const __half*>(sb + SP::VS_OFF)[tid]);
+        const int g = warp - 1;
+        if (g >= 0 && g < NGV) {
+          const uint16_t* vs = reinterpret_cast<const uint16_t*>(sb + SP::VS_OFF);
+          const int lane = tid & 31;
+          float mv = 0.f;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {   // keys 2 lane, 2 lane + 1
+            const int k = 2 * lane + e;
+            if (key0 + k >= j0 && key0 + k < j1)
+              mv = fmaxf(mv, __half2float(__ushort_as_half(vs[k * NG + g])));
+          }
+          mv = warp_max(mv);
+          if (lane == 0) s_vmax[g] = mv;
+        }
+      }
     }
     // the previous P.V batch is done: its V tile, P' columns and stage are free
     if (nO > 0 && !bad) bad = !ptx::mbar_wait(mO, (nO - 1) & 1, kMaxPolls);
+    ptx::fence_proxy_async();   // the converted K tile, before the tensor-core reads
+    tc_fence_before();
     if (__syncthreads_or(bad)) {
       if (tid == 0) s_fail = 1;
       break;
     }
     tc_fence_after();
-    if (tid == 0 && i > 0 && i - 1 + kNS < n_pg) issue(i - 1 + kNS);   // refill the freed stage
-    if (page >= 0) {
-      if constexpr (VI8) convert_side<D>(sb + SP::V_OFF, smem + LY::VH_OFF);
-      if constexpr (!VI8) if (edge) zero_rows<D>(sb + SP::V_OFF, key0, j0, j1);
-      if constexpr (VI8)   // V scales
-        if (tid < kPage * NG)
-          reinterpret_cast<float*>(smem + LY::VSF_OFF)[tid] =
-              __half2float(reinterpret_cast<const __half*>(sb + SP::VS_OFF)[tid]);
-      if constexpr (VI8) {
-        if (warp == 0) {   // the largest V scale of each group among the keys in [j0, j1)
-          const uint16_t* vs = reinterpret_cast<const uint16_t*>(sb + SP::VS_OFF);
-          const int lane = tid & 31;
-#pragma unroll
-          for (int g = 0; g < NGV; ++g) {
-            float mv = 0.f;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {   // keys 2 lane, 2 lane + 1
-              const int k = 2 * lane + e;
-              if (key0 + k >= j0 && key0 + k < j1)
-                mv = fmaxf(mv, __half2float(__ushort_as_half(vs[k * NG + g])));
-            }
-            mv = warp_max(mv);
-            if (lane == 0) s_vmax[g] = mv;
-          }
-        }
-      }
-    }
-    ptx::fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (page < 0) continue;   // flagged by the lookup; every thread skips alike
-    tc_fence_after();
 
-    // ---- S_g = Q_g K_g^T into columns [64g, 64g + 64).  Warp 0 runs this
-    // (descriptors warp-uniform); one elected lane issues.
-    if (warp == 0) {
+    // ---- S_g = Q_g K_g^T into columns [64g, 64g + 64): issued now (the S
+    // columns were freed with the P.V batch), so that it runs while the other
+    // warps convert the V side.  Warp 0 (descriptors warp-uniform); one elected
+    // lane issues.
+    if (page >= 0 && warp == 0) {
       const uint64_t da0 = sdesc(ptx::smem_u32(smem + LY::Q_OFF), 16, 1024);
       const uint64_t db0 = sdesc(ptx::smem_u32(KI8 ? smem + LY::KH_OFF : sb + SP::K_OFF), 16, 1024);
       if (ptx::elect_one()) {
@@ -342,6 +379,24 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
       }
       __syncwarp();
     }
+    if (page >= 0) {
+      if constexpr (VI8) convert_side_from<D, 32>(sb + SP::V_OFF, smem + LY::VH_OFF);
+      if constexpr (!VI8) if (edge) zero_rows<D>(sb + SP::V_OFF, key0, j0, j1);
+    }
+    ptx::fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    // The stage of page i - 1 (its last reader, the previous P.V batch, is done)
+    // takes page ri, whose id was loaded at the top of the iteration and is
+    // checked here as lookup_page checks it.  (Issued from the score-issuing
+    // thread under the score MMAs instead, it delayed their completion.)
+    if (refill) {
+      if (!ri_in_row) flag_error(p.err, INT8KV_DEVERR_LENGTH);
+      issue_id(ri, ri_in_row ? check_page(raw_next, p) : -1);
+    }
+    if (page < 0) continue;   // flagged by the lookup; every thread skips alike
+    tc_fence_after();
+
     // V range per group: 2^e_g bounds every V scale of the group seen so far
     // (the same for every row: block-uniform branches).  O is stable here (the
     // last P.V batch is done; the S batch in flight writes other columns).
@@ -366,7 +421,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
     }
     // the V-scale table takes the range shift: P' = p * table[key][g]
     if constexpr (VI8)
-      if (tid < kPage * NG) reinterpret_cast<float*>(smem + LY::VSF_OFF)[tid] *= sh[tid % NG];
+      if (tid < kPage * NG) reinterpret_cast<float*>(smem + LY::VSF_OFF)[tid] *= sh[tid / kPage];
     const bool okS = ptx::mbar_wait(mS, nS & 1, kMaxPolls);
     ++nS;
     tc_fence_after();
@@ -447,20 +502,29 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
       for (int cc = 0; cc < kChunks; ++cc) {
         const int c = kChunks * half + cc;
         uint32_t v[16];
+        float wt[16];   // table: V scale times the group's range shift
+        if constexpr (VI8) {
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 x = *reinterpret_cast<const float4*>(vsf + g * kPage + c * 16 + 4 * k4);
+            wt[4 * k4] = x.x;
+            wt[4 * k4 + 1] = x.y;
+            wt[4 * k4 + 2] = x.z;
+            wt[4 * k4 + 3] = x.w;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) wt[k] = sh[g];
+        }
 #pragma unroll
         for (int k2 = 0; k2 < 8; ++k2) {
-          float w0, w1;
-          if constexpr (VI8) {   // table: V scale times the group's range shift
-            w0 = sv[cc][2 * k2] * vsf[(c * 16 + 2 * k2) * NG + g];
-            w1 = sv[cc][2 * k2 + 1] * vsf[(c * 16 + 2 * k2 + 1) * NG + g];
-          } else {
-            w0 = sv[cc][2 * k2] * sh[g];
-            w1 = sv[cc][2 * k2 + 1] * sh[g];
-          }
-          const uint32_t h = ptx::pack_f16x2(w0, w1);
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-          v[k2] = h;
-          v[8 + k2] = ptx::pack_f16x2(w0 - f.x, w1 - f.y);
+          const float w0 = sv[cc][2 * k2] * wt[2 * k2], w1 = sv[cc][2 * k2 + 1] * wt[2 * k2 + 1];
+          // hi: w with its 13 low mantissa bits cleared (exact in fp16 for every
+          // normal fp16 magnitude); lo: the exact remainder, rounded to fp16
+          const float h0 = __uint_as_float(__float_as_uint(w0) & 0xFFFFE000u);
+          const float h1 = __uint_as_float(__float_as_uint(w1) & 0xFFFFE000u);
+          v[k2] = ptx::pack_f16x2(h0, h1);
+          v[8 + k2] = ptx::pack_f16x2(w0 - h0, w1 - h1);
         }
         tmem_st16(tbase + lane_off + g * 64 + c * 16, v);
       }
