@@ -773,7 +773,8 @@ def run_extra(args):
     return out
 
 
-PROFILE_CASES = ("decode8k", "decode128k", "append256", "batched16", "prefill", "k8v4_8k")
+PROFILE_CASES = ("decode8k", "decode128k", "append256", "batched16", "prefill", "k8v4_8k",
+                 "q4_0_8k", "simt_k8v4_8k")
 
 
 def run_profile_case(name, reps=5):
@@ -785,14 +786,18 @@ def run_profile_case(name, reps=5):
       batched16   attn_decode_int8 over 16 of the 64-sequence batch's sequences
                   (head_dim 128, the same lengths; 1.1 GB instead of 4.5 GB)
       prefill     append + attn_prefill_chunk_int8 of the 256-query chunk
-      k8v4_8k     attn_decode_int8 on the 8K workload in a k8v4 pool"""
+      k8v4_8k     attn_decode_int8 on the 8K workload in a k8v4 pool
+      q4_0_8k     the same in a q4_0 pool
+      simt_k8v4_8k  the k8v4 case on the CUDA-core decode kernel"""
     import torch
 
     from int8_kv_cache_02_gb300 import binding, inputs
-    if name in ("decode8k", "k8v4_8k"):
+    if name in ("decode8k", "k8v4_8k", "q4_0_8k", "simt_k8v4_8k"):
         w = inputs.grouped8k()
-        variant = binding.K8V8 if name == "decode8k" else binding.K8V4
+        variant = {"decode8k": binding.K8V8, "q4_0_8k": binding.Q4_0}.get(name, binding.K8V4)
         st = DecodeState(w, CTX, variant, 3, append_token=name == "decode8k")
+        if name == "simt_k8v4_8k":
+            st.pool.set_decode_kernel(binding.DECODE_SIMT)
         for i in range(reps):
             st.step(i % 3, append=name == "decode8k")
     elif name == "decode128k":

@@ -548,8 +548,13 @@ cudaError_t launch_decode(const int8kv_pool* pool, int layer, const DecodeArgs& 
   }
   cudaError_t e;
   if (kind == INT8KV_DECODE_WARP_MMA) {
-    query_residency(pool, kind);
-    a.pf_blocks = pool->resident[kind];   // the first wave prefetches its first pages
+    // the first wave prefetches its first pages; the residency query runs once
+    // per pool, outside stream capture (inside, three blocks per SM are assumed)
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (pool->resident[kind] == 0 && cudaStreamIsCapturing(stream, &cs) == cudaSuccess &&
+        cs == cudaStreamCaptureStatusNone)
+      query_residency(pool, kind);
+    a.pf_blocks = pool->resident[kind] ? pool->resident[kind] : 3 * pool->num_sms;
     e = launch_decode_mma(a, k8, v8, pool->tmap_k, pool->tmap_v, layer * pool->n_pages, stream);
     // up to 8 splits are combined inside the kernel (one cluster)
     if (e != cudaSuccess || a.n_splits <= 8) return e;

@@ -318,15 +318,14 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
     // 2t + 9) their high nibbles (4t + 1, 4t + 3); the rotated query fragments
     // follow the same order, as fp16 hi + lo pairs (two MMAs per k-step).
     const int sa_ = rowA, sb_ = rowB & 7;
-    const unsigned char* kA = sb + LY::K_OFF + trA * 128;
-    const unsigned char* kB = sb + LY::K_OFF + trB * 128;
-    const uint4 ca[2] = {*reinterpret_cast<const uint4*>(kA + ((t ^ sa_) << 4)),
-                         *reinterpret_cast<const uint4*>(kA + (((t + 4) ^ sa_) << 4))};
-    const uint4 cb[2] = {*reinterpret_cast<const uint4*>(kB + ((t ^ sb_) << 4)),
-                         *reinterpret_cast<const uint4*>(kB + (((t + 4) ^ sb_) << 4))};
-    const uint4 dsa = *reinterpret_cast<const uint4*>(sb + LY::KS_OFF + trA * 16);
-    const uint4 dsb = *reinterpret_cast<const uint4*>(sb + LY::KS_OFF + trB * 16);
-    const uint32_t dA[4] = {dsa.x, dsa.y, dsa.z, dsa.w}, dB[4] = {dsb.x, dsb.y, dsb.z, dsb.w};
+    // word w of chunk (t + 4h) of each row, loaded where it is used (four words
+    // a chunk; holding the chunks whole would cost 16 registers)
+    const uint32_t* kA0 = reinterpret_cast<const uint32_t*>(sb + LY::K_OFF + trA * 128 + ((t ^ sa_) << 4));
+    const uint32_t* kA1 = reinterpret_cast<const uint32_t*>(sb + LY::K_OFF + trA * 128 + (((t + 4) ^ sa_) << 4));
+    const uint32_t* kB0 = reinterpret_cast<const uint32_t*>(sb + LY::K_OFF + trB * 128 + ((t ^ sb_) << 4));
+    const uint32_t* kB1 = reinterpret_cast<const uint32_t*>(sb + LY::K_OFF + trB * 128 + (((t + 4) ^ sb_) << 4));
+    const uint32_t* dA = reinterpret_cast<const uint32_t*>(sb + LY::KS_OFF + trA * 16);
+    const uint32_t* dB = reinterpret_cast<const uint32_t*>(sb + LY::KS_OFF + trB * 16);
     const uint4* qv = qfrag + r * 4 + t;
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
@@ -334,8 +333,7 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int wi = g >> 1;
-        const uint32_t wa = wi == 0 ? ca[h].x : wi == 1 ? ca[h].y : wi == 2 ? ca[h].z : ca[h].w;
-        const uint32_t wb = wi == 0 ? cb[h].x : wi == 1 ? cb[h].y : wi == 2 ? cb[h].z : cb[h].w;
+        const uint32_t wa = (h ? kA1 : kA0)[wi], wb = (h ? kB1 : kB0)[wi];
         const uint32_t sel = (g & 1) ? 0x4342u : 0x4140u;   // bytes 2g, 2g + 1 -> bytes 0, 2
         const uint32_t xa = ptx::prmt(wa, 0u, sel), xb = ptx::prmt(wb, 0u, sel);
         uint32_t af[4];

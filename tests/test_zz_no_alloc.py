@@ -126,3 +126,40 @@ def test_noalloc_auto_split_fits_the_scratch():
     torch.cuda.synchronize()
     gu.assert_attention_close(out.cpu().numpy(), ref.cpu().numpy().astype(np.float64), "auto fit")
     assert binding.kv_pool_read_device_error(dev) == 0
+
+
+def test_noalloc_in_a_captured_graph_as_lengths_grow():
+    """After a warm call, a noalloc decode recorded into a CUDA graph replays with
+    the lengths read on the device: each replay, after the host advances the
+    lengths, matches the oracle's decode at those lengths."""
+    from int8_kv_cache_02_gb300 import binding
+    from oracle import attention as oatt
+    gu.lib_ready()
+    L = binding.lib()
+    lens0 = [1200, 300]
+    q, ks, vs = inputs.random_case(904, 2, 16, 2, 256, [x + 8 for x in lens0], outliers=True)
+    pt, n_pages = inputs.page_table([x + 8 for x in lens0], 64, seed=5)
+    dev, orc = gu.make_pools(1, 2, 256, 64, 64, n_pages, 0)
+    for b in range(2):
+        gu.fill_sequence(dev, orc, 0, ks[b], vs[b], pt[b])
+    qd, ptd = q.cuda(), pt.cuda()
+    lens = torch.tensor(lens0, dtype=torch.int32, device="cuda")
+    out = torch.zeros((2, 16, 256), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        assert _raw_noalloc(L, dev, qd, lens, ptd, out, 8) == 0   # warm: the scratch address
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        assert _raw_noalloc(L, dev, qd, lens, ptd, out, 8) == 0
+    for step in range(4):
+        now = [x + 2 * step for x in lens0]
+        lens.copy_(torch.tensor(now, dtype=torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = np.stack([oatt.decode(q[b].numpy(), *orc.gather(0, pt[b].numpy(), n), n)
+                        for b, n in enumerate(now)])
+        gu.assert_attention_close(out.cpu().numpy(), ref, f"replay {step}")
+    assert binding.kv_pool_read_device_error(dev) == 0
