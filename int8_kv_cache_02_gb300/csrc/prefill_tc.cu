@@ -193,6 +193,34 @@ __device__ __forceinline__ void convert_side_from(const unsigned char* src, unsi
   }
 }
 
+// The copies of one page as mma::issue_page makes them (K boxes, V boxes, then
+// the K and V scales rows of an int8 side), for one copy at a time: copy c of
+// kCopies, and the bytes the stage's barrier expects for all of them.
+template <int D, bool KI8, bool VI8>
+struct PageCopies {
+  using SP = mma::StagedPage<D, KI8, VI8>;
+  static constexpr int kCopies = SP::KBOXES + SP::VBOXES + (KI8 ? 1 : 0) + (VI8 ? 1 : 0);
+  static __device__ __forceinline__ uint32_t tx(int ng) {
+    return SP::KBYTES + SP::VBYTES + (KI8 ? kPage * ng * 2 : 0) + (VI8 ? kPage * ng * 2 : 0);
+  }
+  static __device__ __forceinline__ void issue(int c, unsigned char* stage, uint64_t* full_bar,
+                                               int page, int row, const PoolView& p, int kvh,
+                                               const CUtensorMap* tmk, const CUtensorMap* tmv) {
+    constexpr int KX = KI8 ? 128 : 64, VX = VI8 ? 128 : 64;   // box width in elements
+    const size_t srow = ((size_t)page * p.Hkv + kvh) * kPage * p.ng;
+    if (c < SP::KBOXES) {
+      ptx::tma_load_2d(stage + SP::K_OFF + c * kBoxBytes, tmk, c * KX, row, full_bar);
+    } else if (c < SP::KBOXES + SP::VBOXES) {
+      const int bx = c - SP::KBOXES;
+      ptx::tma_load_2d(stage + SP::V_OFF + bx * kBoxBytes, tmv, bx * VX, row, full_bar);
+    } else if (KI8 && c == SP::KBOXES + SP::VBOXES) {
+      ptx::bulk_load(stage + SP::KS_OFF, p.ks + srow, kPage * p.ng * 2, full_bar);
+    } else if (VI8) {
+      ptx::bulk_load(stage + SP::VS_OFF, p.vs + srow, kPage * p.ng * 2, full_bar);
+    }
+  }
+};
+
 // Zero the fp16 rows of a staged side whose keys fall outside [j0, j1) (they
 // may hold any bits, and 0 * NaN would reach O).
 template <int D>
@@ -383,16 +411,33 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
       if constexpr (VI8) convert_side_from<D, 32>(sb + SP::V_OFF, smem + LY::VH_OFF);
       if constexpr (!VI8) if (edge) zero_rows<D>(sb + SP::V_OFF, key0, j0, j1);
     }
+    // The stage of page i - 1 (its last reader, the previous P.V batch, is done)
+    // takes page ri, whose id was loaded at the top of the iteration and is
+    // checked here as lookup_page checks it: thread 32 arms the stage's barrier
+    // now, and after the barrier below one lane in each of the next warps issues
+    // one of the page's copies (one thread issuing all of them held its warp for
+    // ~700 clocks, and the block with it).
+    const int rst = ri % kNS;
+    if (refill) {
+      if (!ri_in_row) flag_error(p.err, INT8KV_DEVERR_LENGTH);
+      const int pg = ri_in_row ? check_page(raw_next, p) : -1;
+      stage_page[rst] = pg;
+      if (pg < 0)
+        ptx::mbar_arrive(&full[rst]);
+      else
+        ptx::mbar_arrive_expect_tx(&full[rst], PageCopies<D, KI8, VI8>::tx(p.ng));
+    }
     ptx::fence_proxy_async();
     tc_fence_before();
     __syncthreads();
-    // The stage of page i - 1 (its last reader, the previous P.V batch, is done)
-    // takes page ri, whose id was loaded at the top of the iteration and is
-    // checked here as lookup_page checks it.  (Issued from the score-issuing
-    // thread under the score MMAs instead, it delayed their completion.)
-    if (refill) {
-      if (!ri_in_row) flag_error(p.err, INT8KV_DEVERR_LENGTH);
-      issue_id(ri, ri_in_row ? check_page(raw_next, p) : -1);
+    {
+      const int c = warp - 1;
+      if (i > 0 && ri < n_pg && (tid & 31) == 0 && c >= 0 && c < PageCopies<D, KI8, VI8>::kCopies) {
+        const int pg = stage_page[rst];
+        if (pg >= 0)
+          PageCopies<D, KI8, VI8>::issue(c, smem + LY::ST_OFF + rst * SP::STAGE, &full[rst], pg,
+                                         page_row(pg), p, kvh, &tmk, &tmv);
+      }
     }
     if (page < 0) continue;   // flagged by the lookup; every thread skips alike
     tc_fence_after();
