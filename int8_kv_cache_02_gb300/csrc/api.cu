@@ -81,16 +81,32 @@ EncodeTiled encode_tiled_fn() {
 
 // 2-D view [rows][head_dim] of a whole store (all layers), 64-row x 128-byte
 // boxes with the 128-byte swizzle.
+// A store as rows of head_dim elements, copied in boxes of 64 rows x 128 bytes
+// (128-byte swizzle).  Rows of one box: a 2-D map [rows][128 B].  Rows of
+// several boxes: a 3-D map (x in the box, row, box) with strides (row bytes,
+// 128 B), so that one copy of the box {128 B, 64 rows, all boxes} brings a
+// page's rows as consecutive 64-row boxes.
 bool make_store_map(CUtensorMap* map, void* base, bool is_int8, int head_dim, size_t rows) {
   EncodeTiled enc = encode_tiled_fn();
   if (!enc) return false;
   const size_t esz = is_int8 ? 1 : 2;
-  cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(head_dim * esz)};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / esz), 64};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(map, is_int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
-             base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  const size_t row_bytes = (size_t)head_dim * esz;
+  const cuuint32_t nbox = (cuuint32_t)(row_bytes / 128);
+  const CUtensorMapDataType ty = is_int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  if (nbox <= 1) {
+    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / esz), 64};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, ty, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)(128 / esz), (cuuint64_t)rows, (cuuint64_t)nbox};
+  cuuint64_t strides[2] = {(cuuint64_t)row_bytes, 128};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / esz), 64, nbox};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, ty, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -80,30 +80,33 @@ __device__ __forceinline__ void issue_page(unsigned char* stage, uint64_t* full_
   const uint32_t tx = SP::KBYTES + SP::VBYTES + (KI8 ? kPage * ng * 2 : KSB) +
                       (VI8 ? kPage * ng * 2 : VSB);
   ptx::mbar_arrive_expect_tx(full_bar, tx);
-  constexpr int KX = (KI8 || KQ4) ? 128 : 64;   // box width in elements
-  constexpr int VX = (VI8 || VQ4) ? 128 : 64;
   const size_t srow = ((size_t)page * p.Hkv + kvh) * kPage * ng;
   const size_t vsrow = ((size_t)page * p.Hkv + kvh) * kPage * (VQ4 ? D / 32 : ng);
   const size_t q4row = ((size_t)page * p.Hkv + kvh) * kPage * (D / 32);   // 4-bit K scales
+  // a side of several 128-byte boxes a row comes in one 3-D copy (the map is 3-D)
   if constexpr (kStream) {
     const uint64_t pol = ptx::policy_evict_first();
-#pragma unroll
-    for (int bx = 0; bx < SP::KBOXES; ++bx)
-      ptx::tma_load_2d_hint(stage + SP::K_OFF + bx * kBoxBytes, tmk, bx * KX, row, full_bar, pol);
-#pragma unroll
-    for (int bx = 0; bx < SP::VBOXES; ++bx)
-      ptx::tma_load_2d_hint(stage + SP::V_OFF + bx * kBoxBytes, tmv, bx * VX, row, full_bar, pol);
+    if constexpr (SP::KBOXES > 1)
+      ptx::tma_load_3d_hint(stage + SP::K_OFF, tmk, 0, row, 0, full_bar, pol);
+    else
+      ptx::tma_load_2d_hint(stage + SP::K_OFF, tmk, 0, row, full_bar, pol);
+    if constexpr (SP::VBOXES > 1)
+      ptx::tma_load_3d_hint(stage + SP::V_OFF, tmv, 0, row, 0, full_bar, pol);
+    else
+      ptx::tma_load_2d_hint(stage + SP::V_OFF, tmv, 0, row, full_bar, pol);
     if (KI8) ptx::bulk_load_hint(stage + SP::KS_OFF, p.ks + srow, kPage * ng * 2, full_bar, pol);
     if (KQ4) ptx::bulk_load_hint(stage + SP::KS_OFF, p.ks + q4row, KSB, full_bar, pol);
     if (VI8) ptx::bulk_load_hint(stage + SP::VS_OFF, p.vs + srow, kPage * ng * 2, full_bar, pol);
     if (VQ4) ptx::bulk_load_hint(stage + SP::VS_OFF, p.vs + vsrow, VSB, full_bar, pol);
   } else {
-#pragma unroll
-    for (int bx = 0; bx < SP::KBOXES; ++bx)
-      ptx::tma_load_2d(stage + SP::K_OFF + bx * kBoxBytes, tmk, bx * KX, row, full_bar);
-#pragma unroll
-    for (int bx = 0; bx < SP::VBOXES; ++bx)
-      ptx::tma_load_2d(stage + SP::V_OFF + bx * kBoxBytes, tmv, bx * VX, row, full_bar);
+    if constexpr (SP::KBOXES > 1)
+      ptx::tma_load_3d(stage + SP::K_OFF, tmk, 0, row, 0, full_bar);
+    else
+      ptx::tma_load_2d(stage + SP::K_OFF, tmk, 0, row, full_bar);
+    if constexpr (SP::VBOXES > 1)
+      ptx::tma_load_3d(stage + SP::V_OFF, tmv, 0, row, 0, full_bar);
+    else
+      ptx::tma_load_2d(stage + SP::V_OFF, tmv, 0, row, full_bar);
     if (KI8) ptx::bulk_load(stage + SP::KS_OFF, p.ks + srow, kPage * ng * 2, full_bar);
     if (KQ4) ptx::bulk_load(stage + SP::KS_OFF, p.ks + q4row, KSB, full_bar);
     if (VI8) ptx::bulk_load(stage + SP::VS_OFF, p.vs + srow, kPage * ng * 2, full_bar);

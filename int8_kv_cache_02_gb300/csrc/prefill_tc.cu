@@ -193,27 +193,31 @@ __device__ __forceinline__ void convert_side_from(const unsigned char* src, unsi
   }
 }
 
-// The copies of one page as mma::issue_page makes them (K boxes, V boxes, then
-// the K and V scales rows of an int8 side), for one copy at a time: copy c of
-// kCopies, and the bytes the stage's barrier expects for all of them.
+// The copies of one page as mma::issue_page makes them (the K side, the V side,
+// then the K and V scales rows of an int8 side), for one copy at a time: copy c
+// of kCopies, and the bytes the stage's barrier expects for all of them.
 template <int D, bool KI8, bool VI8>
 struct PageCopies {
   using SP = mma::StagedPage<D, KI8, VI8>;
-  static constexpr int kCopies = SP::KBOXES + SP::VBOXES + (KI8 ? 1 : 0) + (VI8 ? 1 : 0);
+  static constexpr int kCopies = 2 + (KI8 ? 1 : 0) + (VI8 ? 1 : 0);   // K, V (3-D when several boxes), scales
   static __device__ __forceinline__ uint32_t tx(int ng) {
     return SP::KBYTES + SP::VBYTES + (KI8 ? kPage * ng * 2 : 0) + (VI8 ? kPage * ng * 2 : 0);
   }
   static __device__ __forceinline__ void issue(int c, unsigned char* stage, uint64_t* full_bar,
                                                int page, int row, const PoolView& p, int kvh,
                                                const CUtensorMap* tmk, const CUtensorMap* tmv) {
-    constexpr int KX = KI8 ? 128 : 64, VX = VI8 ? 128 : 64;   // box width in elements
     const size_t srow = ((size_t)page * p.Hkv + kvh) * kPage * p.ng;
-    if (c < SP::KBOXES) {
-      ptx::tma_load_2d(stage + SP::K_OFF + c * kBoxBytes, tmk, c * KX, row, full_bar);
-    } else if (c < SP::KBOXES + SP::VBOXES) {
-      const int bx = c - SP::KBOXES;
-      ptx::tma_load_2d(stage + SP::V_OFF + bx * kBoxBytes, tmv, bx * VX, row, full_bar);
-    } else if (KI8 && c == SP::KBOXES + SP::VBOXES) {
+    if (c == 0) {
+      if constexpr (SP::KBOXES > 1)
+        ptx::tma_load_3d(stage + SP::K_OFF, tmk, 0, row, 0, full_bar);
+      else
+        ptx::tma_load_2d(stage + SP::K_OFF, tmk, 0, row, full_bar);
+    } else if (c == 1) {
+      if constexpr (SP::VBOXES > 1)
+        ptx::tma_load_3d(stage + SP::V_OFF, tmv, 0, row, 0, full_bar);
+      else
+        ptx::tma_load_2d(stage + SP::V_OFF, tmv, 0, row, full_bar);
+    } else if (KI8 && c == 2) {
       ptx::bulk_load(stage + SP::KS_OFF, p.ks + srow, kPage * p.ng * 2, full_bar);
     } else if (VI8) {
       ptx::bulk_load(stage + SP::VS_OFF, p.vs + srow, kPage * p.ng * 2, full_bar);
