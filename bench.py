@@ -774,7 +774,7 @@ def run_extra(args):
 
 
 PROFILE_CASES = ("decode8k", "decode128k", "append256", "batched16", "prefill", "k8v4_8k",
-                 "q4_0_8k", "simt_k8v4_8k")
+                 "q4_0_8k", "simt_k8v4_8k", "tiny512", "window8k")
 
 
 def run_profile_case(name, reps=5):
@@ -788,7 +788,9 @@ def run_profile_case(name, reps=5):
       prefill     append + attn_prefill_chunk_int8 of the 256-query chunk
       k8v4_8k     attn_decode_int8 on the 8K workload in a k8v4 pool
       q4_0_8k     the same in a q4_0 pool
-      simt_k8v4_8k  the k8v4 case on the CUDA-core decode kernel"""
+      simt_k8v4_8k  the k8v4 case on the CUDA-core decode kernel
+      tiny512     attn_decode_int8 on the 512-position workload (head_dim 128), 4 splits
+      window8k    attn_decode_multi_int8 on the 8K workload, windows of 4 queries"""
     import torch
 
     from int8_kv_cache_02_gb300 import binding, inputs
@@ -836,6 +838,28 @@ def run_profile_case(name, reps=5):
             binding.attn_decode_int8(pool, 0, q, lens_d, ptd, out, ws, n_splits=ns)
     elif name == "prefill":
         run_prefill(n_iter=reps)
+    elif name == "tiny512":
+        w = inputs.tiny()
+        pt, n_pages = inputs.page_table([512], PS, seed=0)
+        pool = binding.KVPool(1, 2, 128, 128, PS, n_pages, binding.K8V8)
+        binding.kv_quant_append(pool, 0, w["k"].reshape(1, 512, 2, 128).cuda(),
+                                w["v"].reshape(1, 512, 2, 128).cuda(),
+                                torch.zeros(1, dtype=torch.int32, device="cuda"), pt.cuda())
+        out = torch.empty((1, 8, 128), dtype=torch.float32, device="cuda")
+        ws = pool.decode_workspace(1, 8, 4)
+        lens = torch.tensor([512], dtype=torch.int32, device="cuda")
+        for _ in range(reps):
+            binding.attn_decode_int8(pool, 0, w["q"].cuda(), lens, pt.cuda(), out, ws, n_splits=4)
+    elif name == "window8k":
+        st = DecodeState(inputs.grouped8k(), CTX, binding.K8V8, 3, append_token=False)
+        g = torch.Generator().manual_seed(70)
+        qw = inputs.normal_f16((1, 4, st.h, D), g).cuda()
+        outw = torch.empty((1, 4, st.h, D), dtype=torch.float32, device="cuda")
+        ns = binding.attn_decode_n_splits(st.pool, 4, CTX)
+        ws = st.pool.decode_workspace(4, st.h, ns)
+        for i in range(reps):
+            binding.attn_decode_multi_int8(st.pool, 0, qw, st.lens, st.pt[i % 3:i % 3 + 1], outw, ws,
+                                           n_splits=ns)
     else:
         raise SystemExit(f"unknown profile case {name}; one of {', '.join(PROFILE_CASES)}")
     torch.cuda.synchronize()
