@@ -60,7 +60,7 @@ def _random_pool(variant, L_list, ps, n_pages, seed, n_layers=2, Hkv=2, D=64, gs
     return P, pt
 
 
-@pytest.mark.parametrize("variant", [opool.K8V8, opool.K8V16, opool.K16V8])
+@pytest.mark.parametrize("variant", [opool.K8V8, opool.K8V16, opool.K16V8, opool.K8V4, opool.Q4_0])
 def test_round_trip_into_another_paging(variant):
     """Saved from pages of 16 positions, loaded into pages of 64 through another
     permutation: every layer of every sequence reads back the same codes, scales
