@@ -364,6 +364,38 @@ def run_oracle(budget_s, max_steps, n_pos, warmup):
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def host_info():
+    """The host the oracle runs on: its CPU model (from /proc/cpuinfo, else the
+    platform's name for it) and the cores this process may run on."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:   # Arm hosts name the core in lscpu, not in /proc/cpuinfo
+        import subprocess
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name:"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    try:
+        avail = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        avail = os.cpu_count()
+    return {"cpu": model or platform.processor() or platform.machine(), "machine": platform.machine(),
+            "cores_available": avail, "cores_used_by_the_oracle": 1}
+
+
 def oracle_sample_bytes(n_pos):
     """Bytes of the sampled step: append + decode of all heads over the last n_pos positions."""
     return step_bytes(ctx=n_pos)
@@ -482,7 +514,8 @@ def run_ours(args, rank, world, local):
                "cores": 1, "kind": "oracle",
                "sample": f"{r['steps']} full decode steps of the same workload (append + fp64 "
                          f"decode over 8192 positions, all 16 heads), single thread, "
-                         f"{r['seconds']:.1f} s"}
+                         f"{r['seconds']:.1f} s",
+               "host": host_info()}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -887,7 +920,7 @@ def run_reference(args, rank, world, local):
         "config": {"workload": WORKLOAD, "batch": B, "n_heads": H, "n_kv_heads": HKV,
                    "head_dim": D, "group_size": GS, "ctx": CTX, "sampled_positions": n_pos},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host": host_info()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
