@@ -21,10 +21,11 @@
 // are applied per (token, 64-value group) in f32 after each 64-wide partial
 // dot.  On the P.V side the weight of token j for output dims of V group g is
 // P'_jg = p_j * s_v(j, g) (exp-weights times the V scale); it is fed to the
-// tensor core as an fp16 hi + lo pair (two MMAs), which keeps ~22 bits.  To keep
+// tensor core as an fp16 hi + lo pair (two MMAs), which keeps ~21 bits.  To keep
 // P' away from fp16's subnormal range whatever the magnitude of V, each warp
-// tracks a power of two 2^e_g >= every V scale of group g it has seen and
-// feeds P' * 2^(14 - e_g) < 2^14; when e_g grows, the group's accumulators
+// tracks a power of two 2^e_g > every V scale of group g it has seen and
+// feeds p_j * s_v(j, g) * 2^(6 - e_g) < 2^8 * 2^6 = 2^14 (the lazy max bounds p by
+// 2^8); when e_g grows, the group's accumulators
 // are rescaled by the exact power-of-two ratio (the same move the online
 // softmax makes with its running max).
 //
@@ -570,14 +571,14 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       qv[j] = *reinterpret_cast<const uint4*>(sb + LY::V_OFF + tk[j] * 128 + ((r ^ (tk[j] & 7)) << 4));
+    uint32_t pha, pla, phb, plb;   // p of tokens A and B (heads 2t, 2t + 1), fp16 hi + lo
+    mma::split_pair(pr[0], pr[1], pha, pla);
+    mma::split_pair(pr[2], pr[3], phb, plb);
 #pragma unroll
     for (int g = 0; g < NGV; ++g) {
-      const float p0 = pr[0] * wa[g], p1 = pr[1] * wa[g], p2 = pr[2] * wb[g], p3 = pr[3] * wb[g];
-      const uint32_t h01 = ptx::pack_f16x2(p0, p1), h23 = ptx::pack_f16x2(p2, p3);
-      const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-      const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-      const uint32_t e01 = ptx::pack_f16x2(p0 - f01.x, p1 - f01.y);
-      const uint32_t e23 = ptx::pack_f16x2(p2 - f23.x, p3 - f23.y);
+      uint32_t h01, e01, h23, e23;
+      mma::weight_pair(pha, pla, ptx::pack_f16x2(wa[g], wa[g]), h01, e01);
+      mma::weight_pair(phb, plb, ptx::pack_f16x2(wb[g], wb[g]), h23, e23);
       const uint32_t bh0 = ptx::movmatrix_trans(h01), bh1 = ptx::movmatrix_trans(h23);
       const uint32_t bl0 = ptx::movmatrix_trans(e01), bl1 = ptx::movmatrix_trans(e23);
       const int wi = g >> 1;   // the word of the chunk that holds block g's bytes
@@ -603,15 +604,17 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
     return;
   }
 
-  // ---- P.V per V group: P' as an f16 hi + lo pair, transposed into the B fragment
+  // ---- P.V per V group: P' = p * w as an f16 hi + lo pair (p split once, the
+  // group's factor w -- exact in fp16: an fp16 scale times a power of two, below
+  // 2^6 -- applied in half precision), transposed into the B fragment
+  uint32_t pha, pla, phb, plb;   // p of tokens A and B (heads 2t, 2t + 1), fp16 hi + lo
+  mma::split_pair(pr[0], pr[1], pha, pla);
+  mma::split_pair(pr[2], pr[3], phb, plb);
 #pragma unroll
   for (int g = 0; g < NGV; ++g) {
-    const float p0 = pr[0] * wa[g], p1 = pr[1] * wa[g], p2 = pr[2] * wb[g], p3 = pr[3] * wb[g];
-    const uint32_t h01 = ptx::pack_f16x2(p0, p1), h23 = ptx::pack_f16x2(p2, p3);
-    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-    const uint32_t e01 = ptx::pack_f16x2(p0 - f01.x, p1 - f01.y);
-    const uint32_t e23 = ptx::pack_f16x2(p2 - f23.x, p3 - f23.y);
+    uint32_t h01, e01, h23, e23;
+    mma::weight_pair(pha, pla, ptx::pack_f16x2(wa[g], wa[g]), h01, e01);
+    mma::weight_pair(phb, plb, ptx::pack_f16x2(wb[g], wb[g]), h23, e23);
     const uint32_t bh0 = ptx::movmatrix_trans(h01), bh1 = ptx::movmatrix_trans(h23);
     const uint32_t bl0 = ptx::movmatrix_trans(e01), bl1 = ptx::movmatrix_trans(e23);
 #pragma unroll

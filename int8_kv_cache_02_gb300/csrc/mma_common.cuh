@@ -60,6 +60,32 @@ __device__ __forceinline__ int exponent_of(float x) {   // floor(log2 x), x > 0 
   return (int)((__float_as_uint(x) >> 23) & 0xFF) - 127;
 }
 
+// Softmax weights p0, p1 >= 0 (at most 2^8) as fp16 hi + lo pairs: hi keeps each
+// weight's 11 leading bits (its 13 low mantissa bits cleared: exact in fp16 from
+// 2^-14 up), lo the remainder rounded to fp16.
+__device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
+  const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
+  hi = ptx::pack_f16x2(h0, h1);
+  lo = ptx::pack_f16x2(p0 - h0, p1 - h1);
+}
+
+// The P.V weights P' = p * s of two keys (p as the hi + lo pairs of split_pair, s
+// an fp16 factor per key) as a new fp16 hi + lo pair, in half-precision
+// arithmetic: hi = fl(ph s); ph s - hi, an 11-bit by 11-bit product less its
+// rounding to 11 bits, is exact in fp16 outside the subnormal range, so
+// lo = fl(pl s + (ph s - hi)) leaves P' within ~2^-21 of p * s.
+__device__ __forceinline__ void weight_pair(uint32_t ph, uint32_t pl, uint32_t s, uint32_t& hi,
+                                            uint32_t& lo) {
+  const __half2 a = *reinterpret_cast<const __half2*>(&ph);
+  const __half2 b = *reinterpret_cast<const __half2*>(&pl);
+  const __half2 f = *reinterpret_cast<const __half2*>(&s);
+  const __half2 h = __hmul2_rn(a, f);
+  const __half2 l = __hfma2(b, f, __hfma2(a, f, __hneg2(h)));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 // Issue the copies of one page (or, for a page id flagged invalid, complete the
 // stage's barrier with no bytes) into stage `st`.  kStream: the page is read
 // once (decode), so its L2 lines go first; otherwise (prefill: every query tile

@@ -72,7 +72,7 @@ struct TLayout {
   static constexpr int KH_OFF = ST_OFF + kNS * SP::STAGE;   // converted K page (int8 K only)
   static constexpr int VH_OFF = KH_OFF + (KI8 ? kPage * D * 2 : 0);   // converted V page
   static constexpr int KSF_OFF = VH_OFF + (VI8 ? kPage * D * 2 : 0);   // fp32 K scales x scale [key][NG]
-  static constexpr int VSF_OFF = KSF_OFF + kPage * 4 * 4;               // fp32 V scales [NG][key]
+  static constexpr int VSF_OFF = KSF_OFF + kPage * 4 * 4;               // fp16 P.V factors [NG][key]
   static constexpr int BAR_OFF = VSF_OFF + kPage * 4 * 4;
   static constexpr int SMEM = 1024 + BAR_OFF + 128;
   // tensor memory: S_g / P'_g region, then O
@@ -357,14 +357,9 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
         if (tid < kPage * NG)
           reinterpret_cast<float*>(smem + LY::KSF_OFF)[tid] =
               __half2float(reinterpret_cast<const __half*>(sb + SP::KS_OFF)[tid]) * a.scale_log2;
-      // The V scales are staged too: their table (as [group][key]) and each
-      // group's largest scale among the keys in [j0, j1) (warp 1 + g takes group
-      // g) are formed here, in the wait for the previous P.V batch; both were
-      // last read before this iteration began.
+      // Each group's largest V scale among the keys in [j0, j1) (warp 1 + g takes
+      // group g) is formed here, in the wait for the previous P.V batch.
       if constexpr (VI8) {
-        if (tid < kPage * NG)
-          reinterpret_cast<float*>(smem + LY::VSF_OFF)[(tid % NG) * kPage + tid / NG] =
-              __half2float(reinterpret_cast<const __half*>(sb + SP::VS_OFF)[tid]);
         const int g = warp - 1;
         if (g >= 0 && g < NGV) {
           const uint16_t* vs = reinterpret_cast<const uint16_t*>(sb + SP::VS_OFF);
@@ -468,9 +463,16 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
         sh[g] = pow2f(kPShift);
       }
     }
-    // the V-scale table takes the range shift: P' = p * table[key][g]
+    // the table of P.V factors, fp16 [group][key]: the V scale times the group's
+    // range shift (exact: below 2^6), 0 for keys outside [j0, j1)
     if constexpr (VI8)
-      if (tid < kPage * NG) reinterpret_cast<float*>(smem + LY::VSF_OFF)[tid] *= sh[tid / kPage];
+      if (tid < kPage * NG) {
+        const int g = tid / kPage, k = tid % kPage;
+        const float f = key0 + k >= j0 && key0 + k < j1
+                            ? __half2float(reinterpret_cast<const __half*>(sb + SP::VS_OFF)[k * NG + g]) * sh[g]
+                            : 0.f;
+        reinterpret_cast<__half*>(smem + LY::VSF_OFF)[tid] = __float2half_rn(f);
+      }
     const bool okS = ptx::mbar_wait(mS, nS & 1, kMaxPolls);
     ++nS;
     tc_fence_after();
@@ -543,38 +545,33 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
         sv[cc][k] = ptx::ex2(sv[cc][k] - base);   // now p
         l += sv[cc][k];                           // this part's share of the row sum
       }
-    // P'_g hi | lo for chunk c over the S columns of chunk c (already read)
-    const float* vsf = reinterpret_cast<const float*>(smem + LY::VSF_OFF);
+    // P'_g = p * factor(key, g) as fp16 hi | lo for chunk c, over the S columns of
+    // chunk c (already read): p split once, each group's factor applied in half
+    // precision
+    uint32_t ph[kChunks][8], pl[kChunks][8];
+#pragma unroll
+    for (int cc = 0; cc < kChunks; ++cc)
+#pragma unroll
+      for (int k2 = 0; k2 < 8; ++k2)
+        mma::split_pair(sv[cc][2 * k2], sv[cc][2 * k2 + 1], ph[cc][k2], pl[cc][k2]);
+    const uint4* vsf = reinterpret_cast<const uint4*>(smem + LY::VSF_OFF);
 #pragma unroll
     for (int g = 0; g < NGV; ++g)
 #pragma unroll
       for (int cc = 0; cc < kChunks; ++cc) {
         const int c = kChunks * half + cc;
-        uint32_t v[16];
-        float wt[16];   // table: V scale times the group's range shift
+        uint32_t f[8];   // factor pairs of keys (16c + 2k2, 16c + 2k2 + 1)
         if constexpr (VI8) {
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const float4 x = *reinterpret_cast<const float4*>(vsf + g * kPage + c * 16 + 4 * k4);
-            wt[4 * k4] = x.x;
-            wt[4 * k4 + 1] = x.y;
-            wt[4 * k4 + 2] = x.z;
-            wt[4 * k4 + 3] = x.w;
-          }
+          const uint4 x0 = vsf[(g * kPage + c * 16) / 8], x1 = vsf[(g * kPage + c * 16) / 8 + 1];
+          f[0] = x0.x; f[1] = x0.y; f[2] = x0.z; f[3] = x0.w;
+          f[4] = x1.x; f[5] = x1.y; f[6] = x1.z; f[7] = x1.w;
         } else {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) wt[k] = sh[g];
+          for (int k2 = 0; k2 < 8; ++k2) f[k2] = (uint32_t)(kPShift + 15) * 0x04000400u;   // 2^kPShift
         }
+        uint32_t v[16];
 #pragma unroll
-        for (int k2 = 0; k2 < 8; ++k2) {
-          const float w0 = sv[cc][2 * k2] * wt[2 * k2], w1 = sv[cc][2 * k2 + 1] * wt[2 * k2 + 1];
-          // hi: w with its 13 low mantissa bits cleared (exact in fp16 for every
-          // normal fp16 magnitude); lo: the exact remainder, rounded to fp16
-          const float h0 = __uint_as_float(__float_as_uint(w0) & 0xFFFFE000u);
-          const float h1 = __uint_as_float(__float_as_uint(w1) & 0xFFFFE000u);
-          v[k2] = ptx::pack_f16x2(h0, h1);
-          v[8 + k2] = ptx::pack_f16x2(w0 - h0, w1 - h1);
-        }
+        for (int k2 = 0; k2 < 8; ++k2) mma::weight_pair(ph[cc][k2], pl[cc][k2], f[k2], v[k2], v[8 + k2]);
         tmem_st16(tbase + lane_off + g * 64 + c * 16, v);
       }
     tmem_wait_st();
