@@ -349,13 +349,14 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
       const uint32_t pa = dA[g >> 1], pb = dB[g >> 1];
       const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pa));
       const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
-      const float sa = ((g & 1) ? fa.y : fa.x) * scale_log2;
-      const float sbb = ((g & 1) ? fb.y : fb.x) * scale_log2;
+      const float sa = (g & 1) ? fa.y : fa.x, sbb = (g & 1) ? fb.y : fb.x;
       s[0] = fmaf(acc[0], sa, s[0]);
       s[1] = fmaf(acc[1], sa, s[1]);
       s[2] = fmaf(acc[2], sbb, s[2]);
       s[3] = fmaf(acc[3], sbb, s[3]);
     }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s[k] *= scale_log2;   // the softmax scale, once
   } else if constexpr (KI8) {
     float ka[NG], kb[NG];
     load_row_scales<NG>(sb + LY::KS_OFF, trA, ka);
@@ -381,12 +382,13 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
         ptx::mma_f16(acc, af, qf[mc * 4 + ii][0], qf[mc * 4 + ii][1]);
       }
       const int grp = mc / (MACROS / NG);
-      const float sa = ka[grp] * scale_log2, sbb = kb[grp] * scale_log2;
-      s[0] = fmaf(acc[0], sa, s[0]);
-      s[1] = fmaf(acc[1], sa, s[1]);
-      s[2] = fmaf(acc[2], sbb, s[2]);
-      s[3] = fmaf(acc[3], sbb, s[3]);
+      s[0] = fmaf(acc[0], ka[grp], s[0]);
+      s[1] = fmaf(acc[1], ka[grp], s[1]);
+      s[2] = fmaf(acc[2], kb[grp], s[2]);
+      s[3] = fmaf(acc[3], kb[grp], s[3]);
     }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s[k] *= scale_log2;   // the softmax scale, once
   } else {
     const int q4 = lane >> 3, rr = lane & 7;
     const int tok = warp * 16 + rho(rr) + 8 * (q4 & 1);
