@@ -381,14 +381,19 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
         af[3] = sub1152(lop_i8pair(wB[ii] >> 8));
         ptx::mma_f16(acc, af, qf[mc * 4 + ii][0], qf[mc * 4 + ii][1]);
       }
+      // the softmax scale: with a group per macro, once on the sums below;
+      // otherwise folded into each group's scale (fewer multiplies either way)
       const int grp = mc / (MACROS / NG);
-      s[0] = fmaf(acc[0], ka[grp], s[0]);
-      s[1] = fmaf(acc[1], ka[grp], s[1]);
-      s[2] = fmaf(acc[2], kb[grp], s[2]);
-      s[3] = fmaf(acc[3], kb[grp], s[3]);
+      const float sa = NG == MACROS ? ka[grp] : ka[grp] * scale_log2;
+      const float sbb = NG == MACROS ? kb[grp] : kb[grp] * scale_log2;
+      s[0] = fmaf(acc[0], sa, s[0]);
+      s[1] = fmaf(acc[1], sa, s[1]);
+      s[2] = fmaf(acc[2], sbb, s[2]);
+      s[3] = fmaf(acc[3], sbb, s[3]);
     }
+    if constexpr (NG == MACROS)
 #pragma unroll
-    for (int k = 0; k < 4; ++k) s[k] *= scale_log2;   // the softmax scale, once
+      for (int k = 0; k < 4; ++k) s[k] *= scale_log2;
   } else {
     const int q4 = lane >> 3, rr = lane & 7;
     const int tok = warp * 16 + rho(rr) + 8 * (q4 & 1);
@@ -606,17 +611,25 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
     return;
   }
 
-  // ---- P.V per V group: P' = p * w as an f16 hi + lo pair (p split once, the
-  // group's factor w -- exact in fp16: an fp16 scale times a power of two, below
-  // 2^6 -- applied in half precision), transposed into the B fragment
-  uint32_t pha, pla, phb, plb;   // p of tokens A and B (heads 2t, 2t + 1), fp16 hi + lo
-  mma::split_pair(pr[0], pr[1], pha, pla);
-  mma::split_pair(pr[2], pr[3], phb, plb);
+  // ---- P.V per V group: P' = p * w as an f16 hi + lo pair, transposed into the
+  // B fragment.  Several groups: p is split once and each group's factor w
+  // (exact in fp16: an fp16 scale times a power of two, below 2^6) applied in
+  // half precision; one group: P' formed in fp32 and split.
+  uint32_t pha = 0, pla = 0, phb = 0, plb = 0;   // p of tokens A and B (heads 2t, 2t + 1)
+  if constexpr (NGV > 1) {
+    mma::split_pair(pr[0], pr[1], pha, pla);
+    mma::split_pair(pr[2], pr[3], phb, plb);
+  }
 #pragma unroll
   for (int g = 0; g < NGV; ++g) {
     uint32_t h01, e01, h23, e23;
-    mma::weight_pair(pha, pla, ptx::pack_f16x2(wa[g], wa[g]), h01, e01);
-    mma::weight_pair(phb, plb, ptx::pack_f16x2(wb[g], wb[g]), h23, e23);
+    if constexpr (NGV > 1) {
+      mma::weight_pair(pha, pla, ptx::pack_f16x2(wa[g], wa[g]), h01, e01);
+      mma::weight_pair(phb, plb, ptx::pack_f16x2(wb[g], wb[g]), h23, e23);
+    } else {
+      mma::weight_pair_f32(pr[0], pr[1], wa[0], h01, e01);
+      mma::weight_pair_f32(pr[2], pr[3], wb[0], h23, e23);
+    }
     const uint32_t bh0 = ptx::movmatrix_trans(h01), bh1 = ptx::movmatrix_trans(h23);
     const uint32_t bl0 = ptx::movmatrix_trans(e01), bl1 = ptx::movmatrix_trans(e23);
 #pragma unroll

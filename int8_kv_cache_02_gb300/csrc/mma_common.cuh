@@ -70,6 +70,17 @@ __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uin
   lo = ptx::pack_f16x2(p0 - h0, p1 - h1);
 }
 
+// The same pair formed directly (one factor w for both): P' = p * w in fp32,
+// hi = fl16(P'), lo = fl16(P' - hi).  Fewer operations than split_pair followed by
+// weight_pair when a tile has a single V group.
+__device__ __forceinline__ void weight_pair_f32(float p0, float p1, float w, uint32_t& hi,
+                                                uint32_t& lo) {
+  const float w0 = p0 * w, w1 = p1 * w;
+  hi = ptx::pack_f16x2(w0, w1);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  lo = ptx::pack_f16x2(w0 - f.x, w1 - f.y);
+}
+
 // The P.V weights P' = p * s of two keys (p as the hi + lo pairs of split_pair, s
 // an fp16 factor per key) as a new fp16 hi + lo pair, in half-precision
 // arithmetic: hi = fl(ph s); ph s - hi, an 11-bit by 11-bit product less its
