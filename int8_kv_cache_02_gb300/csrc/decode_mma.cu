@@ -79,6 +79,16 @@ constexpr int kMaxCluster = 8;             // splits reduced together through DS
 constexpr int kThreads = kConsumerWarps * 32;
 constexpr float kTau = 8.f;                // lazy rescale: the running max moves when exceeded by > 2^8
 constexpr int kPShift = 6;                 // P' fed to the MMA as P' * 2^(6 - e) < 2^8 * 2^6 = 2^14
+
+// With several V groups a tile splits its softmax weights into fp16 hi + lo once
+// and scales them per group in half precision (mma::weight_pair).  The weights are
+// split as p * 2^5 (at most 2^13 under the lazy max; an exact scaling) and the
+// group factors carry 2^-5 (below 2^1), so that weights down to 2^-19 of the
+// reference and V scales down to 2^-15 of the group's range stay normal in fp16.
+template <int D, bool VI8, int NG, bool VQ4>
+__host__ __device__ constexpr int weight_shift() {
+  return (VQ4 ? D / 32 : (VI8 ? NG : 1)) > 1 ? 5 : 0;
+}
 constexpr int kPagesCached = 256;          // page ids of a block's range kept in shared memory
 constexpr float kCap0 = 1.17549435e-38f;   // smallest normal float: below every nonzero fp16 scale
 using mma::kPage;
@@ -447,6 +457,7 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
     m0 = mn0;
     m1 = mn1;
   }
+  constexpr int KPS = weight_shift<D, VI8, NG, VQ4>();
   const float base0 = m0 == -INFINITY ? 0.f : m0, base1 = m1 == -INFINITY ? 0.f : m1;
   float pr[4];
   pr[0] = ptx::ex2(s[0] - base0);
@@ -456,8 +467,9 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
   l0 += pr[0] + pr[2];
   l1 += pr[1] + pr[3];
 
-  // ---- token weights per V group: s_v * 2^(kPShift - e_g), the range 2^e_g raised
-  // (and the group's accumulators rescaled) when a larger V scale shows up
+  // ---- token weights per V group: s_v * 2^(kPShift - e_g) (times 2^-5 where the
+  // weights are split first, see weight_shift), the range 2^e_g raised (and the
+  // group's accumulators rescaled) when a larger V scale shows up
   float wa[NGV], wb[NGV];
   if constexpr (VI8) {
     float va[NG], vb[NG];
@@ -499,7 +511,7 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
           }
           vexp[g] = ne;
           cap[g] = pow2f(ne);
-          sh[g] = pow2f(kPShift - ne);
+          sh[g] = pow2f(kPShift - KPS - ne);
         }
       }
     }
@@ -554,7 +566,7 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
         }
         vexp[0] = ne;
         cap[0] = pow2f(ne);
-        sh[0] = pow2f(kPShift - ne);
+        sh[0] = pow2f(kPShift - KPS - ne);
       }
     }
 #pragma unroll
@@ -578,9 +590,9 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       qv[j] = *reinterpret_cast<const uint4*>(sb + LY::V_OFF + tk[j] * 128 + ((r ^ (tk[j] & 7)) << 4));
-    uint32_t pha, pla, phb, plb;   // p of tokens A and B (heads 2t, 2t + 1), fp16 hi + lo
-    mma::split_pair(pr[0], pr[1], pha, pla);
-    mma::split_pair(pr[2], pr[3], phb, plb);
+    uint32_t pha, pla, phb, plb;   // p * 2^5 of tokens A and B (heads 2t, 2t + 1), fp16 hi + lo
+    mma::split_pair(pr[0] * (1 << KPS), pr[1] * (1 << KPS), pha, pla);
+    mma::split_pair(pr[2] * (1 << KPS), pr[3] * (1 << KPS), phb, plb);
 #pragma unroll
     for (int g = 0; g < NGV; ++g) {
       uint32_t h01, e01, h23, e23;
@@ -616,9 +628,9 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
   // (exact in fp16: an fp16 scale times a power of two, below 2^6) applied in
   // half precision; one group: P' formed in fp32 and split.
   uint32_t pha = 0, pla = 0, phb = 0, plb = 0;   // p of tokens A and B (heads 2t, 2t + 1)
-  if constexpr (NGV > 1) {
-    mma::split_pair(pr[0], pr[1], pha, pla);
-    mma::split_pair(pr[2], pr[3], phb, plb);
+  if constexpr (NGV > 1) {   // split as p * 2^5
+    mma::split_pair(pr[0] * (1 << KPS), pr[1] * (1 << KPS), pha, pla);
+    mma::split_pair(pr[2] * (1 << KPS), pr[3] * (1 << KPS), phb, plb);
   }
 #pragma unroll
   for (int g = 0; g < NGV; ++g) {
@@ -985,7 +997,8 @@ decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
   float o[MTILES][4];
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   int vexp[NG];      // per V group: 2^vexp > every V scale this warp has seen
-  float cap[NG], sh[NG];   // 2^vexp and 2^(kPShift - vexp); kCap0 and 0 before the first scale
+  float cap[NG], sh[NG];   // 2^vexp and 2^(kPShift - weight_shift - vexp); kCap0 and 0 before
+                           // the first scale
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     vexp[g] = INT_MIN;

@@ -60,7 +60,7 @@ __device__ __forceinline__ int exponent_of(float x) {   // floor(log2 x), x > 0 
   return (int)((__float_as_uint(x) >> 23) & 0xFF) - 127;
 }
 
-// Softmax weights p0, p1 >= 0 (at most 2^8) as fp16 hi + lo pairs: hi keeps each
+// Softmax weights p0, p1 >= 0 (at most 2^15) as fp16 hi + lo pairs: hi keeps each
 // weight's 11 leading bits (its 13 low mantissa bits cleared: exact in fp16 from
 // 2^-14 up), lo the remainder rounded to fp16.
 __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uint32_t& lo) {
@@ -85,7 +85,9 @@ __device__ __forceinline__ void weight_pair_f32(float p0, float p1, float w, uin
 // an fp16 factor per key) as a new fp16 hi + lo pair, in half-precision
 // arithmetic: hi = fl(ph s); ph s - hi, an 11-bit by 11-bit product less its
 // rounding to 11 bits, is exact in fp16 outside the subnormal range, so
-// lo = fl(pl s + (ph s - hi)) leaves P' within ~2^-21 of p * s.
+// lo = fl(pl s + (ph s - hi)) leaves P' within ~2^-21 of p * s.  Exact only
+// while p and s are normal in fp16 (callers split p scaled up by 2^5 and scale s
+// down by as much).
 __device__ __forceinline__ void weight_pair(uint32_t ph, uint32_t pl, uint32_t s, uint32_t& hi,
                                             uint32_t& lo) {
   const __half2 a = *reinterpret_cast<const __half2*>(&ph);

@@ -60,6 +60,10 @@ constexpr int kChunks = 4 / kParts;   // 16-key chunks per thread
 constexpr int kNS = 2;                // stages of the page ring
 constexpr float kTau = 8.f;           // lazy rescale threshold (log2 units)
 constexpr int kPShift = 6;            // P' < 2^8 * 2^6 in fp16
+constexpr int kPSplit = 5;            // p split into fp16 hi + lo as p * 2^5 (<= 2^13), the P.V
+                                      // factors carrying 2^-5: weights down to 2^-19 of the
+                                      // reference and V scales down to 2^-15 of the group's
+                                      // range stay normal
 
 template <int D, bool KI8, bool VI8, int NG>
 struct TLayout {
@@ -457,14 +461,15 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
             tmem_scale(tbase + lane_off + LY::OB + c_lo, c_hi - c_lo, pow2f(vexp[g] - ne));
           vexp[g] = ne;
           cap[g] = pow2f(ne);
-          sh[g] = pow2f(kPShift - ne);
+          sh[g] = pow2f(kPShift - kPSplit - ne);
         }
       } else {
-        sh[g] = pow2f(kPShift);
+        sh[g] = pow2f(kPShift - kPSplit);
       }
     }
     // the table of P.V factors, fp16 [group][key]: the V scale times the group's
-    // range shift (exact: below 2^6), 0 for keys outside [j0, j1)
+    // range shift 2^(kPShift - kPSplit - e_g) (below 2^1: exact unless subnormal),
+    // 0 for keys outside [j0, j1)
     if constexpr (VI8)
       if (tid < kPage * NG) {
         const int g = tid / kPage, k = tid % kPage;
@@ -553,7 +558,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
     for (int cc = 0; cc < kChunks; ++cc)
 #pragma unroll
       for (int k2 = 0; k2 < 8; ++k2)
-        mma::split_pair(sv[cc][2 * k2], sv[cc][2 * k2 + 1], ph[cc][k2], pl[cc][k2]);
+        mma::split_pair(sv[cc][2 * k2] * (1 << kPSplit), sv[cc][2 * k2 + 1] * (1 << kPSplit),
+                        ph[cc][k2], pl[cc][k2]);
     const uint4* vsf = reinterpret_cast<const uint4*>(smem + LY::VSF_OFF);
 #pragma unroll
     for (int g = 0; g < NGV; ++g)
@@ -567,7 +573,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
           f[4] = x1.x; f[5] = x1.y; f[6] = x1.z; f[7] = x1.w;
         } else {
 #pragma unroll
-          for (int k2 = 0; k2 < 8; ++k2) f[k2] = (uint32_t)(kPShift + 15) * 0x04000400u;   // 2^kPShift
+          for (int k2 = 0; k2 < 8; ++k2)
+            f[k2] = (uint32_t)(kPShift - kPSplit + 15) * 0x04000400u;   // 2^(kPShift - kPSplit)
         }
         uint32_t v[16];
 #pragma unroll

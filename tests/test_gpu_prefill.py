@@ -22,10 +22,13 @@ def _lib():
 
 
 def _run(seed, H, Hkv, D, gs, start, n_new, variant, n_splits=0, outliers=True, scale=0.0,
-         spare=2):
+         spare=2, v=None):
+    """v: the sequence's V rows [start + n_new][Hkv][D] (fp16) instead of random ones."""
     from int8_kv_cache_02_gb300 import binding
     L = start + n_new
     q_all, ks, vs = inputs.random_case(seed, n_new, H, Hkv, D, [L], outliers=outliers)
+    if v is not None:
+        vs = [v]
     q = q_all                                                   # [n_new][H][D]
     pt, n_pages = inputs.page_table([L], 64, n_pages_total=-(-L // 64) + spare, seed=seed)
     dev, orc = gu.make_pools(1, Hkv, D, gs, 64, n_pages, variant)
@@ -80,6 +83,32 @@ def test_prefill_rows_agree_with_decode_at_their_length():
     torch.cuda.synchronize()
     assert np.max(np.abs(dec.cpu().numpy() - out)) <= 2e-5
     gu.assert_attention_close(out, ref, "prefill")
+
+
+@pytest.mark.parametrize("vmag", [3e-6, 1e-3, 3e2, 6e4])
+def test_prefill_value_magnitudes(vmag):
+    """V from 3e-6 (fp16 subnormal scales of one or two units of 2^-24) to 6e4 (near
+    fp16's largest value): the V range shift keeps the P.V factors and weights
+    normal in fp16.  (Much smaller V rounds most groups' scales to zero; an output
+    then made only of keys weighted below 2^-19 of the reference key is beyond
+    the fp16 weight pairs' range.)"""
+    start, n_new, Hkv, D = 600, 40, 2, 256
+    g = torch.Generator().manual_seed(int(vmag * 1e6) % 1000 + 7)
+    v = (torch.randn((start + n_new, Hkv, D), generator=g) * vmag).clamp(-65000, 65000)
+    out, ref, *_ = _run(61, 16, Hkv, D, 64, start, n_new, 0, 3, v=v.to(torch.float16))
+    gu.assert_attention_close(out / vmag, ref / vmag, f"vmag {vmag}")
+
+
+def test_prefill_v_scales_growing_along_the_sequence():
+    """V scales spanning 2^20 across positions, rising and falling, so that every
+    group's power-of-two range is raised many times within a block's keys."""
+    start, n_new, Hkv, D = 960, 64, 2, 256
+    g = torch.Generator().manual_seed(78)
+    ramp = torch.pow(2.0, torch.linspace(-12, 8, start + n_new)).roll(300)
+    v = torch.randn((start + n_new, Hkv, D), generator=g) * ramp[:, None, None]
+    for ns in (1, 4):
+        out, ref, *_ = _run(62, 16, Hkv, D, 64, start, n_new, 0, ns, v=v.to(torch.float16))
+        gu.assert_attention_close(out, ref, f"ramp ns {ns}")
 
 
 def test_prefill_softmax_scale_override():
