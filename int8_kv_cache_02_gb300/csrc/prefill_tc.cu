@@ -60,10 +60,11 @@ constexpr int kChunks = 4 / kParts;   // 16-key chunks per thread
 constexpr int kNS = 2;                // stages of the page ring
 constexpr float kTau = 8.f;           // lazy rescale threshold (log2 units)
 constexpr int kPShift = 6;            // P' < 2^8 * 2^6 in fp16
-constexpr int kPSplit = 5;            // p split into fp16 hi + lo as p * 2^5 (<= 2^13), the P.V
-                                      // factors carrying 2^-5: weights down to 2^-19 of the
-                                      // reference and V scales down to 2^-15 of the group's
-                                      // range stay normal
+constexpr int kPSplit = 5;            // weights formed as p * 2^5 (<= 2^13; the exponent's base
+                                      // lowered by 5, the row sums dropping the 2^5 at the end)
+                                      // and split into fp16 hi + lo, the P.V factors carrying
+                                      // 2^-5: weights down to 2^-19 of the reference and V
+                                      // scales down to 2^-15 of the group's range stay normal
 
 template <int D, bool KI8, bool VI8, int NG>
 struct TLayout {
@@ -542,12 +543,12 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
     }
     if (__any_sync(0xffffffffu, need && o_live && al != 1.f))
       tmem_scale(tbase + lane_off + LY::OB + half * (D / kParts), D / kParts, al);
-    const float base = m == -INFINITY ? 0.f : m;
+    const float base = (m == -INFINITY ? 0.f : m) - kPSplit;   // p * 2^kPSplit below
 #pragma unroll
     for (int cc = 0; cc < kChunks; ++cc)
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        sv[cc][k] = ptx::ex2(sv[cc][k] - base);   // now p
+        sv[cc][k] = ptx::ex2(sv[cc][k] - base);   // now p * 2^kPSplit
         l += sv[cc][k];                           // this part's share of the row sum
       }
     // P'_g = p * factor(key, g) as fp16 hi | lo for chunk c, over the S columns of
@@ -558,8 +559,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
     for (int cc = 0; cc < kChunks; ++cc)
 #pragma unroll
       for (int k2 = 0; k2 < 8; ++k2)
-        mma::split_pair(sv[cc][2 * k2] * (1 << kPSplit), sv[cc][2 * k2 + 1] * (1 << kPSplit),
-                        ph[cc][k2], pl[cc][k2]);
+        mma::split_pair(sv[cc][2 * k2], sv[cc][2 * k2 + 1], ph[cc][k2], pl[cc][k2]);
     const uint4* vsf = reinterpret_cast<const uint4*>(smem + LY::VSF_OFF);
 #pragma unroll
     for (int g = 0; g < NGV; ++g)
@@ -622,6 +622,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmk,
   l = 0.f;
 #pragma unroll
   for (int q = 0; q < kParts; ++q) l += s_mx[q][R];
+  l *= 1.f / (1 << kPSplit);   // the row sum of p
   const bool wr = pos < a.n_new;
   const size_t h = (size_t)pos * a.H + (size_t)kvh * G + R % G;
   const int S = a.n_splits;
