@@ -624,9 +624,9 @@ __device__ __forceinline__ void decode_tile(const unsigned char* sb, int warp, i
   }
 
   // ---- P.V per V group: P' = p * w as an f16 hi + lo pair, transposed into the
-  // B fragment.  Several groups: p is split once and each group's factor w
-  // (exact in fp16: an fp16 scale times a power of two, below 2^6) applied in
-  // half precision; one group: P' formed in fp32 and split.
+  // B fragment.  Several groups: p * 2^5 is split once and each group's factor
+  // w * 2^-5 (an fp16 scale times a power of two, below 2^1: exact in fp16 unless
+  // subnormal) applied in half precision; one group: P' formed in fp32 and split.
   uint32_t pha = 0, pla = 0, phb = 0, plb = 0;   // p of tokens A and B (heads 2t, 2t + 1)
   if constexpr (NGV > 1) {   // split as p * 2^5
     mma::split_pair(pr[0] * (1 << KPS), pr[1] * (1 << KPS), pha, pla);
