@@ -60,9 +60,9 @@ __device__ __forceinline__ int exponent_of(float x) {   // floor(log2 x), x > 0 
   return (int)((__float_as_uint(x) >> 23) & 0xFF) - 127;
 }
 
-// Softmax weights p0, p1 >= 0 (at most 2^15) as fp16 hi + lo pairs: hi keeps each
-// weight's 11 leading bits (its 13 low mantissa bits cleared: exact in fp16 from
-// 2^-14 up), lo the remainder rounded to fp16.
+// Softmax weights p0, p1 >= 0 (below 2^16; the kernels pass p * 2^5 <= 2^13) as
+// fp16 hi + lo pairs: hi keeps each weight's 11 leading bits (its 13 low mantissa
+// bits cleared: exact in fp16 from 2^-14 up), lo the remainder rounded to fp16.
 __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uint32_t& lo) {
   const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
   const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
